@@ -1,0 +1,270 @@
+"""Seeded synthetic workloads for the quantized KV-cache write and the top-k gather decode.
+
+This module only draws inputs. It holds none of the method's arithmetic (no quantisation,
+no scale rule, no attention): it returns bf16 bit patterns for K, V and q, slot mappings
+and top-k index lists, drawn from numpy's PCG64 generator in a fixed order. The CPU oracle
+and the CUDA path both consume exactly what it returns.
+
+Draw order inside one workload (one ``np.random.default_rng(seed)`` stream):
+pool K, pool V, outlier choice, slot permutation, q, top-k lists, then any extra
+per-step tensors. Normals are float32 standard normals, scaled (outliers) in float32 and
+rounded to bf16 with round-to-nearest-even. Config 3's layers each use their own stream,
+``default_rng([seed, layer])``.
+
+Workload shapes follow the page workloads:
+* int8 per-(token,head) KV cache for the Qwen3.8-Flash-Next QSA path, §The finding worth
+  upstreaming: 2048 query rows gathering top-k 1024 scattered slots; one KV head of
+  head_dim 256 (256 B of int8 data per head).
+* [Model][SM70][FP8] Add calibrated E4M3 QSA KV cache / [Perf][SM70][FP8] Hoist QSA E4M3 KV
+  scales, §Test plan / §Changes: 24 per-layer scalars (12 layers x K,V); a long top-k 2051
+  split-K shape.
+* SuperPUPS/Qwen3.8-Flash-Next-INT8KV, §What it buys you: MTP k=4 decode (5 query
+  positions per sequence).
+"""
+
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+HEAD_DIM = 256
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even) and return the uint16 bits.
+
+    Inputs are finite by construction here, so no NaN handling is needed.
+    """
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    r = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+@dataclasses.dataclass
+class Workload:
+    """One synthetic problem: tokens written into a slot pool, then query rows gathering it."""
+
+    name: str
+    seed: int
+    num_slots: int
+    num_kv_heads: int
+    num_q_heads: int
+    head_dim: int
+    k_tokens: np.ndarray  # uint16 bf16 bits [T, Hkv, D]
+    v_tokens: np.ndarray  # uint16 bf16 bits [T, Hkv, D]
+    slot_mapping: np.ndarray  # int64 [T], token -> slot, -1 = skip
+    q: np.ndarray  # uint16 bf16 bits [R, Hq, D]
+    topk: np.ndarray  # int32 [R, k], slot ids, -1 = padding
+    softmax_scale: float
+    num_splits: int = 1
+    # Per-step write of new tokens (decode step): bf16 bits [Tn, Hkv, D] and slots [Tn].
+    step_k: Optional[np.ndarray] = None
+    step_v: Optional[np.ndarray] = None
+    step_slots: Optional[np.ndarray] = None
+    notes: str = ""
+
+    @property
+    def rows(self) -> int:
+        return int(self.topk.shape[0])
+
+    @property
+    def topk_len(self) -> int:
+        return int(self.topk.shape[1])
+
+
+def _normals(rng: np.random.Generator, shape, chunk_rows: int = 65536) -> np.ndarray:
+    """float32 standard normals drawn in row chunks (same stream as one big draw)."""
+    out = np.empty(shape, dtype=np.float32)
+    flat = out.reshape(shape[0], -1)
+    for a in range(0, shape[0], chunk_rows):
+        b = min(shape[0], a + chunk_rows)
+        flat[a:b] = rng.standard_normal((b - a, flat.shape[1]), dtype=np.float32)
+    return out
+
+
+def _distinct_rows(rng: np.random.Generator, rows: int, population: int, k: int) -> np.ndarray:
+    """`rows` lists of `k` distinct integers uniform over [0, population), unsorted."""
+    out = np.empty((rows, k), dtype=np.int64)
+    for r in range(rows):
+        out[r] = rng.choice(population, size=k, replace=False)
+    return out
+
+
+def _scaled_bf16(base: np.ndarray, factor: np.ndarray) -> np.ndarray:
+    """Multiply token vectors by per-token factors in float32, then round to bf16 bits."""
+    return f32_to_bf16_bits(base * factor.reshape((-1,) + (1,) * (base.ndim - 1)))
+
+
+def tiny(seed: int = 0) -> Workload:
+    """Tiny int8 sparse decode: 4096 slots, GQA 8, 16 rows x top-k 64, every 64th token x20."""
+    S, H, D, G, R, K = 4096, 1, HEAD_DIM, 8, 16, 64
+    rng = np.random.default_rng(seed)
+    k = _normals(rng, (S, H, D))
+    v = _normals(rng, (S, H, D))
+    factor = np.ones(S, dtype=np.float32)
+    factor[np.arange(S) % 64 == 0] = np.float32(20.0)
+    slot_mapping = rng.permutation(S).astype(np.int64)
+    q = f32_to_bf16_bits(_normals(rng, (R, H * G, D)))
+    topk = _distinct_rows(rng, R, S, K).astype(np.int32)
+    return Workload("tiny int8 sparse decode (S=4096, G=8, R=16, k=64)", seed, S, H, H * G, D,
+                    _scaled_bf16(k, factor), _scaled_bf16(v, factor), slot_mapping, q, topk,
+                    softmax_scale=1.0 / 16.0, num_splits=1)
+
+
+def page1_shape(seed: int = 1, rows: int = 2048, topk: int = 1024, num_slots: int = 262144,
+                with_step: bool = True) -> Workload:
+    """2048 rows x top-k 1024 over a 262144-slot pool, G=16, 1% outlier tokens x16.
+
+    With `with_step`, also draws one decode step's worth of new tokens (one per row) and
+    distinct destination slots for them.
+    """
+    S, H, D, G = num_slots, 1, HEAD_DIM, 16
+    rng = np.random.default_rng(seed)
+    k = _normals(rng, (S, H, D))
+    v = _normals(rng, (S, H, D))
+    n_out = int(round(0.01 * S))
+    outliers = rng.choice(S, size=n_out, replace=False)
+    factor = np.ones(S, dtype=np.float32)
+    factor[outliers] = np.float32(16.0)
+    slot_mapping = rng.permutation(S).astype(np.int64)
+    q = f32_to_bf16_bits(_normals(rng, (rows, H * G, D)))
+    idx = _distinct_rows(rng, rows, S, topk).astype(np.int32)
+    wl = Workload(f"page-1 shape (S={S}, G=16, R={rows}, k={topk})", seed, S, H, H * G, D,
+                  _scaled_bf16(k, factor), _scaled_bf16(v, factor), slot_mapping, q, idx,
+                  softmax_scale=1.0 / 16.0, num_splits=1)
+    if with_step:
+        wl.step_k = f32_to_bf16_bits(_normals(rng, (rows, H, D)))
+        wl.step_v = f32_to_bf16_bits(_normals(rng, (rows, H, D)))
+        wl.step_slots = rng.choice(S, size=rows, replace=False).astype(np.int64)
+    return wl
+
+
+def e4m3_splitk_layer(layer: int, seed: int = 2, rows: int = 64, topk: int = 2051,
+                      num_slots: int = 131072, num_splits: int = 8) -> Workload:
+    """One of 12 layers: its own 131072-slot pool and q; 64 rows x top-k 2051, 8 K-splits."""
+    S, H, D, G = num_slots, 1, HEAD_DIM, 16
+    rng = np.random.default_rng([seed, layer])
+    k = f32_to_bf16_bits(_normals(rng, (S, H, D)))
+    v = f32_to_bf16_bits(_normals(rng, (S, H, D)))
+    slot_mapping = rng.permutation(S).astype(np.int64)
+    q = f32_to_bf16_bits(_normals(rng, (rows, H * G, D)))
+    idx = _distinct_rows(rng, rows, S, topk).astype(np.int32)
+    return Workload(f"calibrated E4M3 split-K layer {layer} (S={S}, R={rows}, k={topk}, P={num_splits})",
+                    seed, S, H, H * G, D, k, v, slot_mapping, q, idx,
+                    softmax_scale=1.0 / 16.0, num_splits=num_splits)
+
+
+E4M3_SPLITK_LAYERS = 12
+
+
+def long_context_decode(seed: int = 3, num_seqs: int = 8, context: int = 131072, block: int = 16,
+                        rows_per_seq: int = 5, topk: int = 2048, recent: int = 4096,
+                        recent_picks: int = 1536, num_splits: int = 16) -> Workload:
+    """8 sequences x 131072 tokens in a paged pool (blocks of 16, randomly permuted).
+
+    Each sequence has 5 query rows (MTP k=4); each row draws 1536 distinct positions from
+    the sequence's last 4096 tokens and 512 distinct positions from the rest. Positions
+    map to physical slots through the permuted block table here, so the kernel takes slot ids.
+    """
+    H, D, G = 1, HEAD_DIM, 16
+    n_blocks_seq = context // block
+    total_blocks = num_seqs * n_blocks_seq
+    S = total_blocks * block
+    rng = np.random.default_rng(seed)
+    k = f32_to_bf16_bits(_normals(rng, (S, H, D)))
+    v = f32_to_bf16_bits(_normals(rng, (S, H, D)))
+    block_perm = rng.permutation(total_blocks).astype(np.int64)
+    # token (b, pos) is token index b*context + pos; its slot via the block table
+    pos = np.arange(context, dtype=np.int64)
+    slot_mapping = np.empty(S, dtype=np.int64)
+    for b in range(num_seqs):
+        phys = block_perm[b * n_blocks_seq + pos // block]
+        slot_mapping[b * context:(b + 1) * context] = phys * block + pos % block
+    R = num_seqs * rows_per_seq
+    q = f32_to_bf16_bits(_normals(rng, (R, H * G, D)))
+    idx = np.empty((R, topk), dtype=np.int32)
+    older = context - recent
+    for b in range(num_seqs):
+        base = b * context
+        for j in range(rows_per_seq):
+            r = b * rows_per_seq + j
+            near = older + rng.choice(recent, size=recent_picks, replace=False)
+            far = rng.choice(older, size=topk - recent_picks, replace=False)
+            positions = np.concatenate([near, far])
+            idx[r] = slot_mapping[base + positions]
+    return Workload(f"long-context decode (8 x {context} ctx, paged blocks of {block}, R={R}, k={topk})",
+                    seed, S, H, H * G, D, k, v, slot_mapping, q, idx,
+                    softmax_scale=1.0 / 16.0, num_splits=num_splits,
+                    notes="block table applied in the generator; kernel sees slot ids")
+
+
+def chunked_prefill(seed: int = 4, new_tokens: int = 8192, num_slots: int = 524288,
+                    topk: int = 1024) -> Workload:
+    """8192 new tokens scattered into a 524288-slot pool; row i attends min(1024, i) positions < i.
+
+    Row 0 has no valid index (all -1). Padding entries are -1.
+    """
+    H, D, G = 1, HEAD_DIM, 16
+    T, S = new_tokens, num_slots
+    rng = np.random.default_rng(seed)
+    k = f32_to_bf16_bits(_normals(rng, (T, H, D)))
+    v = f32_to_bf16_bits(_normals(rng, (T, H, D)))
+    slot_mapping = rng.choice(S, size=T, replace=False).astype(np.int64)
+    q = f32_to_bf16_bits(_normals(rng, (T, H * G, D)))
+    idx = np.full((T, topk), -1, dtype=np.int32)
+    for i in range(1, T):
+        n = min(topk, i)
+        positions = rng.choice(i, size=n, replace=False)
+        idx[i, :n] = slot_mapping[positions]
+    return Workload(f"chunked-prefill write + causal sparse attention (T={T}, S={S}, k={topk})",
+                    seed, S, H, H * G, D, k, v, slot_mapping, q, idx,
+                    softmax_scale=1.0 / 16.0, num_splits=1)
+
+
+def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: int = 16,
+                 num_kv_heads: int = 1, pad_frac: float = 0.0, outlier_frac: float = 0.0,
+                 outlier_factor: float = 16.0, num_tokens: Optional[int] = None,
+                 num_splits: int = 1, softmax_scale: float = 1.0 / 16.0,
+                 zero_tokens: int = 0) -> Workload:
+    """Generic small case for parity tests: ragged top-k, -1 padding, optional outliers.
+
+    `zero_tokens` tokens (chosen after the outliers) get all-zero K and V vectors, the
+    degenerate absmax = 0 case.
+    """
+    S, H, D = num_slots, num_kv_heads, HEAD_DIM
+    T = S if num_tokens is None else num_tokens
+    rng = np.random.default_rng(seed)
+    k = _normals(rng, (T, H, D))
+    v = _normals(rng, (T, H, D))
+    factor = np.ones(T, dtype=np.float32)
+    n_out = int(round(outlier_frac * T))
+    if n_out:
+        factor[rng.choice(T, size=n_out, replace=False)] = np.float32(outlier_factor)
+    if zero_tokens:
+        factor[rng.choice(T, size=zero_tokens, replace=False)] = np.float32(0.0)
+    slot_mapping = rng.choice(S, size=T, replace=False).astype(np.int64)
+    q = f32_to_bf16_bits(_normals(rng, (rows, num_q_heads, D)))
+    written = slot_mapping
+    kk = min(topk, T)
+    idx = np.full((rows, topk), -1, dtype=np.int32)
+    for r in range(rows):
+        picks = written[rng.choice(T, size=kk, replace=False)]
+        if pad_frac > 0:
+            drop = rng.random(kk) < pad_frac
+            picks = np.where(drop, -1, picks)
+        idx[r, :kk] = picks
+    return Workload(f"small random (S={S}, T={T}, R={rows}, k={topk}, Hq={num_q_heads}, Hkv={H})",
+                    seed, S, H, num_q_heads, D, _scaled_bf16(k, factor), _scaled_bf16(v, factor),
+                    slot_mapping, q, idx, softmax_scale=softmax_scale, num_splits=num_splits)
+
+
+CONFIGS = {
+    1: tiny,
+    2: page1_shape,
+    3: e4m3_splitk_layer,
+    4: long_context_decode,
+    5: chunked_prefill,
+}

@@ -1,0 +1,63 @@
+"""The seeded generator: determinism and the structure each workload promises (CPU only)."""
+
+import numpy as np
+
+from gen import chunked_prefill, f32_to_bf16_bits, long_context_decode, small_random, tiny
+
+
+def test_bf16_rounding_is_nearest_even():
+    x = np.float32([1.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -9, -2.5])
+    bits = f32_to_bf16_bits(x)
+    # 1+2^-8 is a tie between 1 and 1+2^-7: even mantissa -> 1.0; 1+3*2^-8 -> 1+2^-6
+    assert bits.tolist() == [0x3F80, 0x3F80, 0x3F82, 0x3F80, 0xC020]
+
+
+def test_deterministic_and_distinct():
+    a, b = tiny(0), tiny(0)
+    for f in ("k_tokens", "v_tokens", "slot_mapping", "q", "topk"):
+        assert np.array_equal(getattr(a, f), getattr(b, f))
+    assert sorted(a.slot_mapping.tolist()) == list(range(4096))
+    for r in range(a.rows):
+        assert len(set(a.topk[r].tolist())) == a.topk_len
+    # every 64th token is an outlier (x20)
+    k = (a.k_tokens.astype(np.uint32) << 16).view(np.float32)
+    big = np.abs(k).max(axis=(1, 2))
+    assert np.median(big[::64]) > 10 * np.median(big[1::64])
+
+
+def test_chunked_prefill_is_causal_and_padded():
+    wl = chunked_prefill(seed=4, new_tokens=300, num_slots=4096, topk=64)
+    pos_of_slot = {int(s): t for t, s in enumerate(wl.slot_mapping)}
+    assert np.all(wl.topk[0] == -1)
+    for i in range(1, 300):
+        n = min(64, i)
+        row = wl.topk[i]
+        assert np.all(row[n:] == -1)
+        pos = [pos_of_slot[int(s)] for s in row[:n]]
+        assert len(set(pos)) == n and max(pos) < i
+
+
+def test_long_context_split_recent_and_far():
+    wl = long_context_decode(seed=3, num_seqs=2, context=8192, block=16, rows_per_seq=5,
+                             topk=256, recent=1024, recent_picks=192)
+    assert len(np.unique(wl.slot_mapping)) == wl.num_slots
+    inv = np.empty(wl.num_slots, dtype=np.int64)
+    inv[wl.slot_mapping] = np.arange(wl.num_slots)
+    for r in range(wl.rows):
+        seq = r // 5
+        tok = inv[wl.topk[r]]
+        assert np.all(tok // 8192 == seq)
+        pos = tok % 8192
+        assert len(set(pos.tolist())) == 256
+        assert np.sum(pos >= 8192 - 1024) == 192
+    # slots inside a block are contiguous
+    assert np.all(np.diff(wl.slot_mapping[:16]) == 1)
+
+
+def test_small_random_padding_and_zero_tokens():
+    wl = small_random(1, num_slots=100, rows=5, topk=40, pad_frac=0.5, zero_tokens=3, num_tokens=60)
+    assert np.any(wl.topk == -1)
+    valid = wl.topk[wl.topk >= 0]
+    assert set(valid.tolist()) <= set(wl.slot_mapping.tolist())
+    # zero factor keeps the sign of negative draws: -0.0 is a zero too
+    assert np.sum(np.all((wl.k_tokens & 0x7FFF) == 0, axis=(1, 2))) == 3
