@@ -37,10 +37,14 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
     Inputs are finite by construction here, so no NaN handling is needed.
     """
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
-    lsb = (u >> np.uint32(16)) & np.uint32(1)
-    r = (u + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
-    return r.astype(np.uint16)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).reshape(-1)
+    out = np.empty(u.shape, dtype=np.uint16)
+    step = 1 << 20  # chunked so the temporaries stay in cache
+    for a in range(0, u.size, step):
+        c = u[a:a + step]
+        lsb = (c >> np.uint32(16)) & np.uint32(1)
+        out[a:a + step] = (c + np.uint32(0x7FFF) + lsb) >> np.uint32(16)
+    return out.reshape(np.shape(x))
 
 
 @dataclasses.dataclass
@@ -86,10 +90,27 @@ def _normals(rng: np.random.Generator, shape, chunk_rows: int = 65536) -> np.nda
 
 
 def _distinct_rows(rng: np.random.Generator, rows: int, population: int, k: int) -> np.ndarray:
-    """`rows` lists of `k` distinct integers uniform over [0, population), unsorted."""
+    """`rows` lists of `k` distinct integers uniform over [0, population), in random order.
+
+    Each row keeps the first k distinct values of an i.i.d. uniform integer stream, which is
+    a uniformly random k-subset in uniformly random order. Streams are drawn 2k at a time
+    per row; a row that is still short draws again. For k > population / 4 a permutation is
+    used instead.
+    """
     out = np.empty((rows, k), dtype=np.int64)
+    if k * 4 > population:
+        for r in range(rows):
+            out[r] = rng.permutation(population)[:k]
+        return out
+    draws = rng.integers(0, population, size=(rows, 2 * k), dtype=np.int64)
     for r in range(rows):
-        out[r] = rng.choice(population, size=k, replace=False)
+        seq = draws[r]
+        while True:
+            _, first = np.unique(seq, return_index=True)
+            if first.size >= k:
+                out[r] = seq[np.sort(first)[:k]]
+                break
+            seq = np.concatenate([seq, rng.integers(0, population, size=2 * k, dtype=np.int64)])
     return out
 
 

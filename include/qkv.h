@@ -1,0 +1,169 @@
+/*
+ * qkv.h -- C ABI of libqkv.so: quantize-on-write into a KV slot pool and the top-k
+ * gather decode attention over it, hand-written for sm_103a (GB300).
+ *
+ * Pages cited (by title):
+ *   [INT8-PR]  "int8 per-(token,head) KV cache for the Qwen3.8-Flash-Next QSA path"
+ *   [INT8-KV]  "SuperPUPS/Qwen3.8-Flash-Next-INT8KV" (INT8 KV build, int8_per_token_head)
+ *   [E4M3-PR]  "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache"
+ *   [HOIST-PR] "[Perf][SM70][FP8] Hoist QSA E4M3 KV scales"
+ *   [SCALES]   "Qwen3.8 Flash Next NVFP4 QSA FP8 E4M3 KV Scales" (model card)
+ *
+ * Conventions shared by every call
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the library never
+ *     allocates, frees or synchronises. Work is enqueued on `stream` (a cudaStream_t passed
+ *     as void*; NULL = the legacy default stream) and the call returns before it runs.
+ *   - Arguments are validated on the host before any launch; an invalid call returns an
+ *     error status and enqueues nothing. A launch failure returns QKV_ERR_CUDA.
+ *   - Data-dependent problems found on the device (an out-of-range slot or index) are never
+ *     trapped: the offending entry is skipped and a bit is OR-ed into the optional
+ *     caller-provided device word `dev_status` (may be NULL).
+ *   - head_dim must be 256 (256 B of int8 data per head, [INT8-PR §The finding worth
+ *     upstreaming]); num_q_heads / num_kv_heads (the GQA group) must be 1..16.
+ *   - Pool layouts, S = num_slots, H = num_kv_heads, D = head_dim:
+ *       QKV_BF16        K, V: bf16 [S, H, D]
+ *       QKV_INT8_SIDE   K, V: int8 [S, H, D]; k_scale, v_scale: fp32 [S, H] (side tensors)
+ *       QKV_INT8_INLINE K, V: bytes [S, H, D + 4]: D int8 codes then the fp32 scale,
+ *                       little-endian (the 260 B record of [INT8-PR])
+ *       QKV_E4M3        K, V: E4M3 bytes [S, H, D]; one fp32 K and one fp32 V scale per layer
+ */
+#ifndef QKV_H
+#define QKV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QKV_OK = 0,
+  QKV_ERR_ARG = 1,         /* null pointer, negative size, bad enum, unsupported shape mix */
+  QKV_ERR_SCALE = 2,       /* a per-layer scale that is not finite or is <= 0 */
+  QKV_ERR_UNSUPPORTED = 3, /* head_dim != 256 or GQA group outside 1..16 */
+  QKV_ERR_ALIGN = 4,       /* a base pointer or stride breaks the required alignment */
+  QKV_ERR_CUDA = 5         /* a kernel launch or attribute call failed */
+} qkv_status;
+
+typedef enum {
+  QKV_BF16 = 0,
+  QKV_INT8_SIDE = 1,
+  QKV_INT8_INLINE = 2,
+  QKV_E4M3 = 3
+} qkv_format;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define QKV_DEV_BAD_SLOT 1u  /* slot_mapping entry >= num_slots or < -1: that token is skipped */
+#define QKV_DEV_BAD_INDEX 2u /* top-k entry >= num_slots or < -1: treated as padding (-1) */
+
+/*
+ * qkv_write_int8 -- quantize new K/V tokens to int8 with one absmax scale per (token, head)
+ * and store them at their slots.            [INT8-PR §The finding worth upstreaming; INT8-KV]
+ *
+ *   For each token t, KV head h, tensor X in {K, V}:
+ *     amax = max_d |x_d| (bf16 widened to fp32), scale = amax / 127 (fp32 IEEE division),
+ *     c_d = clamp(rint(x_d / scale), -127, 127) with ties to even; amax == 0 stores scale 0
+ *     and zero codes. Codes and scale go to slot slot_mapping[t]; -1 skips the token.
+ *
+ *   k, v          bf16 [num_tokens, num_kv_heads, head_dim]; token t starts at element
+ *                 t * token_stride (token_stride >= num_kv_heads*head_dim, a multiple of 8);
+ *                 base pointers 16-byte aligned.
+ *   slot_mapping  int64 [num_tokens]. Slots must be distinct (duplicates race).
+ *   layout        QKV_INT8_SIDE: k_cache/v_cache int8 [S,H,D] (16 B-aligned) and
+ *                 k_scale/v_scale fp32 [S,H];
+ *                 QKV_INT8_INLINE: k_cache/v_cache bytes [S,H,D+4] (4 B-aligned), scale
+ *                 pointers must be NULL.
+ *   num_slots     S; slots outside [0, S) set QKV_DEV_BAD_SLOT and are skipped.
+ * Stored bytes are bit-identical to the CPU oracle's.
+ */
+qkv_status qkv_write_int8(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                          int head_dim, int64_t token_stride, const int64_t* slot_mapping,
+                          qkv_format layout, void* k_cache, void* v_cache, float* k_scale,
+                          float* v_scale, int64_t num_slots, uint32_t* dev_status,
+                          void* stream);
+
+/*
+ * qkv_write_e4m3 -- quantize new K/V tokens to FP8 E4M3 with calibrated per-layer scales.
+ *                                 [SCALES §Calibration; E4M3-PR §Implementation scope]
+ *   stored = e4m3fn(x / scale): the fp32 IEEE quotient rounded to the nearest E4M3 value,
+ *   ties to even, magnitudes above 448 saturated to 448, sign kept (-0 -> 0x80).
+ *   k_scale, v_scale must be finite and > 0, else QKV_ERR_SCALE (the fail-closed gate of
+ *   [E4M3-PR §Non-obvious design decisions]; 1.0 is a legal value).
+ *   k, v, token_stride, slot_mapping, num_slots, dev_status as for qkv_write_int8;
+ *   k_cache, v_cache: E4M3 bytes [S, H, D], 16 B-aligned.
+ */
+qkv_status qkv_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                          int head_dim, int64_t token_stride, const int64_t* slot_mapping,
+                          void* k_cache, void* v_cache, float k_scale, float v_scale,
+                          int64_t num_slots, uint32_t* dev_status, void* stream);
+
+/*
+ * qkv_e4m3_calibrate -- per-tensor calibrated E4M3 scale = (max |x|) / 448 over n bf16
+ * values, computed on the device.                             [SCALES §Calibration]
+ *   x          bf16 [n], 16 B-aligned.
+ *   amax_bits  device uint32 [1]: scratch that receives the fp32 bits of max|x| (the call
+ *              clears it first with a memset on `stream`).
+ *   scale_out  device fp32 [1]: amax / 448 (fp32 IEEE division). 0 when every x is 0.
+ */
+qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out,
+                              void* stream);
+
+/*
+ * qsa_gather_attn -- top-k gather decode attention over a quantized slot pool.
+ *                       [INT8-PR §The finding worth upstreaming; HOIST-PR §Changes]
+ *   For row r, query head g (KV head g / G, G = num_q_heads / num_kv_heads) and the valid
+ *   entries j of topk_idx[r, :] (-1 = padding):
+ *     s_j = softmax_scale * q[r,g,:] . K_j,   o = sum_j softmax(s)_j V_j,
+ *     lse = log sum_j exp(s_j)  (natural log; a row with no valid entry gives o = 0,
+ *     lse = -inf). K_j / V_j are the dequantized slots: int8 c * per-(slot,head) scale,
+ *     E4M3 dec(c) * per-layer scale, or bf16 values.
+ *   Scale hoisting: the K scale multiplies the dot product, not each element (per slot for
+ *   int8, folded into the softmax factor for E4M3); the int8 V scale multiplies p_j; the
+ *   E4M3 V scale is applied once after normalisation -- or, when num_splits > 1, left to
+ *   qsa_splitk_merge (pass v_scale_layer as its v_scale_post).
+ *
+ *   q             bf16 [rows, num_q_heads, head_dim], contiguous, 16 B-aligned.
+ *   fmt           pool layout (see above). k_cache / v_cache 16 B-aligned (INLINE: 4 B).
+ *   k_scale_tok, v_scale_tok  fp32 [S, H] for QKV_INT8_SIDE, else must be NULL.
+ *   k_scale_layer, v_scale_layer  per-layer scales for QKV_E4M3 (finite, > 0, else
+ *                 QKV_ERR_SCALE); ignored for the other formats.
+ *   topk_idx      int32 [rows, topk] slot ids, -1 = padding; entries outside [-1, S) set
+ *                 QKV_DEV_BAD_INDEX and are treated as padding. Duplicates count twice.
+ *   softmax_scale finite.
+ *   num_splits    P >= 1. Split s covers index columns [s*c, min(topk, (s+1)*c)),
+ *                 c = ceil(topk / P) ([E4M3-PR §Implementation scope]: split-K workspace).
+ *   P == 1: out fp32 [rows, num_q_heads, head_dim] and optional lse fp32 [rows, num_q_heads]
+ *           (NULL to skip); o_part / lse_part must be NULL.
+ *   P > 1:  o_part fp32 [rows, P, num_q_heads, head_dim] and lse_part fp32
+ *           [rows, P, num_q_heads] receive the normalised per-split partials (E4M3: without
+ *           the V scale); out / lse must be NULL; follow with qsa_splitk_merge.
+ */
+qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                           int head_dim, qkv_format fmt, const void* k_cache,
+                           const void* v_cache, const float* k_scale_tok,
+                           const float* v_scale_tok, float k_scale_layer, float v_scale_layer,
+                           int64_t num_slots, const int32_t* topk_idx, int topk,
+                           float softmax_scale, int num_splits, float* out, float* lse,
+                           float* o_part, float* lse_part, uint32_t* dev_status, void* stream);
+
+/*
+ * qsa_splitk_merge -- merge split-K partials.      [HOIST-PR §Changes: the V scale is
+ *                                                    applied once after the merge]
+ *   lse = log sum_s exp(lse_s), o = v_scale_post * sum_s exp(lse_s - lse) o_s.
+ *   Rows whose splits are all empty (lse_s = -inf) give o = 0, lse = -inf.
+ *   o_part fp32 [rows, P, num_q_heads, head_dim], lse_part fp32 [rows, P, num_q_heads],
+ *   out fp32 [rows, num_q_heads, head_dim], lse fp32 [rows, num_q_heads] or NULL.
+ *   v_scale_post finite (1.0 for the non-E4M3 formats). head_dim must be 256.
+ */
+qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
+                            int num_q_heads, int head_dim, int num_splits, float v_scale_post,
+                            float* out, float* lse, void* stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+const char* qkv_status_str(qkv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKV_H */

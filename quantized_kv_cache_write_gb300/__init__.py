@@ -1,0 +1,131 @@
+"""Thin Python binding of libqkv.so (quantize-on-write KV cache + top-k gather decode, sm_103a).
+
+Argument marshalling only: every function takes torch tensors that already live on the GPU,
+passes their device pointers, sizes and the current CUDA stream to the C entry point of
+the same name declared in include/qkv.h, and raises QKVError on a non-OK status. All
+arithmetic runs in the library's CUDA kernels; there is no fallback path. Importing this
+package fails loudly if libqkv.so has not been built
+(``python -m quantized_kv_cache_write_gb300.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqkv.so")
+
+QKV_OK, QKV_ERR_ARG, QKV_ERR_SCALE, QKV_ERR_UNSUPPORTED, QKV_ERR_ALIGN, QKV_ERR_CUDA = range(6)
+QKV_BF16, QKV_INT8_SIDE, QKV_INT8_INLINE, QKV_E4M3 = range(4)
+QKV_DEV_BAD_SLOT = 1
+QKV_DEV_BAD_INDEX = 2
+HEAD_DIM = 256
+FORMATS = {"bf16": QKV_BF16, "int8_side": QKV_INT8_SIDE, "int8_inline": QKV_INT8_INLINE, "e4m3": QKV_E4M3}
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m quantized_kv_cache_write_gb300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+_SIGS = {
+    "qkv_write_int8": [_p, _p, _i64, _i32, _i32, _i64, _p, _i32, _p, _p, _p, _p, _i64, _p, _p],
+    "qkv_write_e4m3": [_p, _p, _i64, _i32, _i32, _i64, _p, _p, _p, _f32, _f32, _i64, _p, _p],
+    "qkv_e4m3_calibrate": [_p, _i64, _p, _p, _p],
+    "qsa_gather_attn": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
+                        _i32, _p, _p, _p, _p, _p, _p],
+    "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = ctypes.c_int
+lib.qkv_status_str.argtypes = [ctypes.c_int]
+lib.qkv_status_str.restype = ctypes.c_char_p
+
+
+class QKVError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {lib.qkv_status_str(status).decode()} (status {status})")
+
+
+def status_str(status: int) -> str:
+    return lib.qkv_status_str(status).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(fn: str, status: int):
+    if status != QKV_OK:
+        raise QKVError(fn, status)
+
+
+def _tokens(k: torch.Tensor, v: torch.Tensor):
+    """[T, Hkv, D] views sharing one token stride; heads and dims contiguous."""
+    if k.dim() != 3 or k.shape != v.shape or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("k and v must be bf16 [num_tokens, num_kv_heads, head_dim] of equal shape")
+    if k.stride(2) != 1 or k.stride(1) != k.shape[2] or v.stride()[1:] != k.stride()[1:] or k.stride(0) != v.stride(0):
+        raise ValueError("k and v need contiguous heads and one shared token stride")
+    return k.shape[0], k.shape[1], k.shape[2], k.stride(0)
+
+
+def qkv_write_int8(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None, *,
+                   layout: int = QKV_INT8_SIDE, dev_status=None, stream=None):
+    """int8 per-(token, head) quantize-on-write (side scales or inline 260 B records)."""
+    T, H, D, stride = _tokens(k, v)
+    st = lib.qkv_write_int8(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), layout, _ptr(k_cache),
+                            _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), k_cache.shape[0], _ptr(dev_status),
+                            _stream(stream))
+    _check("qkv_write_int8", st)
+
+
+def qkv_write_e4m3(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: float, *,
+                   dev_status=None, stream=None):
+    """FP8 E4M3 quantize-on-write with calibrated per-layer scales."""
+    T, H, D, stride = _tokens(k, v)
+    st = lib.qkv_write_e4m3(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+                            float(k_scale), float(v_scale), k_cache.shape[0], _ptr(dev_status), _stream(stream))
+    _check("qkv_write_e4m3", st)
+
+
+def qkv_e4m3_calibrate(x, amax_bits, scale_out, *, stream=None):
+    """Device amax/448 over a bf16 tensor; result in scale_out[0] (fp32)."""
+    st = lib.qkv_e4m3_calibrate(_ptr(x), x.numel(), _ptr(amax_bits), _ptr(scale_out), _stream(stream))
+    _check("qkv_e4m3_calibrate", st)
+
+
+def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: float, *, num_kv_heads: int = 1,
+                    num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
+                    k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, num_splits: int = 1, out=None,
+                    lse=None, o_part=None, lse_part=None, dev_status=None, stream=None):
+    """Top-k gather decode attention. q bf16 [R, Hq, D]; topk_idx int32 [R, k]."""
+    R, Hq, D = q.shape
+    S = k_cache.shape[0] if num_slots is None else num_slots
+    topk = topk_idx.shape[1] if topk_idx is not None else 0
+    st = lib.qsa_gather_attn(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
+                             _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer), float(v_scale_layer), S,
+                             _ptr(topk_idx), topk, float(softmax_scale), num_splits, _ptr(out), _ptr(lse),
+                             _ptr(o_part), _ptr(lse_part), _ptr(dev_status), _stream(stream))
+    _check("qsa_gather_attn", st)
+
+
+def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1.0, stream=None):
+    """Merge split-K partials o_part [R, P, Hq, D], lse_part [R, P, Hq] into out [R, Hq, D]."""
+    R, P, Hq, D = o_part.shape
+    st = lib.qsa_splitk_merge(_ptr(o_part), _ptr(lse_part), R, Hq, D, P, float(v_scale_post), _ptr(out), _ptr(lse),
+                              _stream(stream))
+    _check("qsa_splitk_merge", st)

@@ -1,0 +1,165 @@
+// extern "C" entry points of libqkv.so: host-side validation, then one launch each on the
+// caller's stream. Nothing here allocates, frees or synchronises. The declarations, with
+// argument meaning, layout, ownership and error behaviour, are in qkv.h.
+#include <cmath>
+#include <cstdint>
+
+#include "qkv_internal.cuh"
+
+namespace {
+
+using qkv::kHeadDim;
+using qkv::kMaxGroup;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool finite_positive(float s) { return std::isfinite(s) && s > 0.f; }
+qkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QKV_OK : QKV_ERR_CUDA; }
+
+// Shared checks of the two write calls' token inputs.
+qkv_status check_write_inputs(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                              int head_dim, int64_t token_stride, const int64_t* slot_mapping,
+                              const void* k_cache, const void* v_cache, int64_t num_slots) {
+  if (num_tokens < 0 || num_slots < 0 || num_kv_heads < 1) return QKV_ERR_ARG;
+  if (head_dim != kHeadDim) return QKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return QKV_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return QKV_ERR_ARG;
+  if (token_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return QKV_ERR_ARG;
+  if (token_stride % 8 != 0 || !aligned(k, 16) || !aligned(v, 16)) return QKV_ERR_ALIGN;
+  if (!aligned(slot_mapping, 8)) return QKV_ERR_ALIGN;
+  return QKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qkv_status_str(qkv_status s) {
+  switch (s) {
+    case QKV_OK: return "ok";
+    case QKV_ERR_ARG: return "invalid argument";
+    case QKV_ERR_SCALE: return "per-layer scale is not finite and positive";
+    case QKV_ERR_UNSUPPORTED: return "unsupported head_dim or GQA group";
+    case QKV_ERR_ALIGN: return "pointer or stride misaligned";
+    case QKV_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+qkv_status qkv_write_int8(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
+                          int64_t token_stride, const int64_t* slot_mapping, qkv_format layout, void* k_cache,
+                          void* v_cache, float* k_scale, float* v_scale, int64_t num_slots, uint32_t* dev_status,
+                          void* stream) {
+  qkv_status st = check_write_inputs(k, v, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping,
+                                     k_cache, v_cache, num_slots);
+  if (st != QKV_OK) return st;
+  if (layout != QKV_INT8_SIDE && layout != QKV_INT8_INLINE) return QKV_ERR_ARG;
+  const bool inl = layout == QKV_INT8_INLINE;
+  if (inl && (k_scale || v_scale)) return QKV_ERR_ARG;
+  if (num_tokens == 0) return QKV_OK;
+  if (!inl && (!k_scale || !v_scale)) return QKV_ERR_ARG;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
+  if (!inl && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return QKV_ERR_ALIGN;
+  if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
+  return cuda_status(qkv::launch_write_int8(k, v, num_tokens, num_kv_heads, token_stride, slot_mapping, inl,
+                                            k_cache, v_cache, k_scale, v_scale, num_slots, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+qkv_status qkv_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
+                          int64_t token_stride, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                          float k_scale, float v_scale, int64_t num_slots, uint32_t* dev_status, void* stream) {
+  qkv_status st = check_write_inputs(k, v, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping,
+                                     k_cache, v_cache, num_slots);
+  if (st != QKV_OK) return st;
+  if (!finite_positive(k_scale) || !finite_positive(v_scale)) return QKV_ERR_SCALE;
+  if (num_tokens == 0) return QKV_OK;
+  if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
+  if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
+  return cuda_status(qkv::launch_write_e4m3(k, v, num_tokens, num_kv_heads, token_stride, slot_mapping, k_cache,
+                                            v_cache, k_scale, v_scale, num_slots, dev_status,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out, void* stream) {
+  if (n < 0 || !amax_bits || !scale_out || (n > 0 && !x)) return QKV_ERR_ARG;
+  if (n > 0 && !aligned(x, 16)) return QKV_ERR_ALIGN;
+  if (!aligned(amax_bits, 4) || !aligned(scale_out, 4)) return QKV_ERR_ALIGN;
+  return cuda_status(qkv::launch_e4m3_calibrate(x, n, amax_bits, scale_out, static_cast<cudaStream_t>(stream)));
+}
+
+qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
+                           qkv_format fmt, const void* k_cache, const void* v_cache, const float* k_scale_tok,
+                           const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
+                           const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
+                           float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream) {
+  if (rows < 0 || topk < 0 || num_splits < 1 || num_slots < 0) return QKV_ERR_ARG;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return QKV_ERR_ARG;
+  if (head_dim != kHeadDim || num_q_heads / num_kv_heads > kMaxGroup) return QKV_ERR_UNSUPPORTED;
+  if (fmt != QKV_BF16 && fmt != QKV_INT8_SIDE && fmt != QKV_INT8_INLINE && fmt != QKV_E4M3) return QKV_ERR_ARG;
+  if (!std::isfinite(softmax_scale)) return QKV_ERR_ARG;
+  if (fmt == QKV_E4M3 && (!finite_positive(k_scale_layer) || !finite_positive(v_scale_layer)))
+    return QKV_ERR_SCALE;
+  const bool side = fmt == QKV_INT8_SIDE;
+  if (side != (k_scale_tok != nullptr) || side != (v_scale_tok != nullptr)) return QKV_ERR_ARG;
+  if (num_splits == 1) {
+    if (!out || o_part || lse_part) return QKV_ERR_ARG;
+  } else {
+    if (out || lse || !o_part || !lse_part) return QKV_ERR_ARG;
+  }
+  if (static_cast<int64_t>(topk) + num_splits > INT32_MAX) return QKV_ERR_ARG;
+  if (rows * num_kv_heads * static_cast<int64_t>(num_splits) > INT32_MAX) return QKV_ERR_ARG;
+  if (rows == 0) return QKV_OK;
+  if (!q || !k_cache || !v_cache || (topk > 0 && !topk_idx)) return QKV_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
+  if (topk_idx && !aligned(topk_idx, 4)) return QKV_ERR_ALIGN;
+  if (side && (!aligned(k_scale_tok, 4) || !aligned(v_scale_tok, 4))) return QKV_ERR_ALIGN;
+  if ((out && !aligned(out, 16)) || (o_part && !aligned(o_part, 16))) return QKV_ERR_ALIGN;
+  if ((lse && !aligned(lse, 4)) || (lse_part && !aligned(lse_part, 4))) return QKV_ERR_ALIGN;
+  if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
+
+  qkv::GatherArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k_cache = static_cast<const uint8_t*>(k_cache);
+  a.v_cache = static_cast<const uint8_t*>(v_cache);
+  a.k_scale_tok = k_scale_tok;
+  a.v_scale_tok = v_scale_tok;
+  a.k_scale_layer = k_scale_layer;
+  a.v_scale_layer = v_scale_layer;
+  a.num_slots = num_slots;
+  a.topk_idx = topk_idx;
+  a.rows = rows;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.topk = topk;
+  a.num_splits = num_splits;
+  a.softmax_scale = softmax_scale;
+  a.out = out;
+  a.lse = lse;
+  a.o_part = o_part;
+  a.lse_part = lse_part;
+  a.dev_status = dev_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  switch (fmt) {
+    case QKV_BF16: return cuda_status(qkv::launch_gather_bf16(a, s));
+    case QKV_INT8_SIDE: return cuda_status(qkv::launch_gather_int8_side(a, s));
+    case QKV_INT8_INLINE: return cuda_status(qkv::launch_gather_int8_inline(a, s));
+    case QKV_E4M3: return cuda_status(qkv::launch_gather_e4m3(a, s));
+  }
+  return QKV_ERR_ARG;
+}
+
+qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows, int num_q_heads,
+                            int head_dim, int num_splits, float v_scale_post, float* out, float* lse,
+                            void* stream) {
+  if (rows < 0 || num_q_heads < 1 || num_splits < 1) return QKV_ERR_ARG;
+  if (head_dim != kHeadDim) return QKV_ERR_UNSUPPORTED;
+  if (!std::isfinite(v_scale_post)) return QKV_ERR_ARG;
+  if (rows == 0) return QKV_OK;
+  if (!o_part || !lse_part || !out) return QKV_ERR_ARG;
+  if (!aligned(o_part, 16) || !aligned(out, 16) || !aligned(lse_part, 4) || (lse && !aligned(lse, 4)))
+    return QKV_ERR_ALIGN;
+  return cuda_status(qkv::launch_splitk_merge(o_part, lse_part, rows, num_q_heads, num_splits, v_scale_post, out,
+                                              lse, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+// Internal device helpers and launcher declarations for libqkv.so (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qkv.h"
+
+namespace qkv {
+
+constexpr int kHeadDim = 256;
+constexpr int kMaxGroup = 16;
+constexpr int kInlineRecord = kHeadDim + 4;  // 256 code bytes + fp32 scale
+
+// ------------------------------------------------------------------ launchers
+cudaError_t launch_write_int8(const void* k, const void* v, int64_t num_tokens, int num_heads,
+                              int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
+                              void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                              int64_t num_slots, uint32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_heads,
+                              int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
+                              void* v_cache, float k_scale, float v_scale, int64_t num_slots,
+                              uint32_t* dev_status, cudaStream_t stream);
+cudaError_t launch_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out,
+                                  cudaStream_t stream);
+cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
+                                int num_q_heads, int num_splits, float v_scale_post, float* out,
+                                float* lse, cudaStream_t stream);
+
+// Arguments of one gather-attention launch (already validated on the host).
+struct GatherArgs {
+  const __nv_bfloat16* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale_tok;
+  const float* v_scale_tok;
+  float k_scale_layer;
+  float v_scale_layer;
+  int64_t num_slots;
+  const int32_t* topk_idx;
+  int64_t rows;
+  int num_q_heads;
+  int num_kv_heads;
+  int topk;
+  int num_splits;
+  float softmax_scale;
+  float* out;       // [rows, Hq, D] when num_splits == 1
+  float* lse;       // [rows, Hq] or null
+  float* o_part;    // [rows, P, Hq, D] when num_splits > 1
+  float* lse_part;  // [rows, P, Hq]
+  uint32_t* dev_status;
+};
+
+cudaError_t launch_gather_bf16(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_int8_side(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_int8_inline(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_e4m3(const GatherArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------------ device helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// 16-byte async copy global -> shared; src_bytes < 16 zero-fills the rest (0 reads nothing).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];\n" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];\n" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;\n" ::"r"(addr), "r"(v));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two int8 codes sitting in bytes 0 and 2 of `x` (bytes 1, 3 ignored) -> exact fp16x2.
+// (b ^ 0x80) placed under the fp16 exponent of 1024 gives 1024 + 128 + b; subtracting 1152
+// leaves b exactly (every integer below 2048 is an fp16 value).
+__device__ __forceinline__ uint32_t i8pair_to_f16x2(uint32_t x) {
+  uint32_t y = (x & 0x00FF00FFu) ^ 0x64806480u;
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(y), "r"(0x64806480u));
+  return r;
+}
+
+// Two E4M3 bytes (low byte -> low half) -> exact fp16x2 (native conversion).
+__device__ __forceinline__ uint32_t e4m3pair_to_f16x2(uint32_t x16) {
+  uint32_t r;
+  unsigned short s = static_cast<unsigned short>(x16 & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(s));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+}  // namespace qkv

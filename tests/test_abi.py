@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: libqkv.so builds, exports every function include/qkv.h declares,
+and its host-side validation rejects bad calls before any CUDA work (these calls return
+before the first CUDA API call, so they are safe on a machine with no GPU).
+
+The fail-closed scale gate follows "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache"
+§Non-obvious design decisions: a missing (-1.0 sentinel), non-finite or non-positive
+per-layer scale is an error; 1.0 is a legal value.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._builder().build()
+    import quantized_kv_cache_write_gb300 as q
+    assert q.LIB_PATH == path
+    return q
+
+
+def _declared():
+    text = open(HEADER).read()
+    return re.findall(r"^\s*(?:qkv_status|const char\*)\s+(\w+)\s*\(", text, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"qkv_write_int8", "qkv_write_e4m3", "qsa_gather_attn", "qsa_splitk_merge", "qkv_status_str"} <= set(names)
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.status_str(s)
+    assert lib.status_str(99) == "unknown status"
+
+
+FAKE = 0x10000  # a 64 KiB-aligned fake device address: never dereferenced, the calls fail first
+
+
+def _gather(lib, **over):
+    a = dict(q=FAKE, rows=4, hq=16, hkv=1, d=256, fmt=lib.QKV_INT8_SIDE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE,
+             ksl=1.0, vsl=1.0, S=100, idx=FAKE, topk=8, sm=0.0625, P=1, out=FAKE, lse=None, op=None, lp=None)
+    a.update(over)
+    return lib.lib.qsa_gather_attn(a["q"], a["rows"], a["hq"], a["hkv"], a["d"], a["fmt"], a["kc"], a["vc"], a["ks"],
+                                   a["vs"], a["ksl"], a["vsl"], a["S"], a["idx"], a["topk"], a["sm"], a["P"],
+                                   a["out"], a["lse"], a["op"], a["lp"], None, None)
+
+
+def test_gather_host_validation(lib):
+    E = lib
+    assert _gather(lib, d=128) == E.QKV_ERR_UNSUPPORTED
+    assert _gather(lib, hq=34, hkv=2) == E.QKV_ERR_UNSUPPORTED  # group 17
+    assert _gather(lib, hq=15, hkv=2) == E.QKV_ERR_ARG
+    assert _gather(lib, fmt=7) == E.QKV_ERR_ARG
+    assert _gather(lib, ks=None) == E.QKV_ERR_ARG  # side format needs per-slot scales
+    assert _gather(lib, fmt=E.QKV_E4M3) == E.QKV_ERR_ARG  # ... and the others must not get them
+    assert _gather(lib, P=2) == E.QKV_ERR_ARG  # split needs partial buffers, not out
+    assert _gather(lib, P=0) == E.QKV_ERR_ARG
+    assert _gather(lib, rows=-1) == E.QKV_ERR_ARG
+    assert _gather(lib, sm=float("nan")) == E.QKV_ERR_ARG
+    assert _gather(lib, q=FAKE + 8) == E.QKV_ERR_ALIGN
+    assert _gather(lib, out=FAKE + 4) == E.QKV_ERR_ALIGN
+    assert _gather(lib, rows=0) == E.QKV_OK  # nothing to do, nothing launched
+
+
+@pytest.mark.parametrize("bad", [-1.0, 0.0, float("nan"), float("inf"), -0.0])
+def test_e4m3_scale_gate_fails_closed(lib, bad):
+    E = lib
+    kw = dict(fmt=E.QKV_E4M3, ks=None, vs=None)
+    assert _gather(lib, ksl=bad, **kw) == E.QKV_ERR_SCALE
+    assert _gather(lib, vsl=bad, **kw) == E.QKV_ERR_SCALE
+    st = lib.lib.qkv_write_e4m3(FAKE, FAKE, 3, 1, 256, 256, FAKE, FAKE, FAKE, bad, 1.0, 10, None, None)
+    assert st == E.QKV_ERR_SCALE
+
+
+def test_unit_scale_is_legal(lib):
+    # 1.0 passes the gate; rows=0 keeps the call from launching anything
+    assert _gather(lib, fmt=lib.QKV_E4M3, ks=None, vs=None, ksl=1.0, vsl=1.0, rows=0) == lib.QKV_OK
+
+
+def test_write_host_validation(lib):
+    E, L = lib, lib.lib
+    w8 = lambda **o: L.qkv_write_int8(o.get("k", FAKE), FAKE, o.get("T", 3), 1, o.get("d", 256), o.get("ts", 256),
+                                      FAKE, o.get("layout", E.QKV_INT8_SIDE), FAKE, FAKE, o.get("ks", FAKE),
+                                      o.get("vs", FAKE), 10, None, None)
+    assert w8(d=64) == E.QKV_ERR_UNSUPPORTED
+    assert w8(ts=100) == E.QKV_ERR_ARG  # stride below one token
+    assert w8(ts=260) == E.QKV_ERR_ALIGN
+    assert w8(k=FAKE + 2) == E.QKV_ERR_ALIGN
+    assert w8(layout=E.QKV_E4M3) == E.QKV_ERR_ARG
+    assert w8(layout=E.QKV_INT8_INLINE) == E.QKV_ERR_ARG  # inline must not get scale pointers
+    assert w8(ks=None) == E.QKV_ERR_ARG
+    assert w8(T=-1) == E.QKV_ERR_ARG
+    assert w8(T=0) == E.QKV_OK
+
+
+def test_merge_and_calibrate_host_validation(lib):
+    E, L = lib, lib.lib
+    assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 128, 4, 1.0, FAKE, None, None) == E.QKV_ERR_UNSUPPORTED
+    assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 256, 0, 1.0, FAKE, None, None) == E.QKV_ERR_ARG
+    assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 256, 4, float("inf"), FAKE, None, None) == E.QKV_ERR_ARG
+    assert L.qsa_splitk_merge(FAKE + 4, FAKE, 2, 16, 256, 4, 1.0, FAKE, None, None) == E.QKV_ERR_ALIGN
+    assert L.qsa_splitk_merge(FAKE, FAKE, 0, 16, 256, 4, 1.0, FAKE, None, None) == E.QKV_OK
+    assert L.qkv_e4m3_calibrate(FAKE, -1, FAKE, FAKE, None) == E.QKV_ERR_ARG
+    assert L.qkv_e4m3_calibrate(FAKE + 2, 10, FAKE, FAKE, None) == E.QKV_ERR_ALIGN
