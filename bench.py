@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark of one decode step of the quantized-KV top-k gather path on GB300.
+
+Workload (the page-1 micro-benchmark shape of "int8 per-(token,head) KV cache for the
+Qwen3.8-Flash-Next QSA path", §The finding worth upstreaming): a 262144-slot pool of one
+KV head (head_dim 256) stored as int8 with per-(token,head) scales in side tensors, 16
+query heads, 2048 query rows each gathering top-k = 1024 distinct uniform slots. Inputs
+are seeded synthetic data (gen.page1_shape, seed 1).
+
+One step = the whole hot path over one batch: quantize-on-write of the step's 2048 new
+tokens (qkv_write_int8), then the gather decode attention of the 2048 rows
+(qsa_gather_attn; the split-K merge runs too when --splits > 1). The L2 cache is flushed
+(a 256 MiB write) between timed steps, outside the timed events.
+
+Metric: gathered-KV GB/s = rows * top-k * (2 * 256 + 2 * 4) bytes per step / step time,
+plus rows/s. The same step through the C ABI with host buffers (pinned host -> device
+copies of q, indices and new tokens; device -> host copy of the output) gives `e2e`.
+`--impl reference` times the CPU oracle on a bounded row sample instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "gathered-KV GB/s (% of GB300 HBM peak) & rows/s, 2048 rows x topk 1024"
+ROWS, TOPK, HEAD_DIM, GROUP = 2048, 1024, 256, 16
+SLOT_BYTES = {"int8_side": 2 * HEAD_DIM + 8, "int8_inline": 2 * (HEAD_DIM + 4), "e4m3": 2 * HEAD_DIM,
+              "bf16": 4 * HEAD_DIM}
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gather_int8_side_page1_traffic.txt")
+KERNEL_SOURCES = ["gather_attn.cuh", "qkv_internal.cuh", "gather_int8_side.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--splits", type=int, default=1, help="K-splits of each row (1 = unsplit)")
+    ap.add_argument("--no-formats", action="store_true", help="skip the per-format side measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-rows", type=int, default=0, help="oracle rows per sample (0 = auto)")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def load_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "quantized_kv_cache_write_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic():
+    """ncu dram bytes per gather launch, if taken on the current kernel source; else None."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 7:
+                continue
+            try:
+                rows.append((float(p[0]), float(p[1]), p[2], p[3], p[4], p[5], float(p[6])))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        loaded = [r for r in rows if r[6] > 0] or rows
+        sm = sorted(r[0] for r in loaded)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in loaded for i in range(4) if r[2 + i].lower() == "active"})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": loaded[0][1], "reasons": reasons,
+                "samples": len(rows), "samples_under_load": len([r for r in rows if r[6] > 0])}
+
+
+# ------------------------------------------------------------------ the oracle arm
+
+def oracle_setup(wl):
+    from oracle import attention as oatt
+    from oracle import quant as oq
+    kc, vc, ks, vs = oq.write_int8(wl.k_tokens, wl.v_tokens, wl.slot_mapping, wl.num_slots, "side")
+    return oatt.int8_side_pool_fp64(kc, ks), oatt.int8_side_pool_fp64(vc, vs)
+
+
+def oracle_step(wl, K, V, rows):
+    """One bounded oracle step: quantize the sampled rows' new tokens, attend the sampled rows."""
+    from oracle import attention as oatt
+    from oracle import quant as oq
+    n = len(rows)
+    oq.int8_quantize(oq.bf16_bits_to_f32(wl.step_k[:n]))
+    oq.int8_quantize(oq.bf16_bits_to_f32(wl.step_v[:n]))
+    oatt.gather_attention(wl.q, K, V, wl.topk, wl.softmax_scale, rows=rows)
+
+
+def time_oracle(wl, K, V, rows, repeats):
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        oracle_step(wl, K, V, rows)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    from gen import page1_shape
+    wl = page1_shape(1)
+    K, V = oracle_setup(wl)
+    n = args.cpu_sample_rows or 64
+    rows = list(range(n))
+    time_oracle(wl, K, V, rows, max(1, args.warmup))
+    times = time_oracle(wl, K, V, rows, max(1, args.steps))
+    sec = sum(times) / len(times)
+    gbs = n * TOPK * SLOT_BYTES["int8_side"] / sec / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"page-1 shape, oracle sample of {n} of 2048 rows", "rows": ROWS, "topk": TOPK,
+                   "num_slots": wl.num_slots, "num_q_heads": GROUP, "num_kv_heads": 1, "head_dim": HEAD_DIM,
+                   "format": "int8_side", "parallelism": "none (CPU oracle)"},
+        "rows_per_s": round(n / sec, 2),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {n} of 2048 rows (and their {n} new tokens) per step, fp64 numpy oracle, "
+                                   f"1 BLAS thread"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ the GPU arm
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    rank, world, local = dist_env()
+    if world > 1 or rank == 0:
+        os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_kv_cache_write_gb300 as q
+    from gen import page1_shape
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev_index = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+
+    # ---- setup (untimed): every rank runs its own page-1 shape problem (weak scaling)
+    wl = page1_shape(1)
+    S, H, D = wl.num_slots, 1, HEAD_DIM
+    bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    k_tok, v_tok = bf(wl.k_tokens), bf(wl.v_tokens)
+    slots_all = torch.from_numpy(wl.slot_mapping).cuda()
+    q_dev = bf(wl.q)
+    idx = torch.from_numpy(wl.topk).cuda()
+    step_k, step_v = bf(wl.step_k), bf(wl.step_v)
+    step_slots = torch.from_numpy(wl.step_slots).cuda()
+    kc = torch.zeros((S, H, D), dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((S, H), dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    q.qkv_write_int8(k_tok, v_tok, slots_all, kc, vc, ks, vs, dev_status=status)
+    P = args.splits
+    out = torch.empty((ROWS, GROUP, D), dtype=torch.float32, device="cuda")
+    o_part = torch.empty((ROWS, P, GROUP, D), dtype=torch.float32, device="cuda") if P > 1 else None
+    lse_part = torch.empty((ROWS, P, GROUP), dtype=torch.float32, device="cuda") if P > 1 else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def gather(qt, it, ot):
+        if P == 1:
+            q.qsa_gather_attn(qt, q.QKV_INT8_SIDE, kc, vc, it, wl.softmax_scale, k_scale_tok=ks, v_scale_tok=vs,
+                              out=ot, dev_status=status)
+        else:
+            q.qsa_gather_attn(qt, q.QKV_INT8_SIDE, kc, vc, it, wl.softmax_scale, k_scale_tok=ks, v_scale_tok=vs,
+                              num_splits=P, o_part=o_part, lse_part=lse_part, dev_status=status)
+            q.qsa_splitk_merge(o_part, lse_part, ot)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        q.qkv_write_int8(step_k, step_v, step_slots, kc, vc, ks, vs, dev_status=status)
+        if ev:
+            ev[1].record(stream)
+        gather(q_dev, idx, out)
+        if ev:
+            ev[2].record(stream)
+
+    launches_per_step = 2 + (1 if P > 1 else 0)
+    for i in range(args.warmup):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev_index)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    gather_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    write_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    ms = sum(step_ms) / len(step_ms)
+    g_ms = sum(gather_ms) / len(gather_ms)
+    if world > 1:
+        t = torch.tensor([ms, g_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, g_ms = t.tolist()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {status.item()} during the benchmark")
+
+    gathered = ROWS * TOPK * SLOT_BYTES["int8_side"]
+    value = world * gathered / (ms * 1e-3) / 1e9
+    rows_per_s = world * ROWS / (ms * 1e-3)
+    peak, peak_src = load_peak()
+    achieved = gathered / (g_ms * 1e-3) / 1e9
+    uniq_slots = int(np.unique(wl.topk).size)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "int8 codes -> fp16 mma, fp32 accumulate", "data": "synthetic",
+        "config": {"workload": "page-1 shape: 2048 rows x top-k 1024 over a 262144-slot int8 pool "
+                               "(side-tensor scales), 1 KV head, 16 query heads, head_dim 256, seed 1",
+                   "rows": ROWS, "topk": TOPK, "num_slots": S, "num_q_heads": GROUP, "num_kv_heads": 1,
+                   "head_dim": HEAD_DIM, "format": "int8_side", "num_splits": P,
+                   "step": "qkv_write_int8 of 2048 new tokens + qsa_gather_attn" + (" + qsa_splitk_merge" if P > 1 else ""),
+                   "l2": "flushed (256 MiB write) between timed steps", "parallelism": f"dp{world} (independent problems)"},
+        "rows_per_s": round(rows_per_s, 1),
+        "frac_of_hbm_peak_total": round(value / (world * peak), 4),
+        "unique_gathered_GBps": round(world * uniq_slots * SLOT_BYTES["int8_side"] / (ms * 1e-3) / 1e9, 2),
+        "write_ms": round(sum(write_ms) / len(write_ms), 5),
+        "gather_ms": round(g_ms, 5),
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": load_traffic(),
+                     "kernel": "gather_attn_kernel<QKV_INT8_SIDE>",
+                     "algorithmic_bytes_per_launch": gathered, "peak_source": peak_src},
+        "wall_s_timed_region": round(t_wall, 3),
+        "pages_context": {"gb10_side_ms": 9.6, "gb10_inline_ms": 60.2,
+                          "note": "one GB10 (sm_121), Triton path; context only"},
+    }
+
+    # ---- end to end through the public API with host buffers
+    pin = lambda t: t.cpu().pin_memory()
+    h_q, h_idx, h_k, h_v, h_slots = pin(q_dev), pin(idx), pin(step_k), pin(step_v), pin(step_slots)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    d_q, d_idx = torch.empty_like(q_dev), torch.empty_like(idx)
+    d_k, d_v, d_slots = torch.empty_like(step_k), torch.empty_like(step_v), torch.empty_like(step_slots)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx, h_k, h_v, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_idx.copy_(h_idx, non_blocking=True)
+        d_k.copy_(h_k, non_blocking=True)
+        d_v.copy_(h_v, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        q.qkv_write_int8(d_k, d_v, d_slots, kc, vc, ks, vs, dev_status=status)
+        gather(d_q, d_idx, out)
+        h_out.copy_(out, non_blocking=True)
+
+    n_e2e = max(3, min(args.steps, 50))
+    for i in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_ms = []
+    for i in range(n_e2e):
+        flush.fill_(float(i))
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms.append(e0.elapsed_time(e1))
+    em = sum(e_ms) / len(e_ms)
+    if world > 1:
+        t = torch.tensor([em], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        em = t.item()
+    result["e2e"] = {"value": round(world * gathered / (em * 1e-3) / 1e9, 2), "unit": "GB/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(em, 4),
+                     "steps": n_e2e}
+
+    # ---- the other formats, same shape (gather alone; context for the side-vs-inline and
+    #      int8-vs-fp8-vs-bf16 comparisons of the pages)
+    if not args.no_formats and rank == 0:
+        result["formats"] = measure_formats(q, wl, q_dev, idx, flush, stream, max(5, min(args.steps, 30)), peak)
+
+    if rank == 0 and not args.no_cpu_baseline:
+        K, V = oracle_setup(wl)
+        n = args.cpu_sample_rows or 64
+        rows = list(range(n))
+        time_oracle(wl, K, V, rows, 1)
+        times = time_oracle(wl, K, V, rows, 3)
+        sec = sum(times) / len(times)
+        result["cpu_baseline"] = {
+            "value": round(n * TOPK * SLOT_BYTES["int8_side"] / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"first {n} of 2048 rows (and their {n} new tokens) per step, mean of 3 steps, fp64 numpy "
+                      f"oracle, 1 BLAS thread; {round(n / sec, 1)} rows/s"}
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+def measure_formats(q, wl, q_dev, idx, flush, stream, steps, peak):
+    import numpy as np
+    import torch
+    S, D = wl.num_slots, HEAD_DIM
+    bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    k_tok, v_tok = bf(wl.k_tokens), bf(wl.v_tokens)
+    slots = torch.from_numpy(wl.slot_mapping).cuda()
+    out = torch.empty((ROWS, GROUP, D), dtype=torch.float32, device="cuda")
+    res = {}
+    for fmt in ("int8_side", "int8_inline", "e4m3", "bf16"):
+        kw = {}
+        if fmt == "int8_side":
+            kc = torch.zeros((S, 1, D), dtype=torch.int8, device="cuda")
+            vc = torch.zeros_like(kc)
+            ks = torch.zeros((S, 1), dtype=torch.float32, device="cuda")
+            vs = torch.zeros_like(ks)
+            q.qkv_write_int8(k_tok, v_tok, slots, kc, vc, ks, vs)
+            kw = dict(k_scale_tok=ks, v_scale_tok=vs)
+        elif fmt == "int8_inline":
+            kc = torch.zeros((S, 1, D + 4), dtype=torch.uint8, device="cuda")
+            vc = torch.zeros_like(kc)
+            q.qkv_write_int8(k_tok, v_tok, slots, kc, vc, layout=q.QKV_INT8_INLINE)
+        elif fmt == "e4m3":
+            amax = torch.zeros(1, dtype=torch.int32, device="cuda")
+            sc = torch.zeros(2, dtype=torch.float32, device="cuda")
+            q.qkv_e4m3_calibrate(k_tok, amax, sc[0:1])
+            q.qkv_e4m3_calibrate(v_tok, amax, sc[1:2])
+            ksl, vsl = sc.tolist()
+            kc = torch.zeros((S, 1, D), dtype=torch.uint8, device="cuda")
+            vc = torch.zeros_like(kc)
+            q.qkv_write_e4m3(k_tok, v_tok, slots, kc, vc, ksl, vsl)
+            kw = dict(k_scale_layer=ksl, v_scale_layer=vsl)
+        else:
+            kc = torch.zeros((S, 1, D), dtype=torch.bfloat16, device="cuda")
+            vc = torch.zeros_like(kc)
+            kc[slots] = k_tok
+            vc[slots] = v_tok
+        code = q.FORMATS[fmt]
+        for i in range(3):
+            q.qsa_gather_attn(q_dev, code, kc, vc, idx, wl.softmax_scale, out=out, **kw)
+        ms = []
+        for i in range(steps):
+            flush.fill_(float(i))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            q.qsa_gather_attn(q_dev, code, kc, vc, idx, wl.softmax_scale, out=out, **kw)
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        m = sum(ms) / len(ms)
+        gbs = ROWS * TOPK * SLOT_BYTES[fmt] / (m * 1e-3) / 1e9
+        res[fmt] = {"gather_ms": round(m, 5), "gathered_GBps": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
+                    "rows_per_s": round(ROWS / (m * 1e-3), 1), "bytes_per_slot": SLOT_BYTES[fmt]}
+        del kc, vc
+        torch.cuda.empty_cache()
+    return res
+
+
+if __name__ == "__main__":
+    main()
