@@ -71,8 +71,8 @@ typedef enum {
  *   slot_mapping  int64 [num_tokens]. Slots must be distinct (duplicates race).
  *   layout        QKV_INT8_SIDE: k_cache/v_cache int8 [S,H,D] (16 B-aligned) and
  *                 k_scale/v_scale fp32 [S,H];
- *                 QKV_INT8_INLINE: k_cache/v_cache bytes [S,H,D+4] (4 B-aligned), scale
- *                 pointers must be NULL.
+ *                 QKV_INT8_INLINE: k_cache/v_cache bytes [S,H,D+4] (16 B-aligned base; the
+ *                 records themselves sit on 4 B boundaries), scale pointers must be NULL.
  *   num_slots     S; slots outside [0, S) set QKV_DEV_BAD_SLOT and are skipped.
  * Stored bytes are bit-identical to the CPU oracle's.
  */
@@ -123,7 +123,7 @@ qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, flo
  *   qsa_splitk_merge (pass v_scale_layer as its v_scale_post).
  *
  *   q             bf16 [rows, num_q_heads, head_dim], contiguous, 16 B-aligned.
- *   fmt           pool layout (see above). k_cache / v_cache 16 B-aligned (INLINE: 4 B).
+ *   fmt           pool layout (see above). k_cache / v_cache base pointers 16 B-aligned.
  *   k_scale_tok, v_scale_tok  fp32 [S, H] for QKV_INT8_SIDE, else must be NULL.
  *   k_scale_layer, v_scale_layer  per-layer scales for QKV_E4M3 (finite, > 0, else
  *                 QKV_ERR_SCALE); ignored for the other formats.
@@ -158,6 +158,42 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
                             int num_q_heads, int head_dim, int num_splits, float v_scale_post,
                             float* out, float* lse, void* stream);
+
+/*
+ * qsa_gather_attn_splitk_noalloc -- qsa_gather_attn with num_splits > 1 followed by
+ * qsa_splitk_merge, for callers that cannot allocate device memory. The pages have no
+ * counterpart: this is a packaging of the two calls above, not a step of the method.
+ *
+ *   Some callers own only their inputs and outputs -- e.g. a plugin inside a host engine
+ *   that receives pre-allocated tensors and may not call cudaMalloc while serving (an
+ *   allocation can synchronise the device and fragments the host's memory pool). They
+ *   cannot supply the o_part / lse_part workspace of a split call. This entry point keeps
+ *   the partials in a file-scope static device array of QKV_NOALLOC_SCRATCH_BYTES instead,
+ *   and calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ *   Arguments are those of qsa_gather_attn, minus o_part / lse_part; out fp32
+ *   [rows, num_q_heads, head_dim] (16 B-aligned) and optional lse fp32 [rows, num_q_heads]
+ *   receive the merged result (E4M3: v_scale_layer applied after the merge). num_splits == 1
+ *   is forwarded to qsa_gather_attn unchanged.
+ *   Limit: rows * num_splits * num_q_heads * (head_dim + 1) * 4 bytes (lse part rounded up to
+ *   256 B) must fit in QKV_NOALLOC_SCRATCH_BYTES (16 MiB: e.g. 64 rows x 8 splits x 16 heads,
+ *   or 40 rows x 16 splits x 16 heads); larger calls return QKV_ERR_ARG and launch nothing.
+ *   Set-up: the first call on each device looks up the array's device address with
+ *   cudaGetSymbolAddress while that device is current; make that first call before any
+ *   stream capture. The array is held by every GPU that loads the library until the process
+ *   exits. All calls share it and it keeps the last call's partials (every partial is
+ *   rewritten before it is read, so nothing needs clearing): calls that overlap on the GPU --
+ *   on different streams or from different host threads -- race and corrupt each other.
+ */
+#define QKV_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+qkv_status qsa_gather_attn_splitk_noalloc(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                                          int head_dim, qkv_format fmt, const void* k_cache,
+                                          const void* v_cache, const float* k_scale_tok,
+                                          const float* v_scale_tok, float k_scale_layer,
+                                          float v_scale_layer, int64_t num_slots,
+                                          const int32_t* topk_idx, int topk, float softmax_scale,
+                                          int num_splits, float* out, float* lse,
+                                          uint32_t* dev_status, void* stream);
 
 /* Static, human-readable name of a status code. Never NULL. */
 const char* qkv_status_str(qkv_status s);

@@ -5,7 +5,7 @@ passes their device pointers, sizes and the current CUDA stream to the C entry p
 the same name declared in include/qkv.h, and raises QKVError on a non-OK status. All
 arithmetic runs in the library's CUDA kernels; there is no fallback path. Importing this
 package fails loudly if libqkv.so has not been built
-(``python -m quantized_kv_cache_write_gb300.build``).
+(``python quantized_kv_cache_write_gb300/build.py``).
 """
 
 from __future__ import annotations
@@ -26,7 +26,7 @@ HEAD_DIM = 256
 FORMATS = {"bf16": QKV_BF16, "int8_side": QKV_INT8_SIDE, "int8_inline": QKV_INT8_INLINE, "e4m3": QKV_E4M3}
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m quantized_kv_cache_write_gb300.build`")
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python quantized_kv_cache_write_gb300/build.py`")
 
 lib = ctypes.CDLL(LIB_PATH)
 
@@ -38,6 +38,8 @@ _SIGS = {
     "qsa_gather_attn": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
                         _i32, _p, _p, _p, _p, _p, _p],
     "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
+    "qsa_gather_attn_splitk_noalloc": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p,
+                                       _i32, _f32, _i32, _p, _p, _p, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -129,3 +131,36 @@ def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1
     st = lib.qsa_splitk_merge(_ptr(o_part), _ptr(lse_part), R, Hq, D, P, float(v_scale_post), _ptr(out), _ptr(lse),
                               _stream(stream))
     _check("qsa_splitk_merge", st)
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024  # QKV_NOALLOC_SCRATCH_BYTES in include/qkv.h
+
+
+def noalloc_scratch_bytes(rows: int, num_splits: int, num_q_heads: int, head_dim: int = HEAD_DIM) -> int:
+    """Bytes of the library's static scratch that a split call of this size needs."""
+    parts = rows * num_splits * num_q_heads
+    return ((parts * head_dim * 4 + 255) // 256) * 256 + parts * 4
+
+
+def qsa_gather_attn_splitk_noalloc(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: float, *,
+                                   num_splits: int, out, lse=None, num_kv_heads: int = 1,
+                                   num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
+                                   k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, dev_status=None,
+                                   stream=None):
+    """Split-K gather + merge with the partials in the library's static device scratch.
+
+    For callers that may not allocate device memory: only inputs and outputs are passed.
+    Calls share one scratch array per GPU, so calls that overlap on the GPU race.
+    """
+    R, Hq, D = q.shape
+    if num_splits > 1 and noalloc_scratch_bytes(R, num_splits, Hq, D) > NOALLOC_SCRATCH_BYTES:
+        raise ValueError(f"{R} rows x {num_splits} splits x {Hq} heads needs "
+                         f"{noalloc_scratch_bytes(R, num_splits, Hq, D)} bytes of partials, more than the "
+                         f"{NOALLOC_SCRATCH_BYTES}-byte static scratch of qsa_gather_attn_splitk_noalloc")
+    S = k_cache.shape[0] if num_slots is None else num_slots
+    topk = topk_idx.shape[1] if topk_idx is not None else 0
+    st = lib.qsa_gather_attn_splitk_noalloc(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer),
+                                            float(v_scale_layer), S, _ptr(topk_idx), topk, float(softmax_scale),
+                                            num_splits, _ptr(out), _ptr(lse), _ptr(dev_status), _stream(stream))
+    _check("qsa_gather_attn_splitk_noalloc", st)

@@ -1,6 +1,9 @@
 """Build libqkv.so in-tree: nvcc for sm_103a only, one object per .cu, compiled in parallel.
 
-    python -m quantized_kv_cache_write_gb300.build [--force] [--ptxas-verbose]
+    python quantized_kv_cache_write_gb300/build.py [--force] [--ptxas-verbose]
+    python -c "import __graft_entry__ as g; g.build()"
+
+(Run it as a file, not with -m: importing the package first would load a stale library.)
 """
 
 from __future__ import annotations
@@ -27,6 +30,7 @@ SOURCES = [
     "gather_int8_inline.cu",
     "gather_e4m3.cu",
     "gather_bf16.cu",
+    "gather_noalloc.cu",
 ]
 HEADERS = ["qkv_internal.cuh", "gather_attn.cuh"]
 
