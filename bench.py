@@ -96,6 +96,22 @@ def load_traffic():
         return None
 
 
+def max_over_ranks(values, device="cpu"):
+    """Elementwise max of per-rank floats (a barrier-synchronised all-reduce; identity at N=1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms_max: float) -> float:
+    """Weak scaling: every rank processes `units_per_rank`; the job takes the slowest rank's time."""
+    return world * units_per_rank / (ms_max * 1e-3)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
 
@@ -290,18 +306,13 @@ def main():
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     gather_ms = [e[1].elapsed_time(e[2]) for e in evs]
     write_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    ms = sum(step_ms) / len(step_ms)
-    g_ms = sum(gather_ms) / len(gather_ms)
-    if world > 1:
-        t = torch.tensor([ms, g_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, g_ms = t.tolist()
+    ms, g_ms = max_over_ranks([sum(step_ms) / len(step_ms), sum(gather_ms) / len(gather_ms)], device="cuda")
     if status.item() != 0:
         raise RuntimeError(f"device status {status.item()} during the benchmark")
 
     gathered = ROWS * TOPK * SLOT_BYTES["int8_side"]
-    value = world * gathered / (ms * 1e-3) / 1e9
-    rows_per_s = world * ROWS / (ms * 1e-3)
+    value = whole_job_rate(gathered, world, ms) / 1e9
+    rows_per_s = whole_job_rate(ROWS, world, ms)
     peak, peak_src = load_peak()
     achieved = gathered / (g_ms * 1e-3) / 1e9
     uniq_slots = int(np.unique(wl.topk).size)
@@ -363,12 +374,8 @@ def main():
         e1.record(stream)
         e1.synchronize()
         e_ms.append(e0.elapsed_time(e1))
-    em = sum(e_ms) / len(e_ms)
-    if world > 1:
-        t = torch.tensor([em], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        em = t.item()
-    result["e2e"] = {"value": round(world * gathered / (em * 1e-3) / 1e9, 2), "unit": "GB/s",
+    em = max_over_ranks([sum(e_ms) / len(e_ms)], device="cuda")[0]
+    result["e2e"] = {"value": round(whole_job_rate(gathered, world, em) / 1e9, 2), "unit": "GB/s",
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(em, 4),
                      "steps": n_e2e}
 

@@ -8,32 +8,32 @@
 // scope (split-K workspace).
 //
 // Work decomposition: one CTA (4 warps) per (query row, KV head, K-split). The split's
-// index columns are staged in shared memory in chunks of kIdxCap, padding (-1) and bad
-// entries are dropped by a block-wide stream compaction, and the surviving slots are
-// streamed in tiles of kTile = 64 keys through a kStages-deep cp.async pipeline (16 B
-// copies; the 256 B / 512 B rows land XOR-swizzled so every fragment read below is
-// bank-conflict free).
+// index columns are cut into tiles of 16 keys, dealt round-robin to the warps; every warp
+// then runs on its own -- its own cp.async ring (16 B copies, rows XOR-swizzled so all
+// fragment reads are bank-conflict free), its own online softmax, its own accumulators --
+// with no block barrier in the main loop. The four partial results are merged once, at the
+// end, through shared memory.
 //
-// Per tile:
-//   q.K^T  warp w owns keys [16w, 16w+16): mma.sync m16n8k16 with M = the GQA group (16
-//          query heads, padded), N = 8 keys, K = 16 head dims. The query fragments stay in
-//          registers for the whole CTA; the key codes are dequantised straight into the B
-//          fragments (int8 -> fp16 by an exponent splice, E4M3 -> fp16 by the native cvt,
-//          bf16 as stored), so no dequantised copy is ever written back to shared memory.
-//          The head-dim order inside a fragment is permuted to match how a code word
-//          unpacks; the query fragments use the same permutation, so the dot product is
-//          unchanged.
-//   softmax  logits are scaled by the hoisted K scale (per slot for int8, folded into the
-//          per-head factor for E4M3), a cross-warp max exchange gives the tile max, and
-//          p = exp2(s - m) goes to shared memory as a hi + lo pair (fp16 for int8/E4M3, bf16
-//          for the bf16 layout), so p keeps ~22 (~17) bits: with outlier tokens a row can be
-//          a near-even mix of two large V rows of opposite sign, and single-fp16 p then loses
-//          ~1e-3 of the result to cancellation. int8 p also carries the slot's V scale and a
-//          power of two that keeps every value a normal fp16.
-//   p.V    warp w owns head dims [64w, 64w+64): A = p (ldmatrix), B = V codes dequantised
-//          in registers, fp32 accumulators rescaled on a new max.
-// The E4M3 V scale (and the power-of-two pre-scale) is applied once at the end; split
-// partials are written normalised, without the E4M3 V scale.
+// Per 16-key tile and warp:
+//   q.K^T  mma.sync m16n8k16, M = the GQA group (16 query heads, padded), N = 8 keys, K = 16
+//          head dims; 4 independent accumulator chains. Query fragments come from shared
+//          memory (ldmatrix; staged once per CTA as fp16 with a per-head power of two, bf16
+//          for the bf16 layout). Key codes are dequantised straight into B fragments
+//          (int8 -> fp16 by an exponent splice, E4M3 -> fp16 by the native cvt, bf16 as
+//          stored); the head-dim order inside a fragment follows how a code word unpacks and
+//          the staged query uses the same permutation.
+//   softmax  logits times the hoisted K scale (per slot for int8; E4M3's per-layer scale is
+//          folded into the per-head factor). The running max is only raised when a tile's max
+//          exceeds it by more than 2^8 (log2 domain), so the accumulators are rescaled a few
+//          times per row rather than every tile; p <= 2^8 is sized for that.
+//   p.V    p comes straight from the q.K^T accumulators (the m16n8 C layout of two N-tiles is
+//          the m16k16 A layout) as an fp16 hi + lo pair (bf16 pair for the bf16 layout): with
+//          outlier tokens a row can be a near-even mix of two large V rows of opposite sign,
+//          and single-fp16 p would lose ~1e-3 of the result to cancellation. int8 p also
+//          carries the slot's V scale and a power of two keeping it a normal fp16. 32 N-tiles
+//          of 8 head dims each, two MMAs (hi, lo) per tile, V codes dequantised in registers.
+// The E4M3 V scale and the power-of-two pre-scale are applied once at the end; split partials
+// are written normalised, without the E4M3 V scale.
 #pragma once
 
 #include "qkv_internal.cuh"
@@ -43,12 +43,11 @@ namespace gather {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kTile = 64;
-constexpr int kIdxCap = 1024;
-constexpr int kIdxPerThread = kIdxCap / kThreads;
+constexpr int kKeys = 16;  // keys per warp tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kPShift = 14;  // p * 2^14 keeps p >= 2^-28 a normal fp16
+constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units): p <= 2^8
+constexpr int kPShift = 7;    // p * 2^7 <= 2^15 stays a finite fp16; p >= 2^-21 stays normal
 
 template <int FMT>
 struct Fmt;
@@ -74,25 +73,31 @@ struct Fmt<QKV_BF16> {
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true;
 };
 
+constexpr int kORow = 292;  // floats per head row of the final merge buffer (bank-conflict-free)
+
 template <int FMT>
 struct Smem {
   using F = Fmt<FMT>;
-  static constexpr size_t kKV = size_t(F::kStages) * kTile * F::kRowBytes;  // one of K / V
-  static constexpr size_t kScale = F::kSide ? size_t(F::kStages) * kTile * 4 : 0;
-  static constexpr size_t kK = 0;
-  static constexpr size_t kV = kK + kKV;
-  static constexpr size_t kKs = kV + kKV;
-  static constexpr size_t kVs = kKs + kScale;
-  static constexpr size_t kIdx = kVs + kScale;
-  static constexpr size_t kP = kIdx + kIdxCap * 4;
-  static constexpr size_t kPBytes = 2 * 16 * kTile * 2;  // hi and lo halves of p
-  static constexpr size_t kRed = kP + kPBytes;  // [kWarps][16] floats
-  static constexpr size_t kVmax = kRed + kWarps * 16 * 4;
-  static constexpr size_t kCnt = kVmax + kWarps * 4;
-  static constexpr size_t kTotal = kCnt + (kWarps + 4) * 4;
+  static constexpr size_t kQ = 0;  // [16 k-steps][16 heads][16] 16-bit, fragment order
+  static constexpr size_t kQBytes = 16 * 16 * 16 * 2;
+  static constexpr size_t kFac = kQ + kQBytes;  // [16] floats: logit factor per head
+  static constexpr size_t kStageK = 0;
+  static constexpr size_t kStageV = size_t(kKeys) * F::kRowBytes;
+  static constexpr size_t kStageKs = 2 * size_t(kKeys) * F::kRowBytes;  // side: K then V scales
+  static constexpr size_t kStageMeta = kStageKs + (F::kSide ? 2 * kKeys * 4 : 0);  // inline: record offsets
+  static constexpr size_t kStageBytes = kStageMeta + (F::kInline ? kKeys : 0);
+  static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][kStages] stages
+  static constexpr size_t kWarpRing = size_t(F::kStages) * kStageBytes;
+  static constexpr size_t kMask = kRing + kWarps * kWarpRing;  // [kWarps][kStages] uint32
+  static constexpr size_t kM = kMask + kWarps * F::kStages * 4;  // [kWarps][16] floats
+  static constexpr size_t kL = kM + kWarps * 16 * 4;              // [kWarps][16] floats
+  static constexpr size_t kTotal = kL + kWarps * 16 * 4;
+  // final merge buffer [kWarps][16][kORow] floats, reusing the rings
+  static_assert(size_t(kWarps) * 16 * kORow * 4 <= kWarps * kWarpRing, "merge buffer must fit in the rings");
+  static_assert(kRing % 16 == 0 && kStageBytes % 16 == 0, "16 B alignment of the cp.async destinations");
 };
 
-// Shared-memory 16 B chunk position of chunk j of tile row `row`.
+// Shared-memory 16 B chunk position of chunk j of K / V tile row `row`.
 template <int FMT>
 __device__ __forceinline__ int swz_k(int j, int row) {
   if (Fmt<FMT>::kInline) return j;
@@ -102,98 +107,16 @@ __device__ __forceinline__ int swz_k(int j, int row) {
 template <int FMT>
 __device__ __forceinline__ int swz_v(int j, int row) {
   if (Fmt<FMT>::kInline) return j;
-  return j ^ (row & 6);
+  const int i = (row >> 1) & 3;
+  if (Fmt<FMT>::kBf16) return j ^ i;
+  return j ^ ((i & 1) | ((i & 2) << 1));  // 0, 1, 4, 5
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
-// Stage index columns [cs, ce) of row r into sIdx, dropping -1 and out-of-range entries
-// (the latter also flag QKV_DEV_BAD_INDEX). Order is kept. Returns the number kept.
-__device__ __forceinline__ int stage_indices(const GatherArgs& a, int64_t r, int cs, int ce, int32_t* sIdx,
-                                             int* sCnt, int tid, int lane, int warp) {
-  const int n = ce - cs;
-  const int32_t* src = a.topk_idx + r * a.topk + cs;
-  int vals[kIdxPerThread];
-  int cnt = 0;
-  bool bad = false;
-#pragma unroll
-  for (int i = 0; i < kIdxPerThread; ++i) {
-    const int j = tid * kIdxPerThread + i;
-    int v = (j < n) ? __ldg(src + j) : -1;
-    if (v < -1 || static_cast<int64_t>(v) >= a.num_slots) {
-      bad = true;
-      v = -1;
-    }
-    vals[i] = v;
-    cnt += (v >= 0);
-  }
-  if (bad && a.dev_status != nullptr) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
-  int x = cnt;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) sCnt[warp] = x;
-  __syncthreads();
-  int base = x - cnt, total = 0;
-#pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    const int cw = sCnt[w];
-    base += (w < warp) ? cw : 0;
-    total += cw;
-  }
-#pragma unroll
-  for (int i = 0; i < kIdxPerThread; ++i)
-    if (vals[i] >= 0) sIdx[base++] = vals[i];
-  __syncthreads();
-  return total;
-}
-
-// Issue the cp.async copies of one tile (K rows, V rows, side scales) into stage `st`.
-template <int FMT>
-__device__ __forceinline__ void issue_tile(const GatherArgs& a, int h, const int32_t* sIdx, int tile_base,
-                                           int nvalid, uint8_t* smem, int st, int tid) {
-  using F = Fmt<FMT>;
-  using L = Smem<FMT>;
-  const int kk = tid >> 1, half = tid & 1;
-  const int key = tile_base + kk;
-  const bool valid = key < nvalid;
-  const int64_t slot = valid ? sIdx[key] : 0;
-  const int64_t rec = slot * a.num_kv_heads + h;
-  const uint32_t dK = smem_u32(smem + L::kK + (size_t(st) * kTile + kk) * F::kRowBytes);
-  const uint32_t dV = smem_u32(smem + L::kV + (size_t(st) * kTile + kk) * F::kRowBytes);
-  if (F::kInline) {
-    const int64_t off = rec * F::kGlobalRow;
-    const int64_t al = off & ~int64_t(15);
-    const int delta = static_cast<int>(off - al);
-    const uint8_t* gK = a.k_cache + al;
-    const uint8_t* gV = a.v_cache + al;
-    constexpr int kFirst = (F::kChunks + 1) / 2;  // 9 chunks for half 0, 8 for half 1
-    const int j0 = half ? kFirst : 0, j1 = half ? F::kChunks : kFirst;
-    for (int j = j0; j < j1; ++j) {
-      // the last chunk copies only the record's own bytes (never past the pool's end)
-      const int nb = valid ? (j == F::kChunks - 1 ? delta + 4 : 16) : 0;
-      cp_async16(dK + j * 16, gK + j * 16, nb);
-      cp_async16(dV + j * 16, gV + j * 16, nb);
-    }
-  } else {
-    const uint8_t* gK = a.k_cache + rec * F::kGlobalRow;
-    const uint8_t* gV = a.v_cache + rec * F::kGlobalRow;
-    const int nb = valid ? 16 : 0;
-    constexpr int kHalf = F::kChunks / 2;
-#pragma unroll
-    for (int i = 0; i < kHalf; ++i) {
-      const int j = half * kHalf + i;
-      cp_async16(dK + swz_k<FMT>(j, kk) * 16, gK + j * 16, nb);
-      cp_async16(dV + swz_v<FMT>(j, kk) * 16, gV + j * 16, nb);
-    }
-    if (F::kSide) {
-      const float* gs = half ? a.v_scale_tok : a.k_scale_tok;
-      const size_t so = half ? L::kVs : L::kKs;
-      cp_async4(smem_u32(smem + so + (size_t(st) * kTile + kk) * 4), gs + rec, valid ? 4 : 0);
-    }
-  }
+// Byte offset of query element (k-step k, head hd, k-index kappa) in the staged query.
+__device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
+  return k * 512 + hd * 32 + ((((kappa >> 3) ^ ((hd >> 2) & 1))) << 4) + (kappa & 7) * 2;
 }
 
 template <int FMT>
@@ -201,13 +124,6 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   using F = Fmt<FMT>;
   using L = Smem<FMT>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  int32_t* sIdx = reinterpret_cast<int32_t*>(smem + L::kIdx);
-  float* sRed = reinterpret_cast<float*>(smem + L::kRed);
-  float* sVmax = reinterpret_cast<float*>(smem + L::kVmax);
-  int* sCnt = reinterpret_cast<int*>(smem + L::kCnt);
-  const uint32_t sP = smem_u32(smem + L::kP);
-  const uint32_t sPlo = sP + 16 * kTile * 2;  // low halves of p
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, hn = lane >> 2;
   const int h0 = hn, h1 = hn + 8;
@@ -220,410 +136,457 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const int per_split = (a.topk + P - 1) / P;
   const int col0 = min(a.topk, split * per_split);
   const int col1 = min(a.topk, col0 + per_split);
+  float* sFac = reinterpret_cast<float*>(smem + L::kFac);
+  uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + L::kMask) + warp * F::kStages;
+  uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
+  const uint32_t sQ = smem_u32(smem + L::kQ);
 
-  // ---------------- query fragments (registers for the whole CTA)
-  uint32_t qf[16][4];
-  float fac0, fac1;  // log2-domain logit factor of heads h0, h1
+  // ---------------- stage the query once: 8 threads per head, 32 head dims each
   {
-    const __nv_bfloat16* qb = a.q + (r * Hq + static_cast<int64_t>(h) * G) * kHeadDim;
-    uint32_t w0[4][8], w1[4][8];
+    const int qh = tid >> 3, part = tid & 7;
+    const bool live = qh < G;
+    uint32_t w[16];
+    if (live) {
+      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + static_cast<int64_t>(h) * G + qh) * kHeadDim +
+                                                      32 * part);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 x = __ldg(p + i);
+        w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+    int sg = 0;
+    if (!F::kBf16) {
+      // fp16 operands: a power of two puts the head's largest |q| in [2^14, 2^15)
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = max(m, max((w[i] & 0x7FFFu) << 16, w[i] & 0x7FFF0000u));
+#pragma unroll
+      for (int off = 1; off <= 4; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+      sg = m ? max(-64, min(64, 14 - (static_cast<int>(m >> 23) - 127))) : 0;
+    }
+    const float u = pow2f(sg);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int d = 32 * part + i;
+      const int blk = d >> 6, cc = (d >> 4) & 3, ks = (d >> 2) & 3, rr = d & 3;
+      // int8 B fragments pair head dims (+0, +2) / (+1, +3); E4M3 and bf16 pair (+0, +1) / (+2, +3)
+      const int upper = F::kInt8 ? (rr & 1) : (rr >> 1);
+      const int e = F::kInt8 ? (rr >> 1) : (rr & 1);
+      const int kappa = upper * 8 + 2 * cc + e;
+      const uint32_t word = w[i >> 1];
+      const uint32_t bits16 = (i & 1) ? (word >> 16) : (word & 0xFFFFu);
+      uint16_t v16;
+      if (F::kBf16) {
+        v16 = static_cast<uint16_t>(bits16);
+      } else {
+        const __half hv = __float2half_rn(__uint_as_float(bits16 << 16) * u);
+        v16 = *reinterpret_cast<const uint16_t*>(&hv);
+      }
+      *reinterpret_cast<uint16_t*>(smem + L::kQ + q_off(blk * 4 + ks, qh, kappa)) = v16;
+    }
+    if (part == 0) {
+      float base = a.softmax_scale * kLog2e;
+      if (F::kE4m3) base *= a.k_scale_layer;
+      sFac[qh] = live ? base * pow2f(-sg) : 0.f;
+    }
+  }
+  __syncthreads();
+  const float fac0 = sFac[h0], fac1 = sFac[h1];
+
+  // ---------------- this warp's tiles: split tiles warp, warp + 4, ...
+  const int ntiles = (col1 - col0 + kKeys - 1) / kKeys;
+  const int my = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  const int32_t* idx_row = a.topk_idx + r * a.topk;
+
+  auto load_idx = [&](int i) -> int {
+    if (i >= my || lane >= kKeys) return -1;
+    const int col = col0 + (warp + kWarps * i) * kKeys + lane;
+    if (col >= col1) return -1;
+    int v = __ldg(idx_row + col);
+    if (v < -1 || static_cast<int64_t>(v) >= a.num_slots) {
+      if (a.dev_status != nullptr) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+      v = -1;
+    }
+    return v;
+  };
+
+  auto issue = [&](int i, int idxv) {
+    const int st = i % F::kStages;
+    const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
+    if (lane == 0) sMask[st] = mask;
+    const int key = lane >> 1, half = lane & 1;
+    int slot = __shfl_sync(0xffffffffu, idxv, key);
+    const bool valid = slot >= 0;
+    slot = valid ? slot : 0;
+    const int64_t rec = static_cast<int64_t>(slot) * H + h;
+    uint8_t* sb = ring + size_t(st) * L::kStageBytes;
+    const uint32_t dK = smem_u32(sb + L::kStageK + key * F::kRowBytes);
+    const uint32_t dV = smem_u32(sb + L::kStageV + key * F::kRowBytes);
+    if (F::kInline) {
+      const int64_t off = rec * F::kGlobalRow;
+      const int64_t al = off & ~int64_t(15);
+      const int delta = static_cast<int>(off - al);
+      const uint8_t* gK = a.k_cache + al;
+      const uint8_t* gV = a.v_cache + al;
+      if (half == 0) sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
+      constexpr int kFirst = (F::kChunks + 1) / 2;  // 9 chunks for half 0, 8 for half 1
+      const int j0 = half ? kFirst : 0, j1 = half ? F::kChunks : kFirst;
+      for (int j = j0; j < j1; ++j) {
+        // the last chunk copies only the record's own bytes (never past the pool's end)
+        const int nb = valid ? (j == F::kChunks - 1 ? delta + 4 : 16) : 0;
+        cp_async16(dK + j * 16, gK + j * 16, nb);
+        cp_async16(dV + j * 16, gV + j * 16, nb);
+      }
+    } else {
+      const uint8_t* gK = a.k_cache + rec * F::kGlobalRow;
+      const uint8_t* gV = a.v_cache + rec * F::kGlobalRow;
+      const int nb = valid ? 16 : 0;
+      constexpr int kHalf = F::kChunks / 2;
+#pragma unroll
+      for (int t = 0; t < kHalf; ++t) {
+        const int j = half * kHalf + t;
+        cp_async16(dK + swz_k<FMT>(j, key) * 16, gK + j * 16, nb);
+        cp_async16(dV + swz_v<FMT>(j, key) * 16, gV + j * 16, nb);
+      }
+      if (F::kSide) {
+        const float* gs = half ? a.v_scale_tok : a.k_scale_tok;
+        cp_async4(smem_u32(sb + L::kStageKs + (half * kKeys + key) * 4), gs + rec, valid ? 4 : 0);
+      }
+    }
+  };
+
+  // ---------------- online-softmax state (per warp)
+  float mu0 = -INFINITY, mu1 = -INFINITY;  // running max in use (log2 domain), heads h0, h1
+  float l0 = 0.f, l1 = 0.f;                // this thread's share of sum p
+  int eu = -100;                           // int8: 2^eu > every V scale seen
+  float oacc[32][4];
+#pragma unroll
+  for (int t = 0; t < 32; ++t) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
+
+  int nidx = load_idx(0);
+#pragma unroll
+  for (int s = 0; s < F::kStages - 1; ++s) {
+    if (s < my) issue(s, nidx);
+    cp_async_commit();
+    nidx = load_idx(s + 1);
+  }
+
+  for (int i = 0; i < my; ++i) {
+    if (i + F::kStages - 1 < my) issue(i + F::kStages - 1, nidx);
+    cp_async_commit();
+    nidx = load_idx(i + F::kStages);
+    cp_async_wait<F::kStages - 1>();
+    __syncwarp();
+
+    const int st = i % F::kStages;
+    const uint8_t* sb = ring + size_t(st) * L::kStageBytes;
+    const uint8_t* tK = sb + L::kStageK;
+    const uint8_t* tV = sb + L::kStageV;
+    const uint32_t mask = sMask[st];
+
+    // ---- q . K^T: acc[nt][parity of the head-dim block]
+    float acc[2][2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int pz = 0; pz < 2; ++pz) acc[nt][pz][0] = acc[nt][pz][1] = acc[nt][pz][2] = acc[nt][pz][3] = 0.f;
+    int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
+    if (F::kInline) {
+      delta_k[0] = sb[L::kStageMeta + hn];
+      delta_k[1] = sb[L::kStageMeta + 8 + hn];
+    }
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
-      uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, y0 = x0, y1 = x0;
-      if (h0 < G) {
-        const uint4* p = reinterpret_cast<const uint4*>(qb + h0 * kHeadDim + 64 * blk + 16 * c);
-        x0 = __ldg(p);
-        x1 = __ldg(p + 1);
-      }
-      if (h1 < G) {
-        const uint4* p = reinterpret_cast<const uint4*>(qb + h1 * kHeadDim + 64 * blk + 16 * c);
-        y0 = __ldg(p);
-        y1 = __ldg(p + 1);
-      }
-      w0[blk][0] = x0.x; w0[blk][1] = x0.y; w0[blk][2] = x0.z; w0[blk][3] = x0.w;
-      w0[blk][4] = x1.x; w0[blk][5] = x1.y; w0[blk][6] = x1.z; w0[blk][7] = x1.w;
-      w1[blk][0] = y0.x; w1[blk][1] = y0.y; w1[blk][2] = y0.z; w1[blk][3] = y0.w;
-      w1[blk][4] = y1.x; w1[blk][5] = y1.y; w1[blk][6] = y1.z; w1[blk][7] = y1.w;
-    }
-    float base = a.softmax_scale * kLog2e;
-    if (F::kE4m3) base *= a.k_scale_layer;
-    if (F::kBf16) {
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          qf[blk * 4 + ks][0] = w0[blk][2 * ks];
-          qf[blk * 4 + ks][1] = w1[blk][2 * ks];
-          qf[blk * 4 + ks][2] = w0[blk][2 * ks + 1];
-          qf[blk * 4 + ks][3] = w1[blk][2 * ks + 1];
-        }
-      fac0 = base;
-      fac1 = base;
-    } else {
-      // fp16 operands: scale each head by a power of two so its largest |q| lands in
-      // [2^14, 2^15) -- inside fp16's normal range whatever the bf16 magnitudes are.
-      uint32_t m0 = 0, m1 = 0;
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          m0 = max(m0, max((w0[blk][i] & 0x7FFFu) << 16, w0[blk][i] & 0x7FFF0000u));
-          m1 = max(m1, max((w1[blk][i] & 0x7FFFu) << 16, w1[blk][i] & 0x7FFF0000u));
-        }
-#pragma unroll
-      for (int off = 1; off <= 2; off <<= 1) {
-        m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, off));
-        m1 = max(m1, __shfl_xor_sync(0xffffffffu, m1, off));
-      }
-      const int e0 = static_cast<int>(m0 >> 23) - 127, e1 = static_cast<int>(m1 >> 23) - 127;
-      const int sg0 = m0 ? max(-64, min(64, 14 - e0)) : 0;
-      const int sg1 = m1 ? max(-64, min(64, 14 - e1)) : 0;
-      const float u0 = pow2f(sg0), u1 = pow2f(sg1);
-#pragma unroll
-      for (int blk = 0; blk < 4; ++blk)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint32_t a0 = w0[blk][2 * ks], a1 = w0[blk][2 * ks + 1];
-          const uint32_t b0 = w1[blk][2 * ks], b1 = w1[blk][2 * ks + 1];
-          uint32_t* f = qf[blk * 4 + ks];
-          if (F::kInt8) {
-            // int8 B fragments hold head dims (+0, +2) and (+1, +3)
-            f[0] = pack_half2(bf16lo(a0) * u0, bf16lo(a1) * u0);
-            f[2] = pack_half2(bf16hi(a0) * u0, bf16hi(a1) * u0);
-            f[1] = pack_half2(bf16lo(b0) * u1, bf16lo(b1) * u1);
-            f[3] = pack_half2(bf16hi(b0) * u1, bf16hi(b1) * u1);
-          } else {
-            // E4M3 B fragments hold (+0, +1) and (+2, +3)
-            f[0] = pack_half2(bf16lo(a0) * u0, bf16hi(a0) * u0);
-            f[2] = pack_half2(bf16lo(a1) * u0, bf16hi(a1) * u0);
-            f[1] = pack_half2(bf16lo(b0) * u1, bf16hi(b0) * u1);
-            f[3] = pack_half2(bf16lo(b1) * u1, bf16hi(b1) * u1);
-          }
-        }
-      fac0 = base * pow2f(-sg0);
-      fac1 = base * pow2f(-sg1);
-    }
-    if (h0 >= G) fac0 = 0.f;
-    if (h1 >= G) fac1 = 0.f;
-  }
-
-  // ---------------- online-softmax state
-  float m_run0 = -INFINITY, m_run1 = -INFINITY;  // log2-domain running max (uniform in the CTA)
-  float l_run0 = 0.f, l_run1 = 0.f;              // this thread's share of sum p
-  int e_run = -100;                              // int8: 2^e_run > every V scale seen
-  float oacc[8][4];
-#pragma unroll
-  for (int t = 0; t < 8; ++t) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
-
-  for (int cs = col0; cs < col1; cs += kIdxCap) {
-    const int ce = min(col1, cs + kIdxCap);
-    __syncthreads();  // previous chunk's tiles fully consumed
-    const int nvalid = stage_indices(a, r, cs, ce, sIdx, sCnt, tid, lane, warp);
-    const int ntiles = (nvalid + kTile - 1) / kTile;
-
-#pragma unroll
-    for (int st = 0; st < F::kStages - 1; ++st) {
-      if (st < ntiles) issue_tile<FMT>(a, h, sIdx, st * kTile, nvalid, smem, st, tid);
-      cp_async_commit();
-    }
-
-    for (int t = 0; t < ntiles; ++t) {
-      cp_async_wait<F::kStages - 2>();
-      __syncthreads();
-      {
-        const int tn = t + F::kStages - 1;
-        if (tn < ntiles) issue_tile<FMT>(a, h, sIdx, tn * kTile, nvalid, smem, tn % F::kStages, tid);
-        cp_async_commit();
-      }
-      const int st = t % F::kStages;
-      const int tbase = t * kTile;
-      const uint8_t* tK = smem + L::kK + size_t(st) * kTile * F::kRowBytes;
-      const uint8_t* tV = smem + L::kV + size_t(st) * kTile * F::kRowBytes;
-
-      // ---- q . K^T for this warp's 16 keys
-      float sc[2][4];
+      uint32_t kw[2][8];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-        const int row = warp * 16 + nt * 8 + hn;
+        const int row = nt * 8 + hn;
         const uint32_t rowK = smem_u32(tK + row * F::kRowBytes);
-        int delta = 0;
-        if (F::kInline) {
-          const int key = tbase + row;
-          const int64_t slot = key < nvalid ? sIdx[key] : 0;
-          delta = static_cast<int>(((slot * H + h) * F::kGlobalRow) & 15);
+        if (F::kBf16) {
+          const uint4 x = lds128(rowK + (swz_k<FMT>(8 * blk + 2 * c, row) << 4));
+          const uint4 y = lds128(rowK + (swz_k<FMT>(8 * blk + 2 * c + 1, row) << 4));
+          kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
+          kw[nt][4] = y.x; kw[nt][5] = y.y; kw[nt][6] = y.z; kw[nt][7] = y.w;
+        } else if (F::kInline) {
+          const uint32_t p = rowK + delta_k[nt] + 64 * blk + 16 * c;
+          kw[nt][0] = lds32(p); kw[nt][1] = lds32(p + 4); kw[nt][2] = lds32(p + 8); kw[nt][3] = lds32(p + 12);
+        } else {
+          const uint4 x = lds128(rowK + (swz_k<FMT>(4 * blk + c, row) << 4));
+          kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
+        }
+      }
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        uint32_t qa[4];
+        {
+          const int mtx = lane >> 3, j = lane & 7;
+          const int hd = (mtx & 1) * 8 + j;
+          ldmatrix_x4(sQ + (blk * 4 + ks) * 512 + hd * 32 + ((((mtx >> 1) ^ ((hd >> 2) & 1))) << 4), qa[0], qa[1],
+                      qa[2], qa[3]);
         }
 #pragma unroll
-        for (int blk = 0; blk < 4; ++blk) {
-          uint32_t kw[8];
+        for (int nt = 0; nt < 2; ++nt) {
           if (F::kBf16) {
-            const uint4 x = lds128(rowK + (swz_k<FMT>(8 * blk + 2 * c, row) << 4));
-            const uint4 y = lds128(rowK + (swz_k<FMT>(8 * blk + 2 * c + 1, row) << 4));
-            kw[0] = x.x; kw[1] = x.y; kw[2] = x.z; kw[3] = x.w;
-            kw[4] = y.x; kw[5] = y.y; kw[6] = y.z; kw[7] = y.w;
-          } else if (F::kInline) {
-            const uint32_t p = rowK + delta + 64 * blk + 16 * c;
-            kw[0] = lds32(p); kw[1] = lds32(p + 4); kw[2] = lds32(p + 8); kw[3] = lds32(p + 12);
+            mma_bf16(acc[nt][blk & 1], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
+          } else if (F::kInt8) {
+            mma_f16(acc[nt][blk & 1], qa, i8pair_to_f16x2(kw[nt][ks]), i8pair_to_f16x2(kw[nt][ks] >> 8));
           } else {
-            const uint4 x = lds128(rowK + (swz_k<FMT>(4 * blk + c, row) << 4));
-            kw[0] = x.x; kw[1] = x.y; kw[2] = x.z; kw[3] = x.w;
-          }
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint32_t b0, b1;
-            if (F::kBf16) {
-              b0 = kw[2 * ks];
-              b1 = kw[2 * ks + 1];
-              mma_bf16(sc[nt], qf[blk * 4 + ks], b0, b1);
-            } else if (F::kInt8) {
-              b0 = i8pair_to_f16x2(kw[ks]);       // head dims +0, +2
-              b1 = i8pair_to_f16x2(kw[ks] >> 8);  // head dims +1, +3
-              mma_f16(sc[nt], qf[blk * 4 + ks], b0, b1);
-            } else {
-              b0 = e4m3pair_to_f16x2(kw[ks]);        // +0, +1
-              b1 = e4m3pair_to_f16x2(kw[ks] >> 16);  // +2, +3
-              mma_f16(sc[nt], qf[blk * 4 + ks], b0, b1);
-            }
+            mma_f16(acc[nt][blk & 1], qa, e4m3pair_to_f16x2(kw[nt][ks]), e4m3pair_to_f16x2(kw[nt][ks] >> 16));
           }
         }
       }
+    }
 
-      // ---- logits: hoisted K scale, mask, tile max
-      float vsc[2][2];  // int8: V scale of keys (nt, e)
-      float mx0 = -INFINITY, mx1 = -INFINITY, vmx = 0.f;
+    // ---- logits with the hoisted K scale; masked keys -> -inf
+    float s[2][4];  // [nt][0..1: head h0 keys e=0,1; 2..3: head h1]
+    float vsc[2][2];
+    float mx0 = -INFINITY, mx1 = -INFINITY, vmx = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int kt = warp * 16 + nt * 8 + 2 * c + e;
-          const bool valid = tbase + kt < nvalid;
-          float ks = 1.f, vs = 0.f;
-          if (F::kSide) {
-            ks = reinterpret_cast<const float*>(smem + L::kKs)[st * kTile + kt];
-            vs = reinterpret_cast<const float*>(smem + L::kVs)[st * kTile + kt];
-          } else if (F::kInline) {
-            const int64_t slot = valid ? sIdx[tbase + kt] : 0;
-            const int delta = static_cast<int>(((slot * H + h) * F::kGlobalRow) & 15);
-            ks = *reinterpret_cast<const float*>(tK + kt * F::kRowBytes + delta + kHeadDim);
-            vs = *reinterpret_cast<const float*>(tV + kt * F::kRowBytes + delta + kHeadDim);
-          }
-          vs = valid ? vs : 0.f;
-          vsc[nt][e] = vs;
-          vmx = fmaxf(vmx, vs);
-          const float s0 = valid ? sc[nt][e] * fac0 * ks : -INFINITY;
-          const float s1 = valid ? sc[nt][2 + e] * fac1 * ks : -INFINITY;
-          sc[nt][e] = s0;
-          sc[nt][2 + e] = s1;
-          mx0 = fmaxf(mx0, s0);
-          mx1 = fmaxf(mx1, s1);
+      for (int e = 0; e < 2; ++e) {
+        const int kt = nt * 8 + 2 * c + e;
+        const bool valid = (mask >> kt) & 1u;
+        float ksc = 1.f, vs = 0.f;
+        if (F::kSide) {
+          ksc = reinterpret_cast<const float*>(sb + L::kStageKs)[kt];
+          vs = reinterpret_cast<const float*>(sb + L::kStageKs)[kKeys + kt];
+        } else if (F::kInline) {
+          const int dl = sb[L::kStageMeta + kt];
+          ksc = *reinterpret_cast<const float*>(tK + kt * F::kRowBytes + dl + kHeadDim);
+          vs = *reinterpret_cast<const float*>(tV + kt * F::kRowBytes + dl + kHeadDim);
         }
+        vs = valid ? vs : 0.f;
+        vsc[nt][e] = vs;
+        vmx = fmaxf(vmx, vs);
+        const float x0 = acc[nt][0][e] + acc[nt][1][e];
+        const float x1 = acc[nt][0][2 + e] + acc[nt][1][2 + e];
+        s[nt][e] = valid ? x0 * fac0 * ksc : -INFINITY;
+        s[nt][2 + e] = valid ? x1 * fac1 * ksc : -INFINITY;
+        mx0 = fmaxf(mx0, s[nt][e]);
+        mx1 = fmaxf(mx1, s[nt][2 + e]);
+      }
 #pragma unroll
-      for (int off = 1; off <= 2; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        if (F::kInt8) vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
-      }
-      if (c == 0) {
-        sRed[warp * 16 + h0] = mx0;
-        sRed[warp * 16 + h1] = mx1;
-      }
-      if (F::kInt8 && lane == 0) sVmax[warp] = vmx;
-      __syncthreads();
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      if (F::kInt8) vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
+    }
 
-      float tm0 = sRed[h0], tm1 = sRed[h1];
+    // ---- lazy rescale: raise the max in use only past the threshold
+    {
+      const float nm0 = (mx0 > mu0 + kTau) ? mx0 : mu0;
+      const float nm1 = (mx1 > mu1 + kTau) ? mx1 : mu1;
+      int ne = eu;
+      if (F::kInt8 && vmx > 0.f) ne = max(eu, static_cast<int>(__float_as_uint(vmx) >> 23) - 126);
+      const float ov = F::kInt8 ? pow2f(max(eu - ne, -126)) : 1.f;
+      const float al0 = (nm0 == mu0) ? 1.f : fast_exp2(mu0 - nm0);  // mu0 = -inf gives 0
+      const float al1 = (nm1 == mu1) ? 1.f : fast_exp2(mu1 - nm1);
+      if (__any_sync(0xffffffffu, nm0 != mu0 || nm1 != mu1 || ne != eu)) {
+        const float f0 = al0 * ov, f1 = al1 * ov;
 #pragma unroll
-      for (int w = 1; w < kWarps; ++w) {
-        tm0 = fmaxf(tm0, sRed[w * 16 + h0]);
-        tm1 = fmaxf(tm1, sRed[w * 16 + h1]);
+        for (int t = 0; t < 32; ++t) {
+          oacc[t][0] *= f0;
+          oacc[t][1] *= f0;
+          oacc[t][2] *= f1;
+          oacc[t][3] *= f1;
+        }
+        l0 *= al0;
+        l1 *= al1;
       }
-      const float mn0 = fmaxf(m_run0, tm0), mn1 = fmaxf(m_run1, tm1);
-      const float al0 = (mn0 == -INFINITY) ? 1.f : fast_exp2(m_run0 - mn0);
-      const float al1 = (mn1 == -INFINITY) ? 1.f : fast_exp2(m_run1 - mn1);
-      float pm = 1.f, ov = 1.f;
-      if (F::kInt8) {
-        float vm = sVmax[0];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) vm = fmaxf(vm, sVmax[w]);
-        const int et = vm > 0.f ? max(-100, static_cast<int>(__float_as_uint(vm) >> 23) - 126) : -100;
-        const int en = max(e_run, et);
-        ov = pow2f(max(e_run - en, -126));
-        pm = pow2f(kPShift - en);
-        e_run = en;
-      } else if (F::kE4m3) {
-        pm = pow2f(kPShift);
-      }
-      m_run0 = mn0;
-      m_run1 = mn1;
+      mu0 = nm0;
+      mu1 = nm1;
+      eu = ne;
+    }
 
-      // ---- p = exp2(s - m) -> shared memory
-      float ps0 = 0.f, ps1 = 0.f;
+    // ---- p = exp2(s - m): fp32 sums, hi + lo A fragments
+    uint32_t pa[4], pl[4];
+    {
+      const float pm = F::kInt8 ? pow2f(kPShift - eu) : (F::kE4m3 ? pow2f(kPShift) : 1.f);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int kt = warp * 16 + nt * 8 + 2 * c;
         float p[4];
-        p[0] = (mn0 == -INFINITY) ? 0.f : fast_exp2(sc[nt][0] - mn0);
-        p[1] = (mn0 == -INFINITY) ? 0.f : fast_exp2(sc[nt][1] - mn0);
-        p[2] = (mn1 == -INFINITY) ? 0.f : fast_exp2(sc[nt][2] - mn1);
-        p[3] = (mn1 == -INFINITY) ? 0.f : fast_exp2(sc[nt][3] - mn1);
-        ps0 += p[0] + p[1];
-        ps1 += p[2] + p[3];
-        const uint32_t off0 = h0 * (kTile * 2) + ((((kt >> 3) ^ (h0 & 7))) << 4) + (kt & 7) * 2;
-        const uint32_t off1 = h1 * (kTile * 2) + ((((kt >> 3) ^ (h1 & 7))) << 4) + (kt & 7) * 2;
+        p[0] = fast_exp2(s[nt][0] - mu0);  // masked: exp2(-inf) = 0; mu = -inf only with no valid key
+        p[1] = fast_exp2(s[nt][1] - mu0);
+        p[2] = fast_exp2(s[nt][2] - mu1);
+        p[3] = fast_exp2(s[nt][3] - mu1);
+        if (mu0 == -INFINITY) p[0] = p[1] = 0.f;
+        if (mu1 == -INFINITY) p[2] = p[3] = 0.f;
+        l0 += p[0] + p[1];
+        l1 += p[2] + p[3];
+        const float f0 = F::kInt8 ? vsc[nt][0] * pm : pm, f1 = F::kInt8 ? vsc[nt][1] * pm : pm;
+        const float x0 = p[0] * f0, x1 = p[1] * f1, x2 = p[2] * f0, x3 = p[3] * f1;
         if (F::kBf16) {
-          const __nv_bfloat16 a0 = __float2bfloat16_rn(p[0]), a1 = __float2bfloat16_rn(p[1]);
-          const __nv_bfloat16 a2 = __float2bfloat16_rn(p[2]), a3 = __float2bfloat16_rn(p[3]);
-          sts32(sP + off0, pack_bf162(__bfloat162float(a0), __bfloat162float(a1)));
-          sts32(sP + off1, pack_bf162(__bfloat162float(a2), __bfloat162float(a3)));
-          sts32(sPlo + off0, pack_bf162(p[0] - __bfloat162float(a0), p[1] - __bfloat162float(a1)));
-          sts32(sPlo + off1, pack_bf162(p[2] - __bfloat162float(a2), p[3] - __bfloat162float(a3)));
+          const __nv_bfloat162 a0 = __floats2bfloat162_rn(x0, x1), a1 = __floats2bfloat162_rn(x2, x3);
+          pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&a0);
+          pa[2 * nt + 1] = *reinterpret_cast<const uint32_t*>(&a1);
+          pl[2 * nt] = pack_bf162(x0 - __low2float(a0), x1 - __high2float(a0));
+          pl[2 * nt + 1] = pack_bf162(x2 - __low2float(a1), x3 - __high2float(a1));
         } else {
-          const float f0 = F::kInt8 ? vsc[nt][0] * pm : pm, f1 = F::kInt8 ? vsc[nt][1] * pm : pm;
-          const float x0 = p[0] * f0, x1 = p[1] * f1, x2 = p[2] * f0, x3 = p[3] * f1;
-          const __half2 a = __floats2half2_rn(x0, x1), b = __floats2half2_rn(x2, x3);
-          sts32(sP + off0, *reinterpret_cast<const uint32_t*>(&a));
-          sts32(sP + off1, *reinterpret_cast<const uint32_t*>(&b));
-          sts32(sPlo + off0, pack_half2(x0 - __low2float(a), x1 - __high2float(a)));
-          sts32(sPlo + off1, pack_half2(x2 - __low2float(b), x3 - __high2float(b)));
+          const __half2 a0 = __floats2half2_rn(x0, x1), a1 = __floats2half2_rn(x2, x3);
+          pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&a0);
+          pa[2 * nt + 1] = *reinterpret_cast<const uint32_t*>(&a1);
+          pl[2 * nt] = pack_half2(x0 - __low2float(a0), x1 - __high2float(a0));
+          pl[2 * nt + 1] = pack_half2(x2 - __low2float(a1), x3 - __high2float(a1));
         }
       }
-      l_run0 = l_run0 * al0 + ps0;
-      l_run1 = l_run1 * al1 + ps1;
-      const float ao0 = al0 * ov, ao1 = al1 * ov;
-#pragma unroll
-      for (int t2 = 0; t2 < 8; ++t2) {
-        oacc[t2][0] *= ao0;
-        oacc[t2][1] *= ao0;
-        oacc[t2][2] *= ao1;
-        oacc[t2][3] *= ao1;
-      }
-      __syncthreads();
+    }
 
-      // ---- p . V for head dims [64 warp, 64 warp + 64)
+    // ---- p . V over the 256 head dims: N-tile t covers head dims 32*n + t (n = lane / 4)
+    {
+      const int rows[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+      if (F::kBf16) {
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        uint32_t pa[4], pl[4];
-        {
-          const int hrow = (lane & 7) + ((lane >> 3) & 1) * 8;
-          const int j = 2 * kk + (lane >> 4);
-          const uint32_t off = hrow * (kTile * 2) + ((j ^ (hrow & 7)) << 4);
-          ldmatrix_x4(sP + off, pa[0], pa[1], pa[2], pa[3]);
-          ldmatrix_x4(sPlo + off, pl[0], pl[1], pl[2], pl[3]);
-        }
-        const int r0 = 16 * kk + 2 * c;
-        const int rows[4] = {r0, r0 + 1, r0 + 8, r0 + 9};
-        if (F::kBf16) {
-          uint4 vv[4];
+        for (int qd = 0; qd < 4; ++qd) {  // 16 B chunk 4n + qd: head dims 32n + 8qd .. + 8
+          uint32_t vw[4][4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            vv[i] = lds128(smem_u32(tV + rows[i] * F::kRowBytes) + (swz_v<FMT>(8 * warp + hn, rows[i]) << 4));
-          const uint32_t a0[4] = {vv[0].x, vv[0].y, vv[0].z, vv[0].w};
-          const uint32_t a1[4] = {vv[1].x, vv[1].y, vv[1].z, vv[1].w};
-          const uint32_t a2[4] = {vv[2].x, vv[2].y, vv[2].z, vv[2].w};
-          const uint32_t a3[4] = {vv[3].x, vv[3].y, vv[3].z, vv[3].w};
-#pragma unroll
-          for (int t2 = 0; t2 < 8; ++t2) {
-            const uint32_t sel = (t2 & 1) ? 0x7632u : 0x5410u;
-            const uint32_t b0 = __byte_perm(a0[t2 >> 1], a1[t2 >> 1], sel);
-            const uint32_t b1 = __byte_perm(a2[t2 >> 1], a3[t2 >> 1], sel);
-            mma_bf16(oacc[t2], pa, b0, b1);
-            mma_bf16(oacc[t2], pl, b0, b1);
+          for (int ri = 0; ri < 4; ++ri) {
+            const uint4 x = lds128(smem_u32(tV + rows[ri] * F::kRowBytes) + (swz_v<FMT>(4 * hn + qd, rows[ri]) << 4));
+            vw[ri][0] = x.x; vw[ri][1] = x.y; vw[ri][2] = x.z; vw[ri][3] = x.w;
           }
-        } else {
-          uint2 vv[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
+          for (int tt = 0; tt < 8; ++tt) {
+            const uint32_t sel = (tt & 1) ? 0x7632u : 0x5410u;
+            const uint32_t b0 = __byte_perm(vw[0][tt >> 1], vw[1][tt >> 1], sel);
+            const uint32_t b1 = __byte_perm(vw[2][tt >> 1], vw[3][tt >> 1], sel);
+            mma_bf16(oacc[8 * qd + tt], pa, b0, b1);
+            mma_bf16(oacc[8 * qd + tt], pl, b0, b1);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int qd = 0; qd < 2; ++qd) {  // 16 B chunk 2n + qd: head dims 32n + 16qd .. + 16
+          uint32_t vw[4][4];
+#pragma unroll
+          for (int ri = 0; ri < 4; ++ri) {
             if (F::kInline) {
-              const int key = tbase + rows[i];
-              const int64_t slot = key < nvalid ? sIdx[key] : 0;
-              const int delta = static_cast<int>(((slot * H + h) * F::kGlobalRow) & 15);
-              const uint32_t p = smem_u32(tV + rows[i] * F::kRowBytes) + delta + 64 * warp + 8 * hn;
-              vv[i].x = lds32(p);
-              vv[i].y = lds32(p + 4);
+              const uint32_t p =
+                  smem_u32(tV + rows[ri] * F::kRowBytes) + sb[L::kStageMeta + rows[ri]] + 32 * hn + 16 * qd;
+              vw[ri][0] = lds32(p); vw[ri][1] = lds32(p + 4); vw[ri][2] = lds32(p + 8); vw[ri][3] = lds32(p + 12);
             } else {
-              vv[i] = lds64(smem_u32(tV + rows[i] * F::kRowBytes) +
-                            (swz_v<FMT>(4 * warp + (hn >> 1), rows[i]) << 4) + ((hn & 1) << 3));
+              const uint4 x =
+                  lds128(smem_u32(tV + rows[ri] * F::kRowBytes) + (swz_v<FMT>(2 * hn + qd, rows[ri]) << 4));
+              vw[ri][0] = x.x; vw[ri][1] = x.y; vw[ri][2] = x.z; vw[ri][3] = x.w;
             }
           }
           if (F::kInt8) {
 #pragma unroll
-            for (int t2 = 0; t2 < 8; ++t2) {
-              const uint32_t sel = (t2 & 3) | (((t2 & 3) + 4) << 8);
-              const uint32_t x0 = (t2 < 4) ? vv[0].x : vv[0].y, x1 = (t2 < 4) ? vv[1].x : vv[1].y;
-              const uint32_t x2 = (t2 < 4) ? vv[2].x : vv[2].y, x3 = (t2 < 4) ? vv[3].x : vv[3].y;
-              const uint32_t b0 = i8pair_to_f16x2(__byte_perm(x0, x1, sel));
-              const uint32_t b1 = i8pair_to_f16x2(__byte_perm(x2, x3, sel));
-              mma_f16(oacc[t2], pa, b0, b1);
-              mma_f16(oacc[t2], pl, b0, b1);
+            for (int tt = 0; tt < 16; ++tt) {
+              const uint32_t sel = (tt & 3) | (((tt & 3) + 4) << 8);
+              const uint32_t b0 = i8pair_to_f16x2(__byte_perm(vw[0][tt >> 2], vw[1][tt >> 2], sel));
+              const uint32_t b1 = i8pair_to_f16x2(__byte_perm(vw[2][tt >> 2], vw[3][tt >> 2], sel));
+              mma_f16(oacc[16 * qd + tt], pa, b0, b1);
+              mma_f16(oacc[16 * qd + tt], pl, b0, b1);
             }
           } else {
 #pragma unroll
-            for (int t4 = 0; t4 < 4; ++t4) {
-              // [a_t, b_t, a_t+1, b_t+1] for t = 2*(t4&1) within word t4>>1
+            for (int t4 = 0; t4 < 8; ++t4) {  // [a_t, b_t, a_t+1, b_t+1] pairs, t = 2*t4
               const uint32_t sel = (t4 & 1) ? 0x7362u : 0x5140u;
-              const uint32_t x0 = (t4 < 2) ? vv[0].x : vv[0].y, x1 = (t4 < 2) ? vv[1].x : vv[1].y;
-              const uint32_t x2 = (t4 < 2) ? vv[2].x : vv[2].y, x3 = (t4 < 2) ? vv[3].x : vv[3].y;
-              const uint32_t u = __byte_perm(x0, x1, sel), w = __byte_perm(x2, x3, sel);
+              const uint32_t u = __byte_perm(vw[0][t4 >> 1], vw[1][t4 >> 1], sel);
+              const uint32_t w = __byte_perm(vw[2][t4 >> 1], vw[3][t4 >> 1], sel);
               const uint32_t b0 = e4m3pair_to_f16x2(u), b1 = e4m3pair_to_f16x2(w);
               const uint32_t c0 = e4m3pair_to_f16x2(u >> 16), c1 = e4m3pair_to_f16x2(w >> 16);
-              mma_f16(oacc[2 * t4], pa, b0, b1);
-              mma_f16(oacc[2 * t4], pl, b0, b1);
-              mma_f16(oacc[2 * t4 + 1], pa, c0, c1);
-              mma_f16(oacc[2 * t4 + 1], pl, c0, c1);
+              mma_f16(oacc[16 * qd + 2 * t4], pa, b0, b1);
+              mma_f16(oacc[16 * qd + 2 * t4], pl, b0, b1);
+              mma_f16(oacc[16 * qd + 2 * t4 + 1], pa, c0, c1);
+              mma_f16(oacc[16 * qd + 2 * t4 + 1], pl, c0, c1);
             }
           }
         }
       }
     }
+    __syncwarp();
   }
 
-  // ---------------- finalize: sum l over the quad and the warps, normalise, store
+  // ---------------- merge the four warps' partial results
+  cp_async_wait<0>();
 #pragma unroll
   for (int off = 1; off <= 2; off <<= 1) {
-    l_run0 += __shfl_xor_sync(0xffffffffu, l_run0, off);
-    l_run1 += __shfl_xor_sync(0xffffffffu, l_run1, off);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+  }
+  __syncthreads();  // every warp is done with its ring: reuse it as the merge buffer
+  float* sO = reinterpret_cast<float*>(smem + L::kRing);  // [kWarps][16][kORow]
+  float* sM = reinterpret_cast<float*>(smem + L::kM);
+  float* sL = reinterpret_cast<float*>(smem + L::kL);
+  {
+    float post = 1.f;
+    if (F::kInt8) post = pow2f(eu - kPShift);
+    if (F::kE4m3) post = pow2f(-kPShift);
+    float* o0 = sO + (warp * 16 + h0) * kORow + 72 * c;
+    float* o1 = sO + (warp * 16 + h1) * kORow + 72 * c;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      // head dims 64c + 4j .. + 3 (N-tiles 4j..4j+3, column 2c) and 64c + 32 + 4j .. (column 2c+1)
+      reinterpret_cast<float4*>(o0)[j] = make_float4(oacc[4 * j][0] * post, oacc[4 * j + 1][0] * post,
+                                                     oacc[4 * j + 2][0] * post, oacc[4 * j + 3][0] * post);
+      reinterpret_cast<float4*>(o0 + 32)[j] = make_float4(oacc[4 * j][1] * post, oacc[4 * j + 1][1] * post,
+                                                          oacc[4 * j + 2][1] * post, oacc[4 * j + 3][1] * post);
+      reinterpret_cast<float4*>(o1)[j] = make_float4(oacc[4 * j][2] * post, oacc[4 * j + 1][2] * post,
+                                                     oacc[4 * j + 2][2] * post, oacc[4 * j + 3][2] * post);
+      reinterpret_cast<float4*>(o1 + 32)[j] = make_float4(oacc[4 * j][3] * post, oacc[4 * j + 1][3] * post,
+                                                          oacc[4 * j + 2][3] * post, oacc[4 * j + 3][3] * post);
+    }
+    if (c == 0) {
+      sM[warp * 16 + h0] = mu0;
+      sM[warp * 16 + h1] = mu1;
+      sL[warp * 16 + h0] = l0;
+      sL[warp * 16 + h1] = l1;
+    }
   }
   __syncthreads();
-  if (c == 0) {
-    sRed[warp * 16 + h0] = l_run0;
-    sRed[warp * 16 + h1] = l_run1;
-  }
-  __syncthreads();
-  float L0 = 0.f, L1 = 0.f;
+  {
+    const int hh = tid >> 3, part = tid & 7;  // head, 32 head dims
+    if (hh < G) {
+      float mw[kWarps], M = -INFINITY;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) {
-    L0 += sRed[w * 16 + h0];
-    L1 += sRed[w * 16 + h1];
-  }
-  float post = 1.f;
-  if (F::kInt8) post = pow2f(e_run - kPShift);
-  if (F::kE4m3) post = pow2f(-kPShift) * (P == 1 ? a.v_scale_layer : 1.f);
-
+      for (int w = 0; w < kWarps; ++w) {
+        mw[w] = sM[w * 16 + hh];
+        M = fmaxf(M, mw[w]);
+      }
+      float ww[kWarps], lsum = 0.f;
 #pragma unroll
-  for (int hi = 0; hi < 2; ++hi) {
-    const int hh = hi ? h1 : h0;
-    if (hh >= G) continue;
-    const float Lh = hi ? L1 : L0;
-    const float mh = hi ? m_run1 : m_run0;
-    const float f = (Lh > 0.f) ? post / Lh : 0.f;
-    const int64_t qhead = static_cast<int64_t>(h) * G + hh;
-    float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
-                          : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
-    dst += 64 * warp + 16 * c;
-    const int i0 = 2 * hi;
-    reinterpret_cast<float4*>(dst)[0] =
-        make_float4(oacc[0][i0] * f, oacc[1][i0] * f, oacc[2][i0] * f, oacc[3][i0] * f);
-    reinterpret_cast<float4*>(dst)[1] =
-        make_float4(oacc[4][i0] * f, oacc[5][i0] * f, oacc[6][i0] * f, oacc[7][i0] * f);
-    reinterpret_cast<float4*>(dst)[2] =
-        make_float4(oacc[0][i0 + 1] * f, oacc[1][i0 + 1] * f, oacc[2][i0 + 1] * f, oacc[3][i0 + 1] * f);
-    reinterpret_cast<float4*>(dst)[3] =
-        make_float4(oacc[4][i0 + 1] * f, oacc[5][i0 + 1] * f, oacc[6][i0 + 1] * f, oacc[7][i0 + 1] * f);
-    if (warp == 0 && c == 0) {
-      const float lse = (Lh > 0.f) ? (mh + log2f(Lh)) * kLn2 : -INFINITY;
-      if (P == 1) {
-        if (a.lse != nullptr) a.lse[r * Hq + qhead] = lse;
-      } else {
-        a.lse_part[(r * P + split) * Hq + qhead] = lse;
+      for (int w = 0; w < kWarps; ++w) {
+        ww[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+        lsum += ww[w] * sL[w * 16 + hh];
+      }
+      float f = (lsum > 0.f) ? 1.f / lsum : 0.f;
+      if (F::kE4m3 && P == 1) f *= a.v_scale_layer;
+      float res[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) res[i] = 0.f;
+      const int cb = part >> 1, hb = part & 1;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float4* src = reinterpret_cast<const float4*>(sO + (w * 16 + hh) * kORow + 72 * cb + 32 * hb);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 x = src[j];
+          res[4 * j] += ww[w] * x.x;
+          res[4 * j + 1] += ww[w] * x.y;
+          res[4 * j + 2] += ww[w] * x.z;
+          res[4 * j + 3] += ww[w] * x.w;
+        }
+      }
+      const int64_t qhead = static_cast<int64_t>(h) * G + hh;
+      float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
+                            : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
+      dst += 32 * part;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        reinterpret_cast<float4*>(dst)[j] =
+            make_float4(res[4 * j] * f, res[4 * j + 1] * f, res[4 * j + 2] * f, res[4 * j + 3] * f);
+      if (part == 0) {
+        const float lse = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+        if (P == 1) {
+          if (a.lse != nullptr) a.lse[r * Hq + qhead] = lse;
+        } else {
+          a.lse_part[(r * P + split) * Hq + qhead] = lse;
+        }
       }
     }
   }
