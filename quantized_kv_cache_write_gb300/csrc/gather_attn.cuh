@@ -214,48 +214,58 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     return v;
   };
 
+  // Copy one 16-key tile into ring stage i % kStages. Each warp-wide copy instruction moves
+  // whole rows: lanes 0-15 take the 16 B chunks of one key's 256 B row, lanes 16-31 the next
+  // key's (bf16: all 32 lanes on one 512 B row), so every request is a full, coalesced line.
   auto issue = [&](int i, int idxv) {
     const int st = i % F::kStages;
     const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
     if (lane == 0) sMask[st] = mask;
-    const int key = lane >> 1, half = lane & 1;
-    int slot = __shfl_sync(0xffffffffu, idxv, key);
-    const bool valid = slot >= 0;
-    slot = valid ? slot : 0;
-    const int64_t rec = static_cast<int64_t>(slot) * H + h;
     uint8_t* sb = ring + size_t(st) * L::kStageBytes;
-    const uint32_t dK = smem_u32(sb + L::kStageK + key * F::kRowBytes);
-    const uint32_t dV = smem_u32(sb + L::kStageV + key * F::kRowBytes);
-    if (F::kInline) {
-      const int64_t off = rec * F::kGlobalRow;
-      const int64_t al = off & ~int64_t(15);
-      const int delta = static_cast<int>(off - al);
-      const uint8_t* gK = a.k_cache + al;
-      const uint8_t* gV = a.v_cache + al;
-      if (half == 0) sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
-      constexpr int kFirst = (F::kChunks + 1) / 2;  // 9 chunks for half 0, 8 for half 1
-      const int j0 = half ? kFirst : 0, j1 = half ? F::kChunks : kFirst;
-      for (int j = j0; j < j1; ++j) {
-        // the last chunk copies only the record's own bytes (never past the pool's end)
-        const int nb = valid ? (j == F::kChunks - 1 ? delta + 4 : 16) : 0;
+    constexpr int kKeysPerCopy = F::kBf16 ? 1 : 2;
+    constexpr int kLanesPerKey = 32 / kKeysPerCopy;
+    const int sub = lane / kLanesPerKey, j = lane % kLanesPerKey;
+#pragma unroll 4
+    for (int t = 0; t < kKeys / kKeysPerCopy; ++t) {
+      const int key = t * kKeysPerCopy + sub;
+      int slot = __shfl_sync(0xffffffffu, idxv, key);
+      const bool valid = slot >= 0;
+      slot = valid ? slot : 0;
+      const int64_t rec = static_cast<int64_t>(slot) * H + h;
+      const uint32_t dK = smem_u32(sb + L::kStageK + key * F::kRowBytes);
+      const uint32_t dV = smem_u32(sb + L::kStageV + key * F::kRowBytes);
+      if (F::kInline) {
+        const int64_t off = rec * F::kGlobalRow;
+        const int64_t al = off & ~int64_t(15);
+        const int delta = static_cast<int>(off - al);
+        const uint8_t* gK = a.k_cache + al;
+        const uint8_t* gV = a.v_cache + al;
+        const int nb = valid ? 16 : 0;
         cp_async16(dK + j * 16, gK + j * 16, nb);
         cp_async16(dV + j * 16, gV + j * 16, nb);
-      }
-    } else {
-      const uint8_t* gK = a.k_cache + rec * F::kGlobalRow;
-      const uint8_t* gV = a.v_cache + rec * F::kGlobalRow;
-      const int nb = valid ? 16 : 0;
-      constexpr int kHalf = F::kChunks / 2;
-#pragma unroll
-      for (int t = 0; t < kHalf; ++t) {
-        const int j = half * kHalf + t;
+        if (j == 0) {
+          // the 17th chunk copies only the record's own bytes (never past the pool's end)
+          const int nl = valid ? delta + 4 : 0;
+          cp_async16(dK + 16 * 16, gK + 16 * 16, nl);
+          cp_async16(dV + 16 * 16, gV + 16 * 16, nl);
+          sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
+        }
+      } else {
+        const uint8_t* gK = a.k_cache + rec * F::kGlobalRow;
+        const uint8_t* gV = a.v_cache + rec * F::kGlobalRow;
+        const int nb = valid ? 16 : 0;
         cp_async16(dK + swz_k<FMT>(j, key) * 16, gK + j * 16, nb);
         cp_async16(dV + swz_v<FMT>(j, key) * 16, gV + j * 16, nb);
       }
-      if (F::kSide) {
-        const float* gs = half ? a.v_scale_tok : a.k_scale_tok;
-        cp_async4(smem_u32(sb + L::kStageKs + (half * kKeys + key) * 4), gs + rec, valid ? 4 : 0);
-      }
+    }
+    if (F::kSide) {
+      // lanes 0-15: K scales of the 16 keys; lanes 16-31: V scales
+      const int key = lane & 15;
+      int slot = __shfl_sync(0xffffffffu, idxv, key);
+      const bool valid = slot >= 0;
+      slot = valid ? slot : 0;
+      const float* gs = (lane >> 4) ? a.v_scale_tok : a.k_scale_tok;
+      cp_async4(smem_u32(sb + L::kStageKs + lane * 4), gs + static_cast<int64_t>(slot) * H + h, valid ? 4 : 0);
     }
   };
 
