@@ -141,62 +141,6 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
   const uint32_t sQ = smem_u32(smem + L::kQ);
 
-  // ---------------- stage the query once: 8 threads per head, 32 head dims each
-  {
-    const int qh = tid >> 3, part = tid & 7;
-    const bool live = qh < G;
-    uint32_t w[16];
-    if (live) {
-      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + static_cast<int64_t>(h) * G + qh) * kHeadDim +
-                                                      32 * part);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 x = __ldg(p + i);
-        w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
-    }
-    int sg = 0;
-    if (!F::kBf16) {
-      // fp16 operands: a power of two puts the head's largest |q| in [2^14, 2^15)
-      uint32_t m = 0;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) m = max(m, max((w[i] & 0x7FFFu) << 16, w[i] & 0x7FFF0000u));
-#pragma unroll
-      for (int off = 1; off <= 4; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
-      sg = m ? max(-64, min(64, 14 - (static_cast<int>(m >> 23) - 127))) : 0;
-    }
-    const float u = pow2f(sg);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int d = 32 * part + i;
-      const int blk = d >> 6, cc = (d >> 4) & 3, ks = (d >> 2) & 3, rr = d & 3;
-      // int8 B fragments pair head dims (+0, +2) / (+1, +3); E4M3 and bf16 pair (+0, +1) / (+2, +3)
-      const int upper = F::kInt8 ? (rr & 1) : (rr >> 1);
-      const int e = F::kInt8 ? (rr >> 1) : (rr & 1);
-      const int kappa = upper * 8 + 2 * cc + e;
-      const uint32_t word = w[i >> 1];
-      const uint32_t bits16 = (i & 1) ? (word >> 16) : (word & 0xFFFFu);
-      uint16_t v16;
-      if (F::kBf16) {
-        v16 = static_cast<uint16_t>(bits16);
-      } else {
-        const __half hv = __float2half_rn(__uint_as_float(bits16 << 16) * u);
-        v16 = *reinterpret_cast<const uint16_t*>(&hv);
-      }
-      *reinterpret_cast<uint16_t*>(smem + L::kQ + q_off(blk * 4 + ks, qh, kappa)) = v16;
-    }
-    if (part == 0) {
-      float base = a.softmax_scale * kLog2e;
-      if (F::kE4m3) base *= a.k_scale_layer;
-      sFac[qh] = live ? base * pow2f(-sg) : 0.f;
-    }
-  }
-  __syncthreads();
-  const float fac0 = sFac[h0], fac1 = sFac[h1];
-
   // ---------------- this warp's tiles: split tiles warp, warp + 4, ...
   const int ntiles = (col1 - col0 + kKeys - 1) / kKeys;
   const int my = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
@@ -269,6 +213,77 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     }
   };
 
+  // Start the first tiles' index loads and copies before staging the query, so their
+  // latencies overlap the query's.
+  int nidx;
+  {
+    int first[F::kStages];
+#pragma unroll
+    for (int t = 0; t < F::kStages; ++t) first[t] = load_idx(t);
+#pragma unroll
+    for (int t = 0; t < F::kStages - 1; ++t) {
+      if (t < my) issue(t, first[t]);
+      cp_async_commit();
+    }
+    nidx = first[F::kStages - 1];
+  }
+
+  // ---------------- stage the query once: 8 threads per head, 32 head dims each
+  {
+    const int qh = tid >> 3, part = tid & 7;
+    const bool live = qh < G;
+    uint32_t w[16];
+    if (live) {
+      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + static_cast<int64_t>(h) * G + qh) * kHeadDim +
+                                                      32 * part);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 x = __ldg(p + i);
+        w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) w[i] = 0u;
+    }
+    int sg = 0;
+    if (!F::kBf16) {
+      // fp16 operands: a power of two puts the head's largest |q| in [2^14, 2^15)
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) m = max(m, max((w[i] & 0x7FFFu) << 16, w[i] & 0x7FFF0000u));
+#pragma unroll
+      for (int off = 1; off <= 4; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+      sg = m ? max(-64, min(64, 14 - (static_cast<int>(m >> 23) - 127))) : 0;
+    }
+    const float u = pow2f(sg);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int d = 32 * part + i;
+      const int blk = d >> 6, cc = (d >> 4) & 3, ks = (d >> 2) & 3, rr = d & 3;
+      // int8 B fragments pair head dims (+0, +2) / (+1, +3); E4M3 and bf16 pair (+0, +1) / (+2, +3)
+      const int upper = F::kInt8 ? (rr & 1) : (rr >> 1);
+      const int e = F::kInt8 ? (rr >> 1) : (rr & 1);
+      const int kappa = upper * 8 + 2 * cc + e;
+      const uint32_t word = w[i >> 1];
+      const uint32_t bits16 = (i & 1) ? (word >> 16) : (word & 0xFFFFu);
+      uint16_t v16;
+      if (F::kBf16) {
+        v16 = static_cast<uint16_t>(bits16);
+      } else {
+        const __half hv = __float2half_rn(__uint_as_float(bits16 << 16) * u);
+        v16 = *reinterpret_cast<const uint16_t*>(&hv);
+      }
+      *reinterpret_cast<uint16_t*>(smem + L::kQ + q_off(blk * 4 + ks, qh, kappa)) = v16;
+    }
+    if (part == 0) {
+      float base = a.softmax_scale * kLog2e;
+      if (F::kE4m3) base *= a.k_scale_layer;
+      sFac[qh] = live ? base * pow2f(-sg) : 0.f;
+    }
+  }
+  __syncthreads();
+  const float fac0 = sFac[h0], fac1 = sFac[h1];
+
   // ---------------- online-softmax state (per warp)
   float mu0 = -INFINITY, mu1 = -INFINITY;  // running max in use (log2 domain), heads h0, h1
   float l0 = 0.f, l1 = 0.f;                // this thread's share of sum p
@@ -277,13 +292,6 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 #pragma unroll
   for (int t = 0; t < 32; ++t) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
 
-  int nidx = load_idx(0);
-#pragma unroll
-  for (int s = 0; s < F::kStages - 1; ++s) {
-    if (s < my) issue(s, nidx);
-    cp_async_commit();
-    nidx = load_idx(s + 1);
-  }
 
   for (int i = 0; i < my; ++i) {
     if (i + F::kStages - 1 < my) issue(i + F::kStages - 1, nidx);
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     const uint8_t* sb = ring + size_t(st) * L::kStageBytes;
     const uint8_t* tK = sb + L::kStageK;
     const uint8_t* tV = sb + L::kStageV;
-    const uint32_t mask = sMask[st];
+    const uint32_t mask = lds32(smem_u32(sMask + st));
 
     // ---- q . K^T: acc[nt][parity of the head-dim block]
     float acc[2][2][4];
@@ -306,8 +314,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       for (int pz = 0; pz < 2; ++pz) acc[nt][pz][0] = acc[nt][pz][1] = acc[nt][pz][2] = acc[nt][pz][3] = 0.f;
     int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
     if (F::kInline) {
-      delta_k[0] = sb[L::kStageMeta + hn];
-      delta_k[1] = sb[L::kStageMeta + 8 + hn];
+      delta_k[0] = lds_u8(smem_u32(sb + L::kStageMeta + hn));
+      delta_k[1] = lds_u8(smem_u32(sb + L::kStageMeta + 8 + hn));
     }
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
@@ -363,12 +371,12 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         const bool valid = (mask >> kt) & 1u;
         float ksc = 1.f, vs = 0.f;
         if (F::kSide) {
-          ksc = reinterpret_cast<const float*>(sb + L::kStageKs)[kt];
-          vs = reinterpret_cast<const float*>(sb + L::kStageKs)[kKeys + kt];
+          ksc = __uint_as_float(lds32(smem_u32(sb + L::kStageKs + kt * 4)));
+          vs = __uint_as_float(lds32(smem_u32(sb + L::kStageKs + (kKeys + kt) * 4)));
         } else if (F::kInline) {
-          const int dl = sb[L::kStageMeta + kt];
-          ksc = *reinterpret_cast<const float*>(tK + kt * F::kRowBytes + dl + kHeadDim);
-          vs = *reinterpret_cast<const float*>(tV + kt * F::kRowBytes + dl + kHeadDim);
+          const int dl = lds_u8(smem_u32(sb + L::kStageMeta + kt));
+          ksc = __uint_as_float(lds32(smem_u32(tK + kt * F::kRowBytes + dl + kHeadDim)));
+          vs = __uint_as_float(lds32(smem_u32(tV + kt * F::kRowBytes + dl + kHeadDim)));
         }
         vs = valid ? vs : 0.f;
         vsc[nt][e] = vs;
@@ -458,14 +466,16 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
             const uint4 x = lds128(smem_u32(tV + rows[ri] * F::kRowBytes) + (swz_v<FMT>(4 * hn + qd, rows[ri]) << 4));
             vw[ri][0] = x.x; vw[ri][1] = x.y; vw[ri][2] = x.z; vw[ri][3] = x.w;
           }
+          uint32_t bb[8][2];
 #pragma unroll
           for (int tt = 0; tt < 8; ++tt) {
             const uint32_t sel = (tt & 1) ? 0x7632u : 0x5410u;
-            const uint32_t b0 = __byte_perm(vw[0][tt >> 1], vw[1][tt >> 1], sel);
-            const uint32_t b1 = __byte_perm(vw[2][tt >> 1], vw[3][tt >> 1], sel);
-            mma_bf16(oacc[8 * qd + tt], pa, b0, b1);
-            mma_bf16(oacc[8 * qd + tt], pl, b0, b1);
+            bb[tt][0] = __byte_perm(vw[0][tt >> 1], vw[1][tt >> 1], sel);
+            bb[tt][1] = __byte_perm(vw[2][tt >> 1], vw[3][tt >> 1], sel);
+            mma_bf16(oacc[8 * qd + tt], pa, bb[tt][0], bb[tt][1]);
           }
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) mma_bf16(oacc[8 * qd + tt], pl, bb[tt][0], bb[tt][1]);
         }
       } else {
 #pragma unroll
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
           for (int ri = 0; ri < 4; ++ri) {
             if (F::kInline) {
               const uint32_t p =
-                  smem_u32(tV + rows[ri] * F::kRowBytes) + sb[L::kStageMeta + rows[ri]] + 32 * hn + 16 * qd;
+                  smem_u32(tV + rows[ri] * F::kRowBytes) + lds_u8(smem_u32(sb + L::kStageMeta + rows[ri])) + 32 * hn + 16 * qd;
               vw[ri][0] = lds32(p); vw[ri][1] = lds32(p + 4); vw[ri][2] = lds32(p + 8); vw[ri][3] = lds32(p + 12);
             } else {
               const uint4 x =
@@ -484,27 +494,32 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
             }
           }
           if (F::kInt8) {
+            uint32_t bb[16][2];
 #pragma unroll
             for (int tt = 0; tt < 16; ++tt) {
               const uint32_t sel = (tt & 3) | (((tt & 3) + 4) << 8);
-              const uint32_t b0 = i8pair_to_f16x2(__byte_perm(vw[0][tt >> 2], vw[1][tt >> 2], sel));
-              const uint32_t b1 = i8pair_to_f16x2(__byte_perm(vw[2][tt >> 2], vw[3][tt >> 2], sel));
-              mma_f16(oacc[16 * qd + tt], pa, b0, b1);
-              mma_f16(oacc[16 * qd + tt], pl, b0, b1);
+              bb[tt][0] = i8pair_to_f16x2(__byte_perm(vw[0][tt >> 2], vw[1][tt >> 2], sel));
+              bb[tt][1] = i8pair_to_f16x2(__byte_perm(vw[2][tt >> 2], vw[3][tt >> 2], sel));
+              mma_f16(oacc[16 * qd + tt], pa, bb[tt][0], bb[tt][1]);
             }
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt) mma_f16(oacc[16 * qd + tt], pl, bb[tt][0], bb[tt][1]);
           } else {
+            uint32_t bb[16][2];
 #pragma unroll
             for (int t4 = 0; t4 < 8; ++t4) {  // [a_t, b_t, a_t+1, b_t+1] pairs, t = 2*t4
               const uint32_t sel = (t4 & 1) ? 0x7362u : 0x5140u;
               const uint32_t u = __byte_perm(vw[0][t4 >> 1], vw[1][t4 >> 1], sel);
               const uint32_t w = __byte_perm(vw[2][t4 >> 1], vw[3][t4 >> 1], sel);
-              const uint32_t b0 = e4m3pair_to_f16x2(u), b1 = e4m3pair_to_f16x2(w);
-              const uint32_t c0 = e4m3pair_to_f16x2(u >> 16), c1 = e4m3pair_to_f16x2(w >> 16);
-              mma_f16(oacc[16 * qd + 2 * t4], pa, b0, b1);
-              mma_f16(oacc[16 * qd + 2 * t4], pl, b0, b1);
-              mma_f16(oacc[16 * qd + 2 * t4 + 1], pa, c0, c1);
-              mma_f16(oacc[16 * qd + 2 * t4 + 1], pl, c0, c1);
+              bb[2 * t4][0] = e4m3pair_to_f16x2(u);
+              bb[2 * t4][1] = e4m3pair_to_f16x2(w);
+              bb[2 * t4 + 1][0] = e4m3pair_to_f16x2(u >> 16);
+              bb[2 * t4 + 1][1] = e4m3pair_to_f16x2(w >> 16);
+              mma_f16(oacc[16 * qd + 2 * t4], pa, bb[2 * t4][0], bb[2 * t4][1]);
+              mma_f16(oacc[16 * qd + 2 * t4 + 1], pa, bb[2 * t4 + 1][0], bb[2 * t4 + 1][1]);
             }
+#pragma unroll
+            for (int tt = 0; tt < 16; ++tt) mma_f16(oacc[16 * qd + tt], pl, bb[tt][0], bb[tt][1]);
           }
         }
       }
