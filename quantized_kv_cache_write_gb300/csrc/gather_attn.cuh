@@ -7,21 +7,31 @@
 // split-K merge); "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache" §Implementation
 // scope (split-K workspace).
 //
-// Work decomposition: one CTA (4 warps) per (query row, KV head, K-split). The split's
-// index columns are cut into tiles of 16 keys, dealt round-robin to the warps; every warp
-// then runs on its own -- its own cp.async ring (16 B copies, rows XOR-swizzled so all
-// fragment reads are bank-conflict free), its own online softmax, its own accumulators --
-// with no block barrier in the main loop. The four partial results are merged once, at the
-// end, through shared memory.
+// Work decomposition: one CTA (4 warps) per (query row, KV head, K-split). The split's index
+// columns are cut into tiles of 16 keys, dealt round-robin to the warps; every warp then runs
+// on its own -- its own copy ring, online softmax and accumulators -- with no block barrier
+// in the main loop. The four partial results are merged once, at the end, through shared
+// memory.
+//
+// Gathering: 16 B cp.async copies, consecutive lanes on consecutive chunks of a row (whole
+// lines per request), into a two-stage ring per warp. The rows' placement keeps every
+// fragment read below bank-conflict free: odd K rows sit 64 B (bf16: 16 B) further along the
+// bank cycle than even ones, and V row r lands in one of 8 regions whose start rotates with r.
+// (Bulk copies on the TMA engine, one 256 B row each, were measured slower on this access
+// pattern: 6.4 vs 4.8 TB/s of gathered rows with the math removed.)
+//
+// Accumulators: each warp's 16 x 256 fp32 p.V accumulator lives in tensor memory (TMEM,
+// 32 lanes x 128 columns per warp) and streams through registers a quarter at a time around
+// the MMAs. Registers are what bound this kernel's occupancy; holding the accumulator in
+// TMEM leaves room for three CTAs (12 warps) per SM instead of two.
 //
 // Per 16-key tile and warp:
 //   q.K^T  mma.sync m16n8k16, M = the GQA group (16 query heads, padded), N = 8 keys, K = 16
-//          head dims; 4 independent accumulator chains. Query fragments come from shared
-//          memory (ldmatrix; staged once per CTA as fp16 with a per-head power of two, bf16
-//          for the bf16 layout). Key codes are dequantised straight into B fragments
-//          (int8 -> fp16 by an exponent splice, E4M3 -> fp16 by the native cvt, bf16 as
-//          stored); the head-dim order inside a fragment follows how a code word unpacks and
-//          the staged query uses the same permutation.
+//          head dims. Query fragments come from shared memory (ldmatrix; staged once per CTA
+//          as fp16 with a per-head power of two, bf16 for the bf16 layout). Key codes are
+//          dequantised straight into B fragments (int8 -> fp16 by an exponent splice, E4M3 ->
+//          fp16 by the native cvt, bf16 as stored); the head-dim order inside a fragment
+//          follows how a code word unpacks and the staged query uses the same permutation.
 //   softmax  logits times the hoisted K scale (per slot for int8; E4M3's per-layer scale is
 //          folded into the per-head factor). The running max is only raised when a tile's max
 //          exceeds it by more than 2^8 (log2 domain), so the accumulators are rescaled a few
@@ -30,8 +40,8 @@
 //          the m16k16 A layout) as an fp16 hi + lo pair (bf16 pair for the bf16 layout): with
 //          outlier tokens a row can be a near-even mix of two large V rows of opposite sign,
 //          and single-fp16 p would lose ~1e-3 of the result to cancellation. int8 p also
-//          carries the slot's V scale and a power of two keeping it a normal fp16. 32 N-tiles
-//          of 8 head dims each, two MMAs (hi, lo) per tile, V codes dequantised in registers.
+//          carries the slot's V scale and a power of two keeping it a normal fp16. 32 N-tiles:
+//          N-tile 16 s + t, column n covers head dim 128 s + 16 n + t; two MMAs (hi, lo) each.
 // The E4M3 V scale and the power-of-two pre-scale are applied once at the end; split partials
 // are written normalised, without the E4M3 V scale.
 #pragma once
@@ -48,32 +58,42 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units): p <= 2^8
 constexpr int kPShift = 7;    // p * 2^7 <= 2^15 stays a finite fp16; p >= 2^-21 stays normal
+constexpr int kTmemCols = 128;  // per CTA: 4 warps x (their 32 lanes) x 128 fp32 columns
 
+// kRowBytes: bytes of one K (or V) row in shared memory (the inline layout keeps the 272 B
+// of 17 aligned 16 B chunks that cover any 260 B record starting on a 4 B boundary).
+// kKShift: extra offset of the odd K rows.
 template <int FMT>
 struct Fmt;
 template <>
 struct Fmt<QKV_INT8_SIDE> {
-  static constexpr int kRowBytes = 256, kGlobalRow = 256, kChunks = 16, kStages = 3, kMinBlocks = 2;
+  static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
   static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false;
 };
 template <>
 struct Fmt<QKV_INT8_INLINE> {
-  // 17 aligned 16 B chunks cover any 260 B record that starts on a 4 B boundary.
-  static constexpr int kRowBytes = 272, kGlobalRow = kInlineRecord, kChunks = 17, kStages = 3, kMinBlocks = 2;
+  static constexpr int kRowBytes = 272, kGlobalRow = kInlineRecord, kStages = 2, kMinBlocks = 2, kKShift = 16;
   static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false;
 };
 template <>
 struct Fmt<QKV_E4M3> {
-  static constexpr int kRowBytes = 256, kGlobalRow = 256, kChunks = 16, kStages = 3, kMinBlocks = 2;
+  static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false;
 };
 template <>
 struct Fmt<QKV_BF16> {
-  static constexpr int kRowBytes = 512, kGlobalRow = 512, kChunks = 32, kStages = 3, kMinBlocks = 1;
+  static constexpr int kRowBytes = 512, kGlobalRow = 512, kStages = 2, kMinBlocks = 1, kKShift = 16;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true;
 };
 
-constexpr int kORow = 292;  // floats per head row of the final merge buffer (bank-conflict-free)
+// V region i (rows i and i + 8) starts 16 B further along the bank cycle than a plain packing
+// would put it: by i chunks for 256 B rows, by 0, 0, 1, 1, 4, 4, 5, 5 chunks for bf16 rows.
+template <int FMT>
+__host__ __device__ constexpr int v_region_shift(int i) {
+  return Fmt<FMT>::kBf16 ? 16 * ((((i >> 1) & 1)) | (((i >> 2) & 1) << 2)) : 16 * i;
+}
+
+constexpr int kORow = 164;  // floats per head row of the merge buffer, one 128-dim half (bank-conflict-free)
 
 template <int FMT>
 struct Smem {
@@ -81,35 +101,40 @@ struct Smem {
   static constexpr size_t kQ = 0;  // [16 k-steps][16 heads][16] 16-bit, fragment order
   static constexpr size_t kQBytes = 16 * 16 * 16 * 2;
   static constexpr size_t kFac = kQ + kQBytes;  // [16] floats: logit factor per head
+  // one stage: K rows, V rows, side scales (K then V), inline record offsets
+  static constexpr size_t kKArea = 2 * 8 * size_t(F::kRowBytes) + F::kKShift;
+  static constexpr size_t kVRegion = 2 * size_t(F::kRowBytes);
+  static constexpr size_t kVArea = 8 * kVRegion + v_region_shift<FMT>(7);
   static constexpr size_t kStageK = 0;
-  static constexpr size_t kStageV = size_t(kKeys) * F::kRowBytes;
-  static constexpr size_t kStageKs = 2 * size_t(kKeys) * F::kRowBytes;  // side: K then V scales
-  static constexpr size_t kStageMeta = kStageKs + (F::kSide ? 2 * kKeys * 4 : 0);  // inline: record offsets
-  static constexpr size_t kStageBytes = kStageMeta + (F::kInline ? kKeys : 0);
+  static constexpr size_t kStageV = kKArea;
+  static constexpr size_t kStageKs = kStageV + kVArea;
+  static constexpr size_t kStageMeta = kStageKs + (F::kSide ? 2 * kKeys * 4 : 0);
+  static constexpr size_t kStageBytes = ((kStageMeta + (F::kInline ? kKeys : 0)) + 15) / 16 * 16;
   static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][kStages] stages
   static constexpr size_t kWarpRing = size_t(F::kStages) * kStageBytes;
-  static constexpr size_t kMask = kRing + kWarps * kWarpRing;  // [kWarps][kStages] uint32
-  static constexpr size_t kM = kMask + kWarps * F::kStages * 4;  // [kWarps][16] floats
-  static constexpr size_t kL = kM + kWarps * 16 * 4;              // [kWarps][16] floats
+  static constexpr size_t kTmem = kRing + kWarps * kWarpRing;  // TMEM base address
+  static constexpr size_t kMask = kTmem + 16;                     // [kWarps][kStages] uint32
+  static constexpr size_t kM = kMask + kWarps * F::kStages * 4;      // [kWarps][16] floats
+  static constexpr size_t kL = kM + kWarps * 16 * 4;                 // [kWarps][16] floats
   static constexpr size_t kTotal = kL + kWarps * 16 * 4;
   // final merge buffer [kWarps][16][kORow] floats, reusing the rings
   static_assert(size_t(kWarps) * 16 * kORow * 4 <= kWarps * kWarpRing, "merge buffer must fit in the rings");
-  static_assert(kRing % 16 == 0 && kStageBytes % 16 == 0, "16 B alignment of the cp.async destinations");
+  static_assert(kRing % 16 == 0 && kKArea % 16 == 0 && kVArea % 16 == 0, "alignment");
+  // the CTAs that fit an SM (228 KB of shared memory, 1 KB reserved each) never ask for more
+  // than its 512 TMEM columns, so an allocation never has to wait for another CTA
+  static_assert((233472 / (kTotal + 1024)) * kTmemCols <= 512, "TMEM budget");
 };
 
-// Shared-memory 16 B chunk position of chunk j of K / V tile row `row`.
+// Byte offsets of tile row r (0..15) inside a stage (K area, V area).
 template <int FMT>
-__device__ __forceinline__ int swz_k(int j, int row) {
-  if (Fmt<FMT>::kInline) return j;
-  if (Fmt<FMT>::kBf16) return j ^ (row & 1);
-  return j ^ ((row & 1) << 2);
+__device__ __forceinline__ uint32_t k_row_off(int r) {
+  constexpr int RB = Fmt<FMT>::kRowBytes;
+  return RB * (r >> 1) + (r & 1) * (8 * RB + Fmt<FMT>::kKShift);
 }
 template <int FMT>
-__device__ __forceinline__ int swz_v(int j, int row) {
-  if (Fmt<FMT>::kInline) return j;
-  const int i = (row >> 1) & 3;
-  if (Fmt<FMT>::kBf16) return j ^ i;
-  return j ^ ((i & 1) | ((i & 2) << 1));  // 0, 1, 4, 5
+__device__ __forceinline__ uint32_t v_row_off(int r) {
+  constexpr int RB = Fmt<FMT>::kRowBytes;
+  return Smem<FMT>::kStageV + (r & 7) * (2 * RB) + v_region_shift<FMT>(r & 7) + RB * (r >> 3);
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
@@ -140,6 +165,11 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + L::kMask) + warp * F::kStages;
   uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
   const uint32_t sQ = smem_u32(smem + L::kQ);
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kTmem);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(sTmem), kTmemCols);
+    tmem_relinquish_alloc_permit();
+  }
 
   // ---------------- this warp's tiles: split tiles warp, warp + 4, ...
   const int ntiles = (col1 - col0 + kKeys - 1) / kKeys;
@@ -158,58 +188,55 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     return v;
   };
 
-  // Copy one 16-key tile into ring stage i % kStages. Each warp-wide copy instruction moves
-  // whole rows: lanes 0-15 take the 16 B chunks of one key's 256 B row, lanes 16-31 the next
-  // key's (bf16: all 32 lanes on one 512 B row), so every request is a full, coalesced line.
+  // Copy one 16-key tile into ring stage i % kStages.
   auto issue = [&](int i, int idxv) {
     const int st = i % F::kStages;
     const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
     if (lane == 0) sMask[st] = mask;
     uint8_t* sb = ring + size_t(st) * L::kStageBytes;
-    constexpr int kKeysPerCopy = F::kBf16 ? 1 : 2;
-    constexpr int kLanesPerKey = 32 / kKeysPerCopy;
-    const int sub = lane / kLanesPerKey, j = lane % kLanesPerKey;
-#pragma unroll 4
-    for (int t = 0; t < kKeys / kKeysPerCopy; ++t) {
-      const int key = t * kKeysPerCopy + sub;
-      int slot = __shfl_sync(0xffffffffu, idxv, key);
-      const bool valid = slot >= 0;
-      slot = valid ? slot : 0;
-      const int64_t rec = static_cast<int64_t>(slot) * H + h;
-      const uint32_t dK = smem_u32(sb + L::kStageK + key * F::kRowBytes);
-      const uint32_t dV = smem_u32(sb + L::kStageV + key * F::kRowBytes);
-      if (F::kInline) {
-        const int64_t off = rec * F::kGlobalRow;
-        const int64_t al = off & ~int64_t(15);
-        const int delta = static_cast<int>(off - al);
-        const uint8_t* gK = a.k_cache + al;
-        const uint8_t* gV = a.v_cache + al;
-        const int nb = valid ? 16 : 0;
-        cp_async16(dK + j * 16, gK + j * 16, nb);
-        cp_async16(dV + j * 16, gV + j * 16, nb);
-        if (j == 0) {
-          // the 17th chunk copies only the record's own bytes (never past the pool's end)
-          const int nl = valid ? delta + 4 : 0;
-          cp_async16(dK + 16 * 16, gK + 16 * 16, nl);
-          cp_async16(dV + 16 * 16, gV + 16 * 16, nl);
-          sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
+    const uint32_t sbase = smem_u32(sb);
+    {
+      // 16 B copies: consecutive lanes take consecutive chunks of a row (whole lines)
+      constexpr int kChunks = F::kInline ? 17 : F::kRowBytes / 16;
+      constexpr int kTotalCopies = kKeys * kChunks;
+      constexpr int kIters = (kTotalCopies + 31) / 32;
+#pragma unroll
+      for (int t = 0; t < kIters; ++t) {
+        const int e = lane + 32 * t;
+        const bool act = e < kTotalCopies;
+        const int key = act ? e / kChunks : 0;
+        const int jj = e - key * kChunks;
+        int slot = __shfl_sync(0xffffffffu, idxv, key);
+        const bool valid = slot >= 0;
+        slot = valid ? slot : 0;
+        const int64_t rec = static_cast<int64_t>(slot) * H + h;
+        if (act) {
+          const uint32_t dK = sbase + k_row_off<FMT>(key) + jj * 16;
+          const uint32_t dV = sbase + v_row_off<FMT>(key) + jj * 16;
+          if (F::kInline) {
+            const int64_t off = rec * F::kGlobalRow;
+            const int64_t al = off & ~int64_t(15);
+            const int delta = static_cast<int>(off - al);
+            // the 17th chunk copies only the record's own bytes (never past the pool's end)
+            const int nb = valid ? (jj == kChunks - 1 ? delta + 4 : 16) : 0;
+            cp_async16(dK, a.k_cache + al + jj * 16, nb);
+            cp_async16(dV, a.v_cache + al + jj * 16, nb);
+            if (jj == 0) sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
+          } else {
+            const int nb = valid ? 16 : 0;
+            cp_async16(dK, a.k_cache + rec * F::kGlobalRow + jj * 16, nb);
+            cp_async16(dV, a.v_cache + rec * F::kGlobalRow + jj * 16, nb);
+          }
         }
-      } else {
-        const uint8_t* gK = a.k_cache + rec * F::kGlobalRow;
-        const uint8_t* gV = a.v_cache + rec * F::kGlobalRow;
-        const int nb = valid ? 16 : 0;
-        cp_async16(dK + swz_k<FMT>(j, key) * 16, gK + j * 16, nb);
-        cp_async16(dV + swz_v<FMT>(j, key) * 16, gV + j * 16, nb);
       }
     }
     if (F::kSide) {
-      // lanes 0-15: K scales of the 16 keys; lanes 16-31: V scales
-      const int key = lane & 15;
-      int slot = __shfl_sync(0xffffffffu, idxv, key);
+      // lanes 0-15: K scales of the 16 keys; lanes 16-31: V scales (zero for padding)
+      int slot = __shfl_sync(0xffffffffu, idxv, lane & 15);
       const bool valid = slot >= 0;
       slot = valid ? slot : 0;
       const float* gs = (lane >> 4) ? a.v_scale_tok : a.k_scale_tok;
-      cp_async4(smem_u32(sb + L::kStageKs + lane * 4), gs + static_cast<int64_t>(slot) * H + h, valid ? 4 : 0);
+      cp_async4(sbase + L::kStageKs + lane * 4, gs + static_cast<int64_t>(slot) * H + h, valid ? 4 : 0);
     }
   };
 
@@ -281,59 +308,65 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       sFac[qh] = live ? base * pow2f(-sg) : 0.f;
     }
   }
+  tmem_fence_before_sync();
   __syncthreads();
+  tmem_fence_after_sync();
   const float fac0 = sFac[h0], fac1 = sFac[h1];
+  // this warp's accumulator: its 32 TMEM lanes, columns [0, 128); column 4 t + j holds the
+  // C-fragment value j of N-tile t
+  const uint32_t tacc = *sTmem + (static_cast<uint32_t>(32 * warp) << 16);
+  {
+    float z[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) tmem_st32(tacc + 32 * q, z);
+  }
 
   // ---------------- online-softmax state (per warp)
   float mu0 = -INFINITY, mu1 = -INFINITY;  // running max in use (log2 domain), heads h0, h1
   float l0 = 0.f, l1 = 0.f;                // this thread's share of sum p
   int eu = -100;                           // int8: 2^eu > every V scale seen
-  float oacc[32][4];
-#pragma unroll
-  for (int t = 0; t < 32; ++t) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
-
-
   for (int i = 0; i < my; ++i) {
     if (i + F::kStages - 1 < my) issue(i + F::kStages - 1, nidx);
     cp_async_commit();
     nidx = load_idx(i + F::kStages);
     cp_async_wait<F::kStages - 1>();
+    const int st = i % F::kStages;
     __syncwarp();
 
-    const int st = i % F::kStages;
     const uint8_t* sb = ring + size_t(st) * L::kStageBytes;
-    const uint8_t* tK = sb + L::kStageK;
-    const uint8_t* tV = sb + L::kStageV;
+    const uint32_t sbase = smem_u32(sb);
     const uint32_t mask = lds32(smem_u32(sMask + st));
 
-    // ---- q . K^T: acc[nt][parity of the head-dim block]
+    // ---- q . K^T for this warp's 16 keys: acc[nt][parity of the head-dim block]
     float acc[2][2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int pz = 0; pz < 2; ++pz) acc[nt][pz][0] = acc[nt][pz][1] = acc[nt][pz][2] = acc[nt][pz][3] = 0.f;
+    uint32_t rowK[2];
     int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
-    if (F::kInline) {
-      delta_k[0] = lds_u8(smem_u32(sb + L::kStageMeta + hn));
-      delta_k[1] = lds_u8(smem_u32(sb + L::kStageMeta + 8 + hn));
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      rowK[nt] = sbase + k_row_off<FMT>(nt * 8 + hn);
+      if (F::kInline) delta_k[nt] = lds_u8(sbase + L::kStageMeta + nt * 8 + hn);
     }
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
       uint32_t kw[2][8];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const int row = nt * 8 + hn;
-        const uint32_t rowK = smem_u32(tK + row * F::kRowBytes);
         if (F::kBf16) {
-          const uint4 x = lds128(rowK + (swz_k<FMT>(8 * blk + 2 * c, row) << 4));
-          const uint4 y = lds128(rowK + (swz_k<FMT>(8 * blk + 2 * c + 1, row) << 4));
+          const uint4 x = lds128(rowK[nt] + (8 * blk + 2 * c) * 16);
+          const uint4 y = lds128(rowK[nt] + (8 * blk + 2 * c + 1) * 16);
           kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
           kw[nt][4] = y.x; kw[nt][5] = y.y; kw[nt][6] = y.z; kw[nt][7] = y.w;
         } else if (F::kInline) {
-          const uint32_t p = rowK + delta_k[nt] + 64 * blk + 16 * c;
+          const uint32_t p = rowK[nt] + delta_k[nt] + 64 * blk + 16 * c;
           kw[nt][0] = lds32(p); kw[nt][1] = lds32(p + 4); kw[nt][2] = lds32(p + 8); kw[nt][3] = lds32(p + 12);
         } else {
-          const uint4 x = lds128(rowK + (swz_k<FMT>(4 * blk + c, row) << 4));
+          const uint4 x = lds128(rowK[nt] + (4 * blk + c) * 16);
           kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
         }
       }
@@ -371,12 +404,12 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         const bool valid = (mask >> kt) & 1u;
         float ksc = 1.f, vs = 0.f;
         if (F::kSide) {
-          ksc = __uint_as_float(lds32(smem_u32(sb + L::kStageKs + kt * 4)));
-          vs = __uint_as_float(lds32(smem_u32(sb + L::kStageKs + (kKeys + kt) * 4)));
+          ksc = __uint_as_float(lds32(sbase + L::kStageKs + kt * 4));
+          vs = __uint_as_float(lds32(sbase + L::kStageKs + (kKeys + kt) * 4));
         } else if (F::kInline) {
-          const int dl = lds_u8(smem_u32(sb + L::kStageMeta + kt));
-          ksc = __uint_as_float(lds32(smem_u32(tK + kt * F::kRowBytes + dl + kHeadDim)));
-          vs = __uint_as_float(lds32(smem_u32(tV + kt * F::kRowBytes + dl + kHeadDim)));
+          const int dl = lds_u8(sbase + L::kStageMeta + kt);
+          ksc = __uint_as_float(lds32(sbase + k_row_off<FMT>(kt) + dl + kHeadDim));
+          vs = __uint_as_float(lds32(sbase + v_row_off<FMT>(kt) + dl + kHeadDim));
         }
         vs = valid ? vs : 0.f;
         vsc[nt][e] = vs;
@@ -396,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     }
 
     // ---- lazy rescale: raise the max in use only past the threshold
+    bool rescale;
+    float rf0 = 1.f, rf1 = 1.f;  // accumulator factors for heads h0, h1 when rescaling
     {
       const float nm0 = (mx0 > mu0 + kTau) ? mx0 : mu0;
       const float nm1 = (mx1 > mu1 + kTau) ? mx1 : mu1;
@@ -404,15 +439,10 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       const float ov = F::kInt8 ? pow2f(max(eu - ne, -126)) : 1.f;
       const float al0 = (nm0 == mu0) ? 1.f : fast_exp2(mu0 - nm0);  // mu0 = -inf gives 0
       const float al1 = (nm1 == mu1) ? 1.f : fast_exp2(mu1 - nm1);
-      if (__any_sync(0xffffffffu, nm0 != mu0 || nm1 != mu1 || ne != eu)) {
-        const float f0 = al0 * ov, f1 = al1 * ov;
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          oacc[t][0] *= f0;
-          oacc[t][1] *= f0;
-          oacc[t][2] *= f1;
-          oacc[t][3] *= f1;
-        }
+      rescale = __any_sync(0xffffffffu, nm0 != mu0 || nm1 != mu1 || ne != eu);
+      if (rescale) {
+        rf0 = al0 * ov;
+        rf1 = al1 * ov;
         l0 *= al0;
         l1 *= al1;
       }
@@ -454,58 +484,60 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       }
     }
 
-    // ---- p . V over the 256 head dims: N-tile t covers head dims 32*n + t (n = lane / 4)
+    // ---- p . V: sweep sw covers head dims [128 sw, 128 sw + 128); lane group n reads the
+    //      16 head dims 128 sw + 16 n .. + 16 of the rows 2c, 2c + 1, 2c + 8, 2c + 9
     {
       const int rows[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
-      if (F::kBf16) {
+      uint32_t rowV[4];
+      int dv[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int qd = 0; qd < 4; ++qd) {  // 16 B chunk 4n + qd: head dims 32n + 8qd .. + 8
-          uint32_t vw[4][4];
+      for (int ri = 0; ri < 4; ++ri) {
+        rowV[ri] = sbase + v_row_off<FMT>(rows[ri]);
+        if (F::kInline) dv[ri] = lds_u8(sbase + L::kStageMeta + rows[ri]);
+      }
+#pragma unroll
+      for (int sw = 0; sw < 2; ++sw) {
+        // accumulator quarters 2 sw (N-tiles 16 sw + 0..7) and 2 sw + 1 (16 sw + 8..15)
+        float ob[2][32];
+        tmem_wait_st();  // the previous stores of these registers' columns are done
+        tmem_ld32(tacc + 64 * sw, ob[0]);
+        tmem_ld32(tacc + 64 * sw + 32, ob[1]);
+        uint32_t bb[16][2];
+        if (F::kBf16) {
+          uint32_t vw[4][8];
 #pragma unroll
           for (int ri = 0; ri < 4; ++ri) {
-            const uint4 x = lds128(smem_u32(tV + rows[ri] * F::kRowBytes) + (swz_v<FMT>(4 * hn + qd, rows[ri]) << 4));
+            const uint32_t p = rowV[ri] + 2 * (128 * sw + 16 * hn);
+            const uint4 x = lds128(p), y = lds128(p + 16);
             vw[ri][0] = x.x; vw[ri][1] = x.y; vw[ri][2] = x.z; vw[ri][3] = x.w;
+            vw[ri][4] = y.x; vw[ri][5] = y.y; vw[ri][6] = y.z; vw[ri][7] = y.w;
           }
-          uint32_t bb[8][2];
 #pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
+          for (int tt = 0; tt < 16; ++tt) {
             const uint32_t sel = (tt & 1) ? 0x7632u : 0x5410u;
             bb[tt][0] = __byte_perm(vw[0][tt >> 1], vw[1][tt >> 1], sel);
             bb[tt][1] = __byte_perm(vw[2][tt >> 1], vw[3][tt >> 1], sel);
-            mma_bf16(oacc[8 * qd + tt], pa, bb[tt][0], bb[tt][1]);
           }
-#pragma unroll
-          for (int tt = 0; tt < 8; ++tt) mma_bf16(oacc[8 * qd + tt], pl, bb[tt][0], bb[tt][1]);
-        }
-      } else {
-#pragma unroll
-        for (int qd = 0; qd < 2; ++qd) {  // 16 B chunk 2n + qd: head dims 32n + 16qd .. + 16
+        } else {
           uint32_t vw[4][4];
 #pragma unroll
           for (int ri = 0; ri < 4; ++ri) {
+            const uint32_t p = rowV[ri] + dv[ri] + 128 * sw + 16 * hn;
             if (F::kInline) {
-              const uint32_t p =
-                  smem_u32(tV + rows[ri] * F::kRowBytes) + lds_u8(smem_u32(sb + L::kStageMeta + rows[ri])) + 32 * hn + 16 * qd;
               vw[ri][0] = lds32(p); vw[ri][1] = lds32(p + 4); vw[ri][2] = lds32(p + 8); vw[ri][3] = lds32(p + 12);
             } else {
-              const uint4 x =
-                  lds128(smem_u32(tV + rows[ri] * F::kRowBytes) + (swz_v<FMT>(2 * hn + qd, rows[ri]) << 4));
+              const uint4 x = lds128(p);
               vw[ri][0] = x.x; vw[ri][1] = x.y; vw[ri][2] = x.z; vw[ri][3] = x.w;
             }
           }
           if (F::kInt8) {
-            uint32_t bb[16][2];
 #pragma unroll
             for (int tt = 0; tt < 16; ++tt) {
               const uint32_t sel = (tt & 3) | (((tt & 3) + 4) << 8);
               bb[tt][0] = i8pair_to_f16x2(__byte_perm(vw[0][tt >> 2], vw[1][tt >> 2], sel));
               bb[tt][1] = i8pair_to_f16x2(__byte_perm(vw[2][tt >> 2], vw[3][tt >> 2], sel));
-              mma_f16(oacc[16 * qd + tt], pa, bb[tt][0], bb[tt][1]);
             }
-#pragma unroll
-            for (int tt = 0; tt < 16; ++tt) mma_f16(oacc[16 * qd + tt], pl, bb[tt][0], bb[tt][1]);
           } else {
-            uint32_t bb[16][2];
 #pragma unroll
             for (int t4 = 0; t4 < 8; ++t4) {  // [a_t, b_t, a_t+1, b_t+1] pairs, t = 2*t4
               const uint32_t sel = (t4 & 1) ? 0x7362u : 0x5140u;
@@ -515,106 +547,149 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
               bb[2 * t4][1] = e4m3pair_to_f16x2(w);
               bb[2 * t4 + 1][0] = e4m3pair_to_f16x2(u >> 16);
               bb[2 * t4 + 1][1] = e4m3pair_to_f16x2(w >> 16);
-              mma_f16(oacc[16 * qd + 2 * t4], pa, bb[2 * t4][0], bb[2 * t4][1]);
-              mma_f16(oacc[16 * qd + 2 * t4 + 1], pa, bb[2 * t4 + 1][0], bb[2 * t4 + 1][1]);
             }
-#pragma unroll
-            for (int tt = 0; tt < 16; ++tt) mma_f16(oacc[16 * qd + tt], pl, bb[tt][0], bb[tt][1]);
           }
         }
+        tmem_wait_ld(ob[0]);
+        tmem_wait_ld(ob[1]);
+        if (rescale) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              ob[b][4 * t] *= rf0;
+              ob[b][4 * t + 1] *= rf0;
+              ob[b][4 * t + 2] *= rf1;
+              ob[b][4 * t + 3] *= rf1;
+            }
+        }
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+          float* acc4 = &ob[tt >> 3][4 * (tt & 7)];
+          if (F::kBf16)
+            mma_bf16(acc4, pa, bb[tt][0], bb[tt][1]);
+          else
+            mma_f16(acc4, pa, bb[tt][0], bb[tt][1]);
+        }
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+          float* acc4 = &ob[tt >> 3][4 * (tt & 7)];
+          if (F::kBf16)
+            mma_bf16(acc4, pl, bb[tt][0], bb[tt][1]);
+          else
+            mma_f16(acc4, pl, bb[tt][0], bb[tt][1]);
+        }
+        tmem_st32(tacc + 64 * sw, ob[0]);
+        tmem_st32(tacc + 64 * sw + 32, ob[1]);
       }
     }
     __syncwarp();
   }
 
-  // ---------------- merge the four warps' partial results
+  // ---------------- merge the four warps' partial results, one 128-dim half at a time
   cp_async_wait<0>();
 #pragma unroll
   for (int off = 1; off <= 2; off <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
   }
-  __syncthreads();  // every warp is done with its ring: reuse it as the merge buffer
+  tmem_wait_st();
+  __syncthreads();  // every warp is done with its ring: reuse the rings as the merge buffer
   float* sO = reinterpret_cast<float*>(smem + L::kRing);  // [kWarps][16][kORow]
   float* sM = reinterpret_cast<float*>(smem + L::kM);
   float* sL = reinterpret_cast<float*>(smem + L::kL);
-  {
-    float post = 1.f;
-    if (F::kInt8) post = pow2f(eu - kPShift);
-    if (F::kE4m3) post = pow2f(-kPShift);
-    float* o0 = sO + (warp * 16 + h0) * kORow + 72 * c;
-    float* o1 = sO + (warp * 16 + h1) * kORow + 72 * c;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      // head dims 64c + 4j .. + 3 (N-tiles 4j..4j+3, column 2c) and 64c + 32 + 4j .. (column 2c+1)
-      reinterpret_cast<float4*>(o0)[j] = make_float4(oacc[4 * j][0] * post, oacc[4 * j + 1][0] * post,
-                                                     oacc[4 * j + 2][0] * post, oacc[4 * j + 3][0] * post);
-      reinterpret_cast<float4*>(o0 + 32)[j] = make_float4(oacc[4 * j][1] * post, oacc[4 * j + 1][1] * post,
-                                                          oacc[4 * j + 2][1] * post, oacc[4 * j + 3][1] * post);
-      reinterpret_cast<float4*>(o1)[j] = make_float4(oacc[4 * j][2] * post, oacc[4 * j + 1][2] * post,
-                                                     oacc[4 * j + 2][2] * post, oacc[4 * j + 3][2] * post);
-      reinterpret_cast<float4*>(o1 + 32)[j] = make_float4(oacc[4 * j][3] * post, oacc[4 * j + 1][3] * post,
-                                                          oacc[4 * j + 2][3] * post, oacc[4 * j + 3][3] * post);
-    }
-    if (c == 0) {
-      sM[warp * 16 + h0] = mu0;
-      sM[warp * 16 + h1] = mu1;
-      sL[warp * 16 + h0] = l0;
-      sL[warp * 16 + h1] = l1;
-    }
+  if (c == 0) {
+    sM[warp * 16 + h0] = mu0;
+    sM[warp * 16 + h1] = mu1;
+    sL[warp * 16 + h0] = l0;
+    sL[warp * 16 + h1] = l1;
   }
+  float post = 1.f;
+  if (F::kInt8) post = pow2f(eu - kPShift);
+  if (F::kE4m3) post = pow2f(-kPShift);
+#pragma unroll 1
+  for (int sw = 0; sw < 2; ++sw) {
+    {
+      float ob[2][32];
+      tmem_ld32(tacc + 64 * sw, ob[0]);
+      tmem_ld32(tacc + 64 * sw + 32, ob[1]);
+      tmem_wait_ld(ob[0]);
+      tmem_wait_ld(ob[1]);
+      // local head dim 32 c + x sits at 40 c + x of a head row: x < 8 and 16 <= x < 24 come
+      // from quarter 0 (columns 2c and 2c + 1 of N-tile x mod 8), the others from quarter 1
+      float* o0 = sO + (warp * 16 + h0) * kORow + 40 * c;
+      float* o1 = sO + (warp * 16 + h1) * kORow + 40 * c;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int b = (k >> 1) & 1;            // quarter of x = 4k .. 4k + 3
+        const int j = (k >> 2);                // column 2c (0) or 2c + 1 (1)
+        const int t = 4 * (k & 1);             // first N-tile within the quarter
+        const float* q = ob[b];
+        reinterpret_cast<float4*>(o0)[k] = make_float4(q[4 * t + j] * post, q[4 * (t + 1) + j] * post,
+                                                       q[4 * (t + 2) + j] * post, q[4 * (t + 3) + j] * post);
+        reinterpret_cast<float4*>(o1)[k] = make_float4(q[4 * t + 2 + j] * post, q[4 * (t + 1) + 2 + j] * post,
+                                                       q[4 * (t + 2) + 2 + j] * post, q[4 * (t + 3) + 2 + j] * post);
+      }
+    }
+    __syncthreads();
+    {
+      const int hh = tid >> 3, part = tid & 7;  // head, local head dims [16 part, 16 part + 16)
+      if (hh < G) {
+        float mw[kWarps], M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          mw[w] = sM[w * 16 + hh];
+          M = fmaxf(M, mw[w]);
+        }
+        float ww[kWarps], lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          ww[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+          lsum += ww[w] * sL[w * 16 + hh];
+        }
+        float f = (lsum > 0.f) ? 1.f / lsum : 0.f;
+        if (F::kE4m3 && P == 1) f *= a.v_scale_layer;
+        float res[16];
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) res[i2] = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float4* src =
+              reinterpret_cast<const float4*>(sO + (w * 16 + hh) * kORow + 40 * (part >> 1) + 16 * (part & 1));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float4 x = src[k];
+            res[4 * k] += ww[w] * x.x;
+            res[4 * k + 1] += ww[w] * x.y;
+            res[4 * k + 2] += ww[w] * x.z;
+            res[4 * k + 3] += ww[w] * x.w;
+          }
+        }
+        const int64_t qhead = static_cast<int64_t>(h) * G + hh;
+        float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
+                              : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
+        dst += 128 * sw + 16 * part;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          reinterpret_cast<float4*>(dst)[k] =
+              make_float4(res[4 * k] * f, res[4 * k + 1] * f, res[4 * k + 2] * f, res[4 * k + 3] * f);
+        if (sw == 0 && part == 0) {
+          const float lse = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+          if (P == 1) {
+            if (a.lse != nullptr) a.lse[r * Hq + qhead] = lse;
+          } else {
+            a.lse_part[(r * P + split) * Hq + qhead] = lse;
+          }
+        }
+      }
+    }
+    __syncthreads();  // the merge buffer is rewritten by the next half
+  }
+  // every warp's TMEM accesses are complete (the loads above were waited for): free the columns
+  tmem_fence_before_sync();
   __syncthreads();
-  {
-    const int hh = tid >> 3, part = tid & 7;  // head, 32 head dims
-    if (hh < G) {
-      float mw[kWarps], M = -INFINITY;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        mw[w] = sM[w * 16 + hh];
-        M = fmaxf(M, mw[w]);
-      }
-      float ww[kWarps], lsum = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        ww[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-        lsum += ww[w] * sL[w * 16 + hh];
-      }
-      float f = (lsum > 0.f) ? 1.f / lsum : 0.f;
-      if (F::kE4m3 && P == 1) f *= a.v_scale_layer;
-      float res[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) res[i] = 0.f;
-      const int cb = part >> 1, hb = part & 1;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float4* src = reinterpret_cast<const float4*>(sO + (w * 16 + hh) * kORow + 72 * cb + 32 * hb);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 x = src[j];
-          res[4 * j] += ww[w] * x.x;
-          res[4 * j + 1] += ww[w] * x.y;
-          res[4 * j + 2] += ww[w] * x.z;
-          res[4 * j + 3] += ww[w] * x.w;
-        }
-      }
-      const int64_t qhead = static_cast<int64_t>(h) * G + hh;
-      float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
-                            : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
-      dst += 32 * part;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        reinterpret_cast<float4*>(dst)[j] =
-            make_float4(res[4 * j] * f, res[4 * j + 1] * f, res[4 * j + 2] * f, res[4 * j + 3] * f);
-      if (part == 0) {
-        const float lse = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;
-        if (P == 1) {
-          if (a.lse != nullptr) a.lse[r * Hq + qhead] = lse;
-        } else {
-          a.lse_part[(r * P + split) * Hq + qhead] = lse;
-        }
-      }
-    }
-  }
+  tmem_fence_after_sync();
+  if (warp == 0) tmem_dealloc(*sTmem, kTmemCols);
 }
 
 template <int FMT>
