@@ -124,6 +124,7 @@ qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, flo
  *
  *   q             bf16 [rows, num_q_heads, head_dim], contiguous, 16 B-aligned.
  *   fmt           pool layout (see above). k_cache / v_cache base pointers 16 B-aligned.
+ *                 S * num_kv_heads must stay <= 2^31 - 1 (else QKV_ERR_UNSUPPORTED).
  *   k_scale_tok, v_scale_tok  fp32 [S, H] for QKV_INT8_SIDE, else must be NULL.
  *   k_scale_layer, v_scale_layer  per-layer scales for QKV_E4M3 (finite, > 0, else
  *                 QKV_ERR_SCALE); ignored for the other formats.

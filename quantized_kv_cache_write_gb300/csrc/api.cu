@@ -108,6 +108,8 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
   }
   if (static_cast<int64_t>(topk) + num_splits > INT32_MAX) return QKV_ERR_ARG;
   if (rows * num_kv_heads * static_cast<int64_t>(num_splits) > INT32_MAX) return QKV_ERR_ARG;
+  // the kernels number records (slot * H + head) in 32 bits
+  if (num_slots * num_kv_heads > INT32_MAX) return QKV_ERR_UNSUPPORTED;
   if (rows == 0) return QKV_OK;
   if (!q || !k_cache || !v_cache || (topk > 0 && !topk_idx)) return QKV_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;

@@ -58,6 +58,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units): p <= 2^8
 constexpr int kPShift = 7;    // p * 2^7 <= 2^15 stays a finite fp16; p >= 2^-21 stays normal
+constexpr int kEuHeadroom = 3;  // int8: the V-scale bound 2^eu is raised 2^3 past the largest scale seen
 constexpr int kTmemCols = 128;  // per CTA: 4 warps x (their 32 lanes) x 128 fp32 columns
 
 // kRowBytes: bytes of one K (or V) row in shared memory (the inline layout keeps the 272 B
@@ -171,10 +172,15 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     tmem_relinquish_alloc_permit();
   }
 
-  // ---------------- this warp's tiles: split tiles warp, warp + 4, ...
+  // ---------------- this warp's tiles: split tiles warp, warp + 4, ... (an empty pool has
+  // no valid index: every row is empty)
   const int ntiles = (col1 - col0 + kKeys - 1) / kKeys;
-  const int my = ntiles > warp ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  const int my = (ntiles > warp && a.num_slots > 0) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   const int32_t* idx_row = a.topk_idx + r * a.topk;
+  if (a.num_slots == 0 && a.dev_status != nullptr) {  // no tiles run: still flag every non-padding entry
+    for (int col = col0 + tid; col < col1; col += kThreads)
+      if (__ldg(idx_row + col) != -1) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+  }
 
   auto load_idx = [&](int i) -> int {
     if (i >= my || lane >= kKeys) return -1;
@@ -188,6 +194,18 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     return v;
   };
 
+  // Fixed per-lane parts of the copies of 256 B / 512 B rows: at step t lane l copies chunk
+  // l % kRowChunks of key l / kRowChunks + kKeyStep t (consecutive lanes on consecutive chunks
+  // of a row: whole lines per request), so only the record base changes from step to step.
+  constexpr int kRowChunks = F::kRowBytes / 16;
+  constexpr int kKeyStep = F::kInline ? 1 : 32 / kRowChunks;
+  static_assert(F::kInline || 32 % kRowChunks == 0, "a row's chunks must tile a warp");
+  const int chunk_l = F::kInline ? 0 : lane % kRowChunks;
+  const uint8_t* kb_l = a.k_cache + 16 * chunk_l;
+  const uint8_t* vb_l = a.v_cache + 16 * chunk_l;
+  const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT>(lane / kRowChunks) + 16 * chunk_l;
+  const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(lane / kRowChunks) - L::kStageV + 16 * chunk_l;
+
   // Copy one 16-key tile into ring stage i % kStages.
   auto issue = [&](int i, int idxv) {
     const int st = i % F::kStages;
@@ -195,7 +213,23 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     if (lane == 0) sMask[st] = mask;
     uint8_t* sb = ring + size_t(st) * L::kStageBytes;
     const uint32_t sbase = smem_u32(sb);
-    {
+    // record number (slot * H + h; the host keeps it below 2^31) of key `lane`, -1 = padding
+    const int rec_l = idxv >= 0 ? idxv * H + h : -1;
+    if (!F::kInline) {
+#pragma unroll
+      for (int t = 0; t < kKeys / kKeyStep; ++t) {
+        int rec = __shfl_sync(0xffffffffu, rec_l, lane / kRowChunks + kKeyStep * t);
+        // int8 padding reads record 0 (finite codes; its p is 0): no zero-fill needed. E4M3 and
+        // bf16 zero-fill it, as a stale NaN code times p = 0 would still give NaN.
+        const int nb = (F::kInt8 || rec >= 0) ? 16 : 0;
+        rec = max(rec, 0);
+        const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(rec)) * F::kGlobalRow;
+        // offsets of key l / kRowChunks + kKeyStep t relative to key l / kRowChunks
+        const uint32_t tk = k_row_off<FMT>(kKeyStep * t), tv = v_row_off<FMT>(kKeyStep * t);
+        cp_async16(sbase + dk_l + tk, kb_l + off, nb);
+        cp_async16(sbase + dv_l + tv, vb_l + off, nb);
+      }
+    } else {
       // 16 B copies: consecutive lanes take consecutive chunks of a row (whole lines)
       constexpr int kChunks = F::kInline ? 17 : F::kRowBytes / 16;
       constexpr int kTotalCopies = kKeys * kChunks;
@@ -222,21 +256,15 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
             cp_async16(dK, a.k_cache + al + jj * 16, nb);
             cp_async16(dV, a.v_cache + al + jj * 16, nb);
             if (jj == 0) sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
-          } else {
-            const int nb = valid ? 16 : 0;
-            cp_async16(dK, a.k_cache + rec * F::kGlobalRow + jj * 16, nb);
-            cp_async16(dV, a.v_cache + rec * F::kGlobalRow + jj * 16, nb);
           }
         }
       }
     }
     if (F::kSide) {
       // lanes 0-15: K scales of the 16 keys; lanes 16-31: V scales (zero for padding)
-      int slot = __shfl_sync(0xffffffffu, idxv, lane & 15);
-      const bool valid = slot >= 0;
-      slot = valid ? slot : 0;
+      const int rec = __shfl_sync(0xffffffffu, rec_l, lane & 15);
       const float* gs = (lane >> 4) ? a.v_scale_tok : a.k_scale_tok;
-      cp_async4(sbase + L::kStageKs + lane * 4, gs + static_cast<int64_t>(slot) * H + h, valid ? 4 : 0);
+      cp_async4(sbase + L::kStageKs + lane * 4, gs + max(rec, 0), rec >= 0 ? 4 : 0);
     }
   };
 
@@ -283,24 +311,25 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       sg = m ? max(-64, min(64, 14 - (static_cast<int>(m >> 23) - 127))) : 0;
     }
     const float u = pow2f(sg);
+    // two head dims per 32-bit store: the pair that shares a B-fragment register of a code
+    // word (int8: d, d + 2; E4M3 and bf16: d, d + 1) sits in adjacent k-indices
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const int d = 32 * part + i;
-      const int blk = d >> 6, cc = (d >> 4) & 3, ks = (d >> 2) & 3, rr = d & 3;
-      // int8 B fragments pair head dims (+0, +2) / (+1, +3); E4M3 and bf16 pair (+0, +1) / (+2, +3)
-      const int upper = F::kInt8 ? (rr & 1) : (rr >> 1);
-      const int e = F::kInt8 ? (rr >> 1) : (rr & 1);
-      const int kappa = upper * 8 + 2 * cc + e;
-      const uint32_t word = w[i >> 1];
-      const uint32_t bits16 = (i & 1) ? (word >> 16) : (word & 0xFFFFu);
-      uint16_t v16;
-      if (F::kBf16) {
-        v16 = static_cast<uint16_t>(bits16);
-      } else {
-        const __half hv = __float2half_rn(__uint_as_float(bits16 << 16) * u);
-        v16 = *reinterpret_cast<const uint16_t*>(&hv);
+    for (int g4 = 0; g4 < 8; ++g4) {
+#pragma unroll
+      for (int up = 0; up < 2; ++up) {
+        const int i0 = 4 * g4 + (F::kInt8 ? up : 2 * up), i1 = i0 + (F::kInt8 ? 2 : 1);
+        const int d = 32 * part + i0;
+        const int blk = d >> 6, cc = (d >> 4) & 3, ks = (d >> 2) & 3;
+        const uint32_t b0 = (i0 & 1) ? (w[i0 >> 1] >> 16) : (w[i0 >> 1] & 0xFFFFu);
+        const uint32_t b1 = (i1 & 1) ? (w[i1 >> 1] >> 16) : (w[i1 >> 1] & 0xFFFFu);
+        uint32_t v32;
+        if (F::kBf16) {
+          v32 = b0 | (b1 << 16);
+        } else {
+          v32 = pack_half2(__uint_as_float(b0 << 16) * u, __uint_as_float(b1 << 16) * u);
+        }
+        sts32(smem_u32(smem + L::kQ + q_off(blk * 4 + ks, qh, up * 8 + 2 * cc)), v32);
       }
-      *reinterpret_cast<uint16_t*>(smem + L::kQ + q_off(blk * 4 + ks, qh, kappa)) = v16;
     }
     if (part == 0) {
       float base = a.softmax_scale * kLog2e;
@@ -434,12 +463,20 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     {
       const float nm0 = (mx0 > mu0 + kTau) ? mx0 : mu0;
       const float nm1 = (mx1 > mu1 + kTau) ? mx1 : mu1;
+      // int8: when a V scale reaches 2^eu, raise eu to kEuHeadroom past it, so that later,
+      // slightly larger scales do not force another rescale (terms p v 2^(7 - eu) stay below
+      // 2^15; the headroom only moves the smallest ones 2^3 closer to the subnormal range)
       int ne = eu;
-      if (F::kInt8 && vmx > 0.f) ne = max(eu, static_cast<int>(__float_as_uint(vmx) >> 23) - 126);
+      if (F::kInt8 && vmx > 0.f) {
+        const int ev = static_cast<int>(__float_as_uint(vmx) >> 23) - 126;  // 2^ev > vmx
+        if (ev > eu) ne = ev + kEuHeadroom;
+      }
       const float ov = F::kInt8 ? pow2f(max(eu - ne, -126)) : 1.f;
       const float al0 = (nm0 == mu0) ? 1.f : fast_exp2(mu0 - nm0);  // mu0 = -inf gives 0
       const float al1 = (nm1 == mu1) ? 1.f : fast_exp2(mu1 - nm1);
-      rescale = __any_sync(0xffffffffu, nm0 != mu0 || nm1 != mu1 || ne != eu);
+      // an accumulator row whose head has seen no valid key yet is still zero: it needs no rescale
+      const bool live0 = mu0 != -INFINITY, live1 = mu1 != -INFINITY;
+      rescale = __any_sync(0xffffffffu, (live0 && (nm0 != mu0 || ne != eu)) || (live1 && (nm1 != mu1 || ne != eu)));
       if (rescale) {
         rf0 = al0 * ov;
         rf1 = al1 * ov;

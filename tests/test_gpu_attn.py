@@ -105,6 +105,23 @@ def test_bad_indices_are_flagged_and_treated_as_padding():
     assert_close(lse, rl, "lse")
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_empty_pool_gives_empty_rows_and_flags_indices(fmt):
+    # the buffers hold slots, but the call says the pool is empty: every index is out of range
+    import dataclasses
+    wl = small_random(51, num_slots=64, rows=3, topk=40, pad_frac=0.3)
+    gp = GpuPool(wl, fmt)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse, _, _ = gp.attend(dataclasses.replace(wl, num_slots=0), dev_status=status)
+    assert np.all(out == 0) and np.all(lse == -np.inf)
+    assert status.item() == 2
+    # all-padding rows with an empty pool raise nothing
+    status.zero_()
+    wl_pad = dataclasses.replace(wl, num_slots=0, topk=np.full_like(wl.topk, -1))
+    out, lse, _, _ = gp.attend(wl_pad, dev_status=status)
+    assert np.all(out == 0) and np.all(lse == -np.inf) and status.item() == 0
+
+
 def test_duplicate_indices_count_twice():
     wl = small_random(50, num_slots=500, rows=2, topk=30)
     wl.topk[:, 10:20] = wl.topk[:, 0:10]
