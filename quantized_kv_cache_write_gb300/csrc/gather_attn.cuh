@@ -69,22 +69,22 @@ struct Fmt;
 template <>
 struct Fmt<QKV_INT8_SIDE> {
   static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
-  static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false;
+  static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false, kNatural = true;
 };
 template <>
 struct Fmt<QKV_INT8_INLINE> {
   static constexpr int kRowBytes = 272, kGlobalRow = kInlineRecord, kStages = 2, kMinBlocks = 2, kKShift = 16;
-  static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false;
+  static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false, kNatural = false;
 };
 template <>
 struct Fmt<QKV_E4M3> {
   static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
-  static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false;
+  static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false, kNatural = true;
 };
 template <>
 struct Fmt<QKV_BF16> {
   static constexpr int kRowBytes = 512, kGlobalRow = 512, kStages = 2, kMinBlocks = 1, kKShift = 16;
-  static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true;
+  static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true, kNatural = false;
 };
 
 // V region i (rows i and i + 8) starts 16 B further along the bank cycle than a plain packing
@@ -94,7 +94,10 @@ __host__ __device__ constexpr int v_region_shift(int i) {
   return Fmt<FMT>::kBf16 ? 16 * ((((i >> 1) & 1)) | (((i >> 2) & 1) << 2)) : 16 * i;
 }
 
-constexpr int kORow = 164;  // floats per head row of the merge buffer, one 128-dim half (bank-conflict-free)
+// floats per head row of the merge buffer (one 128-dim half), chosen bank-conflict free for the
+// layout's fragment-to-head-dim order
+template <int FMT>
+__host__ __device__ constexpr int merge_row() { return Fmt<FMT>::kNatural ? 136 : 164; }
 
 template <int FMT>
 struct Smem {
@@ -118,19 +121,42 @@ struct Smem {
   static constexpr size_t kM = kMask + kWarps * F::kStages * 4;      // [kWarps][16] floats
   static constexpr size_t kL = kM + kWarps * 16 * 4;                 // [kWarps][16] floats
   static constexpr size_t kTotal = kL + kWarps * 16 * 4;
-  // final merge buffer [kWarps][16][kORow] floats, reusing the rings
-  static_assert(size_t(kWarps) * 16 * kORow * 4 <= kWarps * kWarpRing, "merge buffer must fit in the rings");
+  // final merge buffer [kWarps][16][merge_row] floats, reusing the rings
+  static_assert(size_t(kWarps) * 16 * merge_row<FMT>() * 4 <= kWarps * kWarpRing, "merge buffer must fit in the rings");
   static_assert(kRing % 16 == 0 && kKArea % 16 == 0 && kVArea % 16 == 0, "alignment");
   // the CTAs that fit an SM (228 KB of shared memory, 1 KB reserved each) never ask for more
   // than its 512 TMEM columns, so an allocation never has to wait for another CTA
   static_assert((233472 / (kTotal + 1024)) * kTmemCols <= 512, "TMEM budget");
 };
 
+// Key row (0..15 within a tile) feeding column n of N-tile nt of q.K^T -- and so the key whose
+// p a thread holds. The p.V B fragments of the natural layouts come from transposed byte
+// matrices: a register holds keys 4c .. 4c + 3 of one head dim, which pair up as (4c, 4c + 2)
+// and (4c + 1, 4c + 3) for int8 (exponent splice of bytes 0, 2 / 1, 3) and as (4c, 4c + 1),
+// (4c + 2, 4c + 3) for E4M3 (the cvt takes two adjacent bytes). q.K^T produces p in that
+// order. The inline layout uses the int8 order too, so it sums exactly like the side layout.
+template <int FMT>
+__device__ __forceinline__ int key_of(int nt, int n) {
+  if (Fmt<FMT>::kInt8) return 2 * n + nt;
+  if (Fmt<FMT>::kE4m3) return 4 * (n >> 1) + (n & 1) + 2 * nt;
+  return 8 * nt + n;
+}
+
 // Byte offsets of tile row r (0..15) inside a stage (K area, V area).
+// K: two regions of 8 rows, the second 8 rows + kKShift further on; a row goes to the second
+// region when bit b of r is set -- b = 1 for int8 and b = 0 otherwise, so that the two rows a
+// quarter-warp reads together (keys 4k + nt and 4k + 2 + nt for int8, 4k + 2nt and
+// 4k + 1 + 2nt for E4M3) fall on disjoint banks.
+// V: row r in region r mod 8, each region 2 rows plus 16 (r mod 8) B of rotation (bf16: see
+// v_region_shift): 8 consecutive rows start on 8 distinct 16 B banks, as the transposed
+// matrix loads and the 16 B fragment reads want.
 template <int FMT>
 __device__ __forceinline__ uint32_t k_row_off(int r) {
   constexpr int RB = Fmt<FMT>::kRowBytes;
-  return RB * (r >> 1) + (r & 1) * (8 * RB + Fmt<FMT>::kKShift);
+  const int b = Fmt<FMT>::kInt8 ? 1 : 0;
+  const int region = (r >> b) & 1;
+  const int idx = ((r >> (b + 1)) << b) | (r & ((1 << b) - 1));  // r without bit b
+  return RB * idx + region * (8 * RB + Fmt<FMT>::kKShift);
 }
 template <int FMT>
 __device__ __forceinline__ uint32_t v_row_off(int r) {
@@ -378,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      rowK[nt] = sbase + k_row_off<FMT>(nt * 8 + hn);
-      if (F::kInline) delta_k[nt] = lds_u8(sbase + L::kStageMeta + nt * 8 + hn);
+      const int key = key_of<FMT>(nt, hn);
+      rowK[nt] = sbase + k_row_off<FMT>(key);
+      if (F::kInline) delta_k[nt] = lds_u8(sbase + L::kStageMeta + key);
     }
 #pragma unroll
     for (int blk = 0; blk < 4; ++blk) {
@@ -429,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int kt = nt * 8 + 2 * c + e;
+        const int kt = key_of<FMT>(nt, 2 * c + e);
         const bool valid = (mask >> kt) & 1u;
         float ksc = 1.f, vs = 0.f;
         if (F::kSide) {
@@ -521,10 +548,14 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       }
     }
 
-    // ---- p . V: sweep sw covers head dims [128 sw, 128 sw + 128); lane group n reads the
-    //      16 head dims 128 sw + 16 n .. + 16 of the rows 2c, 2c + 1, 2c + 8, 2c + 9
+    // ---- p . V: sweep sw covers head dims [128 sw, 128 sw + 128).
+    //      Natural layouts: N-tile t holds head dims 8 t .. 8 t + 7; its B fragments come from
+    //      transposed 16 x 16 byte matrices (keys x 16 head dims) of the V rows.
+    //      Others: lane group n reads the 16 head dims 128 sw + 16 n .. + 16 of the four key
+    //      rows whose p it holds; N-tile 16 s + t, column n covers head dim 128 s + 16 n + t.
     {
-      const int rows[4] = {2 * c, 2 * c + 1, 2 * c + 8, 2 * c + 9};
+      const int rows[4] = {key_of<FMT>(0, 2 * c), key_of<FMT>(0, 2 * c + 1), key_of<FMT>(1, 2 * c),
+                           key_of<FMT>(1, 2 * c + 1)};
       uint32_t rowV[4];
       int dv[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -532,15 +563,36 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         rowV[ri] = sbase + v_row_off<FMT>(rows[ri]);
         if (F::kInline) dv[ri] = lds_u8(sbase + L::kStageMeta + rows[ri]);
       }
+      // natural layouts: lane l addresses key row l % 16 of the 16 B column block l / 16 (+ 2 m)
+      const uint32_t vmat = sbase + v_row_off<FMT>(lane & 15) + 16 * (lane >> 4);
 #pragma unroll
       for (int sw = 0; sw < 2; ++sw) {
         // accumulator quarters 2 sw (N-tiles 16 sw + 0..7) and 2 sw + 1 (16 sw + 8..15)
         float ob[2][32];
-        tmem_wait_st();  // the previous stores of these registers' columns are done
+        // the previous sweep's stores have read these registers (and the previous tile's
+        // stores of these columns are done)
+        tmem_wait_st();
         tmem_ld32(tacc + 64 * sw, ob[0]);
         tmem_ld32(tacc + 64 * sw + 32, ob[1]);
         uint32_t bb[16][2];
-        if (F::kBf16) {
+        if (F::kNatural) {
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            // 16 B column blocks 8 sw + 2 m and 8 sw + 2 m + 1: N-tiles 4 m .. 4 m + 3 of the sweep
+            uint32_t x[4];
+            ldmatrix_x2_trans_b8(vmat + 16 * (8 * sw + 2 * m), x[0], x[1], x[2], x[3]);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (F::kInt8) {
+                bb[4 * m + u][0] = i8pair_to_f16x2(x[u]);       // keys 4c, 4c + 2
+                bb[4 * m + u][1] = i8pair_to_f16x2(x[u] >> 8);  // keys 4c + 1, 4c + 3
+              } else {
+                bb[4 * m + u][0] = e4m3pair_to_f16x2(x[u]);        // keys 4c, 4c + 1
+                bb[4 * m + u][1] = e4m3pair_to_f16x2(x[u] >> 16);  // keys 4c + 2, 4c + 3
+              }
+            }
+          }
+        } else if (F::kBf16) {
           uint32_t vw[4][8];
 #pragma unroll
           for (int ri = 0; ri < 4; ++ri) {
@@ -632,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   }
   tmem_wait_st();
   __syncthreads();  // every warp is done with its ring: reuse the rings as the merge buffer
+  constexpr int kORow = merge_row<FMT>();
   float* sO = reinterpret_cast<float*>(smem + L::kRing);  // [kWarps][16][kORow]
   float* sM = reinterpret_cast<float*>(smem + L::kM);
   float* sL = reinterpret_cast<float*>(smem + L::kL);
@@ -652,12 +705,23 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       tmem_ld32(tacc + 64 * sw + 32, ob[1]);
       tmem_wait_ld(ob[0]);
       tmem_wait_ld(ob[1]);
+      if (F::kNatural) {
+        // N-tile tt of the half holds local head dims 8 tt + 2c, 8 tt + 2c + 1 (heads h0, h1)
+        float* o0 = sO + (warp * 16 + h0) * kORow + 2 * c;
+        float* o1 = sO + (warp * 16 + h1) * kORow + 2 * c;
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt) {
+          const float* q = &ob[tt >> 3][4 * (tt & 7)];
+          *reinterpret_cast<float2*>(o0 + 8 * tt) = make_float2(q[0] * post, q[1] * post);
+          *reinterpret_cast<float2*>(o1 + 8 * tt) = make_float2(q[2] * post, q[3] * post);
+        }
+      }
       // local head dim 32 c + x sits at 40 c + x of a head row: x < 8 and 16 <= x < 24 come
       // from quarter 0 (columns 2c and 2c + 1 of N-tile x mod 8), the others from quarter 1
       float* o0 = sO + (warp * 16 + h0) * kORow + 40 * c;
       float* o1 = sO + (warp * 16 + h1) * kORow + 40 * c;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < (F::kNatural ? 0 : 8); ++k) {
         const int b = (k >> 1) & 1;            // quarter of x = 4k .. 4k + 3
         const int j = (k >> 2);                // column 2c (0) or 2c + 1 (1)
         const int t = 4 * (k & 1);             // first N-tile within the quarter
@@ -670,7 +734,10 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     }
     __syncthreads();
     {
-      const int hh = tid >> 3, part = tid & 7;  // head, local head dims [16 part, 16 part + 16)
+      // head hh; part covers the local head dims d(k) .. d(k) + 3, k = 0..3 (natural layouts:
+      // d(k) = 4 part + 32 k, so that 8 consecutive threads read all 32 banks; others:
+      // d(k) = 16 part + 4 k, stored at 40 (part / 2) + 16 (part % 2) + 4 k)
+      const int hh = tid >> 3, part = tid & 7;
       if (hh < G) {
         float mw[kWarps], M = -INFINITY;
 #pragma unroll
@@ -691,11 +758,10 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         for (int i2 = 0; i2 < 16; ++i2) res[i2] = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
-          const float4* src =
-              reinterpret_cast<const float4*>(sO + (w * 16 + hh) * kORow + 40 * (part >> 1) + 16 * (part & 1));
+          const float* src = sO + (w * 16 + hh) * kORow + (F::kNatural ? 4 * part : 40 * (part >> 1) + 16 * (part & 1));
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const float4 x = src[k];
+            const float4 x = *reinterpret_cast<const float4*>(src + (F::kNatural ? 32 * k : 4 * k));
             res[4 * k] += ww[w] * x.x;
             res[4 * k + 1] += ww[w] * x.y;
             res[4 * k + 2] += ww[w] * x.z;
@@ -705,10 +771,10 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         const int64_t qhead = static_cast<int64_t>(h) * G + hh;
         float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
                               : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
-        dst += 128 * sw + 16 * part;
+        dst += 128 * sw + (F::kNatural ? 4 * part : 16 * part);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          reinterpret_cast<float4*>(dst)[k] =
+          *reinterpret_cast<float4*>(dst + (F::kNatural ? 32 * k : 4 * k)) =
               make_float4(res[4 * k] * f, res[4 * k + 1] * f, res[4 * k + 2] * f, res[4 * k + 3] * f);
         if (sw == 0 && part == 0) {
           const float lse = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;

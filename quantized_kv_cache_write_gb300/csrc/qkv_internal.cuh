@@ -116,6 +116,17 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
                : "r"(addr));
 }
 
+// Two 16 x 16 byte matrices, transposed: lanes 0-15 give the row addresses (16 B each) of
+// matrix 0, lanes 16-31 those of matrix 1. Lane (g, c) = (lane / 4, lane % 4) receives in r0
+// the bytes of rows 4c .. 4c + 3 (row 4c in the low byte) at column g of matrix 0, in r1 the
+// same rows at column g + 8; r2, r3 likewise for matrix 1.
+__device__ __forceinline__ void ldmatrix_x2_trans_b8(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                     uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // D = A(16x16, row) * B(16x8, col) + D, fp32 accumulate. Register-only, so not volatile:
 // the compiler may interleave independent MMAs.
 __device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
