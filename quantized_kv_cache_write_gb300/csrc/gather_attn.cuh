@@ -208,11 +208,15 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       if (__ldg(idx_row + col) != -1) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
   }
 
+  // Start the load of tile i's index of key `lane` (-1 past the split's end). The value is
+  // only checked where it is used, one tile later, so the load's latency stays hidden.
   auto load_idx = [&](int i) -> int {
     if (i >= my || lane >= kKeys) return -1;
     const int col = col0 + (warp + kWarps * i) * kKeys + lane;
-    if (col >= col1) return -1;
-    int v = __ldg(idx_row + col);
+    return col < col1 ? __ldg(idx_row + col) : -1;
+  };
+  // Entries outside [-1, num_slots) are flagged and become padding.
+  auto checked = [&](int v) -> int {
     if (v < -1 || static_cast<int64_t>(v) >= a.num_slots) {
       if (a.dev_status != nullptr) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
       v = -1;
@@ -233,7 +237,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(lane / kRowChunks) - L::kStageV + 16 * chunk_l;
 
   // Copy one 16-key tile into ring stage i % kStages.
-  auto issue = [&](int i, int idxv) {
+  auto issue = [&](int i, int raw_idx) {
+    const int idxv = checked(raw_idx);
     const int st = i % F::kStages;
     const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
     if (lane == 0) sMask[st] = mask;
