@@ -56,6 +56,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kKeys = 16;  // keys per warp tile
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kMaxFinite = 3.4028234663852886e38f;  // largest finite fp32
 constexpr float kTau = 8.0f;  // lazy-rescale threshold (log2 units): p <= 2^8
 constexpr int kPShift = 7;    // p * 2^7 <= 2^15 stays a finite fp16; p >= 2^-21 stays normal
 constexpr int kEuHeadroom = 3;  // int8: the V-scale bound 2^eu is raised 2^3 past the largest scale seen
@@ -224,17 +225,19 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     return v;
   };
 
-  // Fixed per-lane parts of the copies of 256 B / 512 B rows: at step t lane l copies chunk
-  // l % kRowChunks of key l / kRowChunks + kKeyStep t (consecutive lanes on consecutive chunks
-  // of a row: whole lines per request), so only the record base changes from step to step.
+  // Fixed per-lane parts of the copies of 256 B / 512 B rows. One copy instruction covers
+  // four keys, one 128 B line of each (8 consecutive lanes on 8 consecutive 16 B chunks):
+  // lane l takes key l / 8 + 4 t (t = 0..3) and chunks l % 8 + 8 u of it, so only the record
+  // base changes per key and every chunk of a key is an immediate offset from it. (More
+  // keys per instruction split a request over more lines and were measured slower.)
   constexpr int kRowChunks = F::kRowBytes / 16;
-  constexpr int kKeyStep = F::kInline ? 1 : 32 / kRowChunks;
-  static_assert(F::kInline || 32 % kRowChunks == 0, "a row's chunks must tile a warp");
-  const int chunk_l = F::kInline ? 0 : lane % kRowChunks;
-  const uint8_t* kb_l = a.k_cache + 16 * chunk_l;
-  const uint8_t* vb_l = a.v_cache + 16 * chunk_l;
-  const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT>(lane / kRowChunks) + 16 * chunk_l;
-  const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(lane / kRowChunks) - L::kStageV + 16 * chunk_l;
+  constexpr int kKpi = 4;                              // keys per copy instruction
+  constexpr int kHs = F::kInline ? 1 : kRowChunks / 8;  // lines per key
+  const int key_sub = lane >> 3, chunk_sub = lane & 7;
+  const uint8_t* kb_l = a.k_cache + 16 * chunk_sub;
+  const uint8_t* vb_l = a.v_cache + 16 * chunk_sub;
+  const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT>(key_sub) + 16 * chunk_sub;
+  const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(key_sub) - L::kStageV + 16 * chunk_sub;
 
   // Copy one 16-key tile into ring stage i % kStages.
   auto issue = [&](int i, int raw_idx) {
@@ -248,17 +251,20 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     const int rec_l = idxv >= 0 ? idxv * H + h : -1;
     if (!F::kInline) {
 #pragma unroll
-      for (int t = 0; t < kKeys / kKeyStep; ++t) {
-        int rec = __shfl_sync(0xffffffffu, rec_l, lane / kRowChunks + kKeyStep * t);
+      for (int t = 0; t < kKeys / kKpi; ++t) {
+        int rec = __shfl_sync(0xffffffffu, rec_l, key_sub + kKpi * t);
         // int8 padding reads record 0 (finite codes; its p is 0): no zero-fill needed. E4M3 and
         // bf16 zero-fill it, as a stale NaN code times p = 0 would still give NaN.
         const int nb = (F::kInt8 || rec >= 0) ? 16 : 0;
         rec = max(rec, 0);
         const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(rec)) * F::kGlobalRow;
-        // offsets of key l / kRowChunks + kKeyStep t relative to key l / kRowChunks
-        const uint32_t tk = k_row_off<FMT>(kKeyStep * t), tv = v_row_off<FMT>(kKeyStep * t);
-        cp_async16(sbase + dk_l + tk, kb_l + off, nb);
-        cp_async16(sbase + dv_l + tv, vb_l + off, nb);
+        // offsets of key l / 8 + 4 t relative to key l / 8 (the row layouts are additive)
+        const uint32_t tk = k_row_off<FMT>(kKpi * t), tv = v_row_off<FMT>(kKpi * t);
+#pragma unroll
+        for (int u = 0; u < kHs; ++u) {
+          cp_async16(sbase + dk_l + tk + 128 * u, kb_l + off + 128 * u, nb);
+          cp_async16(sbase + dv_l + tv + 128 * u, vb_l + off + 128 * u, nb);
+        }
       }
     } else {
       // 16 B copies: consecutive lanes take consecutive chunks of a row (whole lines)
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
           ksc = __uint_as_float(lds32(sbase + k_row_off<FMT>(kt) + dl + kHeadDim));
           vs = __uint_as_float(lds32(sbase + v_row_off<FMT>(kt) + dl + kHeadDim));
         }
-        vs = valid ? vs : 0.f;
+        // (padding keys already carry a zero V scale: their scale copies zero-fill)
         vsc[nt][e] = vs;
         vmx = fmaxf(vmx, vs);
         const float x0 = acc[nt][0][e] + acc[nt][1][e];
@@ -524,15 +530,16 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     uint32_t pa[4], pl[4];
     {
       const float pm = F::kInt8 ? pow2f(kPShift - eu) : (F::kE4m3 ? pow2f(kPShift) : 1.f);
+      // a head whose max is still -inf has only masked (-inf) logits: subtracting the most
+      // negative finite float instead gives exp2(-inf) = 0 rather than exp2(NaN)
+      const float m0 = fmaxf(mu0, -kMaxFinite), m1 = fmaxf(mu1, -kMaxFinite);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         float p[4];
-        p[0] = fast_exp2(s[nt][0] - mu0);  // masked: exp2(-inf) = 0; mu = -inf only with no valid key
-        p[1] = fast_exp2(s[nt][1] - mu0);
-        p[2] = fast_exp2(s[nt][2] - mu1);
-        p[3] = fast_exp2(s[nt][3] - mu1);
-        if (mu0 == -INFINITY) p[0] = p[1] = 0.f;
-        if (mu1 == -INFINITY) p[2] = p[3] = 0.f;
+        p[0] = fast_exp2(s[nt][0] - m0);  // masked: exp2(-inf) = 0
+        p[1] = fast_exp2(s[nt][1] - m0);
+        p[2] = fast_exp2(s[nt][2] - m1);
+        p[3] = fast_exp2(s[nt][3] - m1);
         l0 += p[0] + p[1];
         l1 += p[2] + p[3];
         const float f0 = F::kInt8 ? vsc[nt][0] * pm : pm, f1 = F::kInt8 ? vsc[nt][1] * pm : pm;
