@@ -110,11 +110,28 @@ def qkv_e4m3_calibrate(x, amax_bits, scale_out, *, stream=None):
     _check("qkv_e4m3_calibrate", st)
 
 
+def _expect_shape(name: str, t, shape):
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part=None, lse_part=None):
+    """The kernels index every buffer by q's row count: the others must agree with it."""
+    R, Hq, D = q.shape
+    if topk_idx is not None and (topk_idx.dim() != 2 or topk_idx.shape[0] != R):
+        raise ValueError(f"topk_idx must be [{R}, k], got {tuple(topk_idx.shape)}")
+    _expect_shape("out", out, (R, Hq, D))
+    _expect_shape("lse", lse, (R, Hq))
+    _expect_shape("o_part", o_part, (R, num_splits, Hq, D))
+    _expect_shape("lse_part", lse_part, (R, num_splits, Hq))
+
+
 def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: float, *, num_kv_heads: int = 1,
                     num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
                     k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, num_splits: int = 1, out=None,
                     lse=None, o_part=None, lse_part=None, dev_status=None, stream=None):
     """Top-k gather decode attention. q bf16 [R, Hq, D]; topk_idx int32 [R, k]."""
+    _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
     R, Hq, D = q.shape
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_idx.shape[1] if topk_idx is not None else 0
@@ -128,6 +145,9 @@ def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: floa
 def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1.0, stream=None):
     """Merge split-K partials o_part [R, P, Hq, D], lse_part [R, P, Hq] into out [R, Hq, D]."""
     R, P, Hq, D = o_part.shape
+    _expect_shape("lse_part", lse_part, (R, P, Hq))
+    _expect_shape("out", out, (R, Hq, D))
+    _expect_shape("lse", lse, (R, Hq))
     st = lib.qsa_splitk_merge(_ptr(o_part), _ptr(lse_part), R, Hq, D, P, float(v_scale_post), _ptr(out), _ptr(lse),
                               _stream(stream))
     _check("qsa_splitk_merge", st)
@@ -152,6 +172,7 @@ def qsa_gather_attn_splitk_noalloc(q, fmt: int, k_cache, v_cache, topk_idx, soft
     For callers that may not allocate device memory: only inputs and outputs are passed.
     Calls share one scratch array per GPU, so calls that overlap on the GPU race.
     """
+    _check_gather_shapes(q, topk_idx, num_splits, out, lse)
     R, Hq, D = q.shape
     if num_splits > 1 and noalloc_scratch_bytes(R, num_splits, Hq, D) > NOALLOC_SCRATCH_BYTES:
         raise ValueError(f"{R} rows x {num_splits} splits x {Hq} heads needs "

@@ -114,3 +114,28 @@ def test_merge_and_calibrate_host_validation(lib):
     assert L.qsa_splitk_merge(FAKE, FAKE, 0, 16, 256, 4, 1.0, FAKE, None, None) == E.QKV_OK
     assert L.qkv_e4m3_calibrate(FAKE, -1, FAKE, FAKE, None) == E.QKV_ERR_ARG
     assert L.qkv_e4m3_calibrate(FAKE + 2, 10, FAKE, FAKE, None) == E.QKV_ERR_ALIGN
+
+
+def test_binding_rejects_buffers_that_disagree_with_q(lib):
+    """The kernels index every buffer by q's row count; the binding refuses a mismatch
+    before any call, so a short topk_idx or out can never be read or written past its end."""
+    import torch
+    q = torch.zeros((4, 16, 256), dtype=torch.bfloat16)
+    kc = torch.zeros((8, 1, 256), dtype=torch.int8)
+    idx_ok = torch.zeros((4, 5), dtype=torch.int32)
+    out_ok = torch.zeros((4, 16, 256), dtype=torch.float32)
+    cases = [
+        dict(topk_idx=torch.zeros((3, 5), dtype=torch.int32), out=out_ok),
+        dict(topk_idx=idx_ok, out=torch.zeros((3, 16, 256), dtype=torch.float32)),
+        dict(topk_idx=idx_ok, out=out_ok, lse=torch.zeros((4, 8), dtype=torch.float32)),
+        dict(topk_idx=idx_ok, out=None, num_splits=2, o_part=torch.zeros((4, 3, 16, 256)),
+             lse_part=torch.zeros((4, 2, 16))),
+    ]
+    for kw in cases:
+        with pytest.raises(ValueError):
+            lib.qsa_gather_attn(q, lib.QKV_INT8_SIDE, kc, kc, kw.pop("topk_idx"), 0.0625, **kw)
+    with pytest.raises(ValueError):
+        lib.qsa_splitk_merge(torch.zeros((4, 2, 16, 256)), torch.zeros((4, 3, 16)), out_ok)
+    with pytest.raises(ValueError):
+        lib.qsa_gather_attn_splitk_noalloc(q, lib.QKV_INT8_SIDE, kc, kc, idx_ok, 0.0625, num_splits=2,
+                                           out=torch.zeros((2, 16, 256)))
