@@ -121,7 +121,8 @@ struct Smem {
   static constexpr size_t kMask = kTmem + 16;                     // [kWarps][kStages] uint32
   static constexpr size_t kM = kMask + kWarps * F::kStages * 4;      // [kWarps][16] floats
   static constexpr size_t kL = kM + kWarps * 16 * 4;                 // [kWarps][16] floats
-  static constexpr size_t kTotal = kL + kWarps * 16 * 4;
+  static constexpr size_t kPost = kL + kWarps * 16 * 4;             // [kWarps] floats
+  static constexpr size_t kTotal = kPost + kWarps * 4;
   // final merge buffer [kWarps][16][merge_row] floats, reusing the rings
   static_assert(size_t(kWarps) * 16 * merge_row<FMT>() * 4 <= kWarps * kWarpRing, "merge buffer must fit in the rings");
   static_assert(kRing % 16 == 0 && kKArea % 16 == 0 && kVArea % 16 == 0, "alignment");
@@ -702,15 +703,16 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   float* sO = reinterpret_cast<float*>(smem + L::kRing);  // [kWarps][16][kORow]
   float* sM = reinterpret_cast<float*>(smem + L::kM);
   float* sL = reinterpret_cast<float*>(smem + L::kL);
+  float* sPost = reinterpret_cast<float*>(smem + L::kPost);
   if (c == 0) {
     sM[warp * 16 + h0] = mu0;
     sM[warp * 16 + h1] = mu1;
     sL[warp * 16 + h0] = l0;
     sL[warp * 16 + h1] = l1;
   }
-  float post = 1.f;
-  if (F::kInt8) post = pow2f(eu - kPShift);
-  if (F::kE4m3) post = pow2f(-kPShift);
+  // the accumulators carry p times 2^(kPShift - eu) (int8) or 2^kPShift (E4M3); that power of
+  // two is undone in the combine weights rather than on every accumulator value
+  if (lane == 0) sPost[warp] = F::kInt8 ? pow2f(eu - kPShift) : (F::kE4m3 ? pow2f(-kPShift) : 1.f);
 #pragma unroll 1
   for (int sw = 0; sw < 2; ++sw) {
     {
@@ -726,8 +728,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 #pragma unroll
         for (int tt = 0; tt < 16; ++tt) {
           const float* q = &ob[tt >> 3][4 * (tt & 7)];
-          *reinterpret_cast<float2*>(o0 + 8 * tt) = make_float2(q[0] * post, q[1] * post);
-          *reinterpret_cast<float2*>(o1 + 8 * tt) = make_float2(q[2] * post, q[3] * post);
+          *reinterpret_cast<float2*>(o0 + 8 * tt) = make_float2(q[0], q[1]);
+          *reinterpret_cast<float2*>(o1 + 8 * tt) = make_float2(q[2], q[3]);
         }
       }
       // local head dim 32 c + x sits at 40 c + x of a head row: x < 8 and 16 <= x < 24 come
@@ -740,10 +742,10 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         const int j = (k >> 2);                // column 2c (0) or 2c + 1 (1)
         const int t = 4 * (k & 1);             // first N-tile within the quarter
         const float* q = ob[b];
-        reinterpret_cast<float4*>(o0)[k] = make_float4(q[4 * t + j] * post, q[4 * (t + 1) + j] * post,
-                                                       q[4 * (t + 2) + j] * post, q[4 * (t + 3) + j] * post);
-        reinterpret_cast<float4*>(o1)[k] = make_float4(q[4 * t + 2 + j] * post, q[4 * (t + 1) + 2 + j] * post,
-                                                       q[4 * (t + 2) + 2 + j] * post, q[4 * (t + 3) + 2 + j] * post);
+        reinterpret_cast<float4*>(o0)[k] = make_float4(q[4 * t + j], q[4 * (t + 1) + j], q[4 * (t + 2) + j],
+                                                       q[4 * (t + 3) + j]);
+        reinterpret_cast<float4*>(o1)[k] = make_float4(q[4 * t + 2 + j], q[4 * (t + 1) + 2 + j],
+                                                       q[4 * (t + 2) + 2 + j], q[4 * (t + 3) + 2 + j]);
       }
     }
     __syncthreads();
@@ -773,13 +775,14 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float* src = sO + (w * 16 + hh) * kORow + (F::kNatural ? 4 * part : 40 * (part >> 1) + 16 * (part & 1));
+          const float wo = ww[w] * sPost[w];  // exact: the post factor is a power of two
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float4 x = *reinterpret_cast<const float4*>(src + (F::kNatural ? 32 * k : 4 * k));
-            res[4 * k] += ww[w] * x.x;
-            res[4 * k + 1] += ww[w] * x.y;
-            res[4 * k + 2] += ww[w] * x.z;
-            res[4 * k + 3] += ww[w] * x.w;
+            res[4 * k] += wo * x.x;
+            res[4 * k + 1] += wo * x.y;
+            res[4 * k + 2] += wo * x.z;
+            res[4 * k + 3] += wo * x.w;
           }
         }
         const int64_t qhead = static_cast<int64_t>(h) * G + hh;
