@@ -406,12 +406,11 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     const uint32_t sbase = smem_u32(sb);
     const uint32_t mask = lds32(smem_u32(sMask + st));
 
-    // ---- q . K^T for this warp's 16 keys: acc[nt][parity of the head-dim block]
-    float acc[2][2][4];
+    // ---- q . K^T for this warp's 16 keys: one accumulator per N-tile (the two chains
+    //      interleave; splitting each further measured no faster)
+    float acc[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int pz = 0; pz < 2; ++pz) acc[nt][pz][0] = acc[nt][pz][1] = acc[nt][pz][2] = acc[nt][pz][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
     uint32_t rowK[2];
     int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
 #pragma unroll
@@ -450,11 +449,11 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           if (F::kBf16) {
-            mma_bf16(acc[nt][blk & 1], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
+            mma_bf16(acc[nt], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
           } else if (F::kInt8) {
-            mma_f16(acc[nt][blk & 1], qa, i8pair_to_f16x2(kw[nt][ks]), i8pair_to_f16x2(kw[nt][ks] >> 8));
+            mma_f16(acc[nt], qa, i8pair_to_f16x2(kw[nt][ks]), i8pair_to_f16x2(kw[nt][ks] >> 8));
           } else {
-            mma_f16(acc[nt][blk & 1], qa, e4m3pair_to_f16x2(kw[nt][ks]), e4m3pair_to_f16x2(kw[nt][ks] >> 16));
+            mma_f16(acc[nt], qa, e4m3pair_to_f16x2(kw[nt][ks]), e4m3pair_to_f16x2(kw[nt][ks] >> 16));
           }
         }
       }
@@ -482,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         // (padding keys already carry a zero V scale: their scale copies zero-fill)
         vsc[nt][e] = vs;
         vmx = fmaxf(vmx, vs);
-        const float x0 = acc[nt][0][e] + acc[nt][1][e];
-        const float x1 = acc[nt][0][2 + e] + acc[nt][1][2 + e];
+        const float x0 = acc[nt][e];
+        const float x1 = acc[nt][2 + e];
         s[nt][e] = valid ? x0 * fac0 * ksc : -INFINITY;
         s[nt][2 + e] = valid ? x1 * fac1 * ksc : -INFINITY;
         mx0 = fmaxf(mx0, s[nt][e]);
@@ -713,6 +712,31 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   // the accumulators carry p times 2^(kPShift - eu) (int8) or 2^kPShift (E4M3); that power of
   // two is undone in the combine weights rather than on every accumulator value
   if (lane == 0) sPost[warp] = F::kInt8 ? pow2f(eu - kPShift) : (F::kE4m3 ? pow2f(-kPShift) : 1.f);
+  __syncthreads();
+  // combine weights, once per CTA: thread (hh, part) owns head hh and a quarter of each half's
+  // head dims; warp w's partial enters with exp2(m_w - M) 2^(its pre-scale) / l
+  const int hh = tid >> 3, part = tid & 7;
+  float wo[kWarps];
+  float lse_h = -INFINITY;
+  if (hh < G) {
+    float mw[kWarps], M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mw[w] = sM[w * 16 + hh];
+      M = fmaxf(M, mw[w]);
+    }
+    float ww[kWarps], lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      ww[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
+      lsum += ww[w] * sL[w * 16 + hh];
+    }
+    float f = (lsum > 0.f) ? 1.f / lsum : 0.f;
+    if (F::kE4m3 && P == 1) f *= a.v_scale_layer;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) wo[w] = ww[w] * sPost[w] * f;
+    lse_h = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+  }
 #pragma unroll 1
   for (int sw = 0; sw < 2; ++sw) {
     {
@@ -750,39 +774,23 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     }
     __syncthreads();
     {
-      // head hh; part covers the local head dims d(k) .. d(k) + 3, k = 0..3 (natural layouts:
+      // part covers the local head dims d(k) .. d(k) + 3, k = 0..3 (natural layouts:
       // d(k) = 4 part + 32 k, so that 8 consecutive threads read all 32 banks; others:
       // d(k) = 16 part + 4 k, stored at 40 (part / 2) + 16 (part % 2) + 4 k)
-      const int hh = tid >> 3, part = tid & 7;
       if (hh < G) {
-        float mw[kWarps], M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          mw[w] = sM[w * 16 + hh];
-          M = fmaxf(M, mw[w]);
-        }
-        float ww[kWarps], lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          ww[w] = (mw[w] == -INFINITY) ? 0.f : fast_exp2(mw[w] - M);
-          lsum += ww[w] * sL[w * 16 + hh];
-        }
-        float f = (lsum > 0.f) ? 1.f / lsum : 0.f;
-        if (F::kE4m3 && P == 1) f *= a.v_scale_layer;
         float res[16];
 #pragma unroll
         for (int i2 = 0; i2 < 16; ++i2) res[i2] = 0.f;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float* src = sO + (w * 16 + hh) * kORow + (F::kNatural ? 4 * part : 40 * (part >> 1) + 16 * (part & 1));
-          const float wo = ww[w] * sPost[w];  // exact: the post factor is a power of two
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float4 x = *reinterpret_cast<const float4*>(src + (F::kNatural ? 32 * k : 4 * k));
-            res[4 * k] += wo * x.x;
-            res[4 * k + 1] += wo * x.y;
-            res[4 * k + 2] += wo * x.z;
-            res[4 * k + 3] += wo * x.w;
+            res[4 * k] += wo[w] * x.x;
+            res[4 * k + 1] += wo[w] * x.y;
+            res[4 * k + 2] += wo[w] * x.z;
+            res[4 * k + 3] += wo[w] * x.w;
           }
         }
         const int64_t qhead = static_cast<int64_t>(h) * G + hh;
@@ -792,9 +800,9 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           *reinterpret_cast<float4*>(dst + (F::kNatural ? 32 * k : 4 * k)) =
-              make_float4(res[4 * k] * f, res[4 * k + 1] * f, res[4 * k + 2] * f, res[4 * k + 3] * f);
+              make_float4(res[4 * k], res[4 * k + 1], res[4 * k + 2], res[4 * k + 3]);
         if (sw == 0 && part == 0) {
-          const float lse = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;
+          const float lse = lse_h;
           if (P == 1) {
             if (a.lse != nullptr) a.lse[r * Hq + qhead] = lse;
           } else {
