@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   __syncthreads();
   tmem_fence_after_sync();
   const float fac0 = sFac[h0], fac1 = sFac[h1];
+  const uint64_t fac00 = f2pack(fac0, fac0), fac11 = f2pack(fac1, fac1);
   // this warp's accumulator: its 32 TMEM lanes, columns [0, 128); column 4 t + j holds the
   // C-fragment value j of N-tile t
   const uint32_t tacc = *sTmem + (static_cast<uint32_t>(32 * warp) << 16);
@@ -392,7 +393,9 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 
   // ---------------- online-softmax state (per warp)
   float mu0 = -INFINITY, mu1 = -INFINITY;  // running max in use (log2 domain), heads h0, h1
-  float l0 = 0.f, l1 = 0.f;                // this thread's share of sum p
+  // this thread's share of sum p for heads h0 (l0) and h1 (l1), each kept as a pair of
+  // partial sums (keys e = 0 and e = 1) so that it accumulates with packed adds
+  uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
   int eu = -100;                           // int8: 2^eu > every V scale seen
   for (int i = 0; i < my; ++i) {
     if (i + F::kStages - 1 < my) issue(i + F::kStages - 1, nidx);
@@ -464,11 +467,14 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     float vsc[2][2];
     float mx0 = -INFINITY, mx1 = -INFINITY, vmx = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < 2; ++nt) {
+      float ksc2[2];
+      bool valid2[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int kt = key_of<FMT>(nt, 2 * c + e);
         const bool valid = (mask >> kt) & 1u;
+        valid2[e] = valid;
         float ksc = 1.f, vs = 0.f;
         if (F::kSide) {
           ksc = __uint_as_float(lds32(sbase + L::kStageKs + kt * 4));
@@ -481,13 +487,20 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         // (padding keys already carry a zero V scale: their scale copies zero-fill)
         vsc[nt][e] = vs;
         vmx = fmaxf(vmx, vs);
-        const float x0 = acc[nt][e];
-        const float x1 = acc[nt][2 + e];
-        s[nt][e] = valid ? x0 * fac0 * ksc : -INFINITY;
-        s[nt][2 + e] = valid ? x1 * fac1 * ksc : -INFINITY;
-        mx0 = fmaxf(mx0, s[nt][e]);
-        mx1 = fmaxf(mx1, s[nt][2 + e]);
+        ksc2[e] = ksc;
       }
+      // logits of keys e = 0, 1 for heads h0 (acc 0, 1) and h1 (acc 2, 3), as fp32 pairs
+      const uint64_t kk = f2pack(ksc2[0], ksc2[1]);
+      float t0, t1, t2, t3;
+      f2unpack(f2mul(f2pack(acc[nt][0], acc[nt][1]), f2mul(fac00, kk)), t0, t1);
+      f2unpack(f2mul(f2pack(acc[nt][2], acc[nt][3]), f2mul(fac11, kk)), t2, t3);
+      s[nt][0] = valid2[0] ? t0 : -INFINITY;
+      s[nt][1] = valid2[1] ? t1 : -INFINITY;
+      s[nt][2] = valid2[0] ? t2 : -INFINITY;
+      s[nt][3] = valid2[1] ? t3 : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+      mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+    }
 #pragma unroll
     for (int off = 1; off <= 2; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -520,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       if (rescale) {
         rf0 = al0 * ov;
         rf1 = al1 * ov;
-        l0 *= al0;
-        l1 *= al1;
+        l0 = f2mul(l0, f2pack(al0, al0));
+        l1 = f2mul(l1, f2pack(al1, al1));
       }
       mu0 = nm0;
       mu1 = nm1;
@@ -535,29 +548,45 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       // a head whose max is still -inf has only masked (-inf) logits: subtracting the most
       // negative finite float instead gives exp2(-inf) = 0 rather than exp2(NaN)
       const float m0 = fmaxf(mu0, -kMaxFinite), m1 = fmaxf(mu1, -kMaxFinite);
+      const uint64_t mm0 = f2pack(m0, m0), mm1 = f2pack(m1, m1), pm2 = f2pack(pm, pm);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         float p[4];
-        p[0] = fast_exp2(s[nt][0] - m0);  // masked: exp2(-inf) = 0
-        p[1] = fast_exp2(s[nt][1] - m0);
-        p[2] = fast_exp2(s[nt][2] - m1);
-        p[3] = fast_exp2(s[nt][3] - m1);
-        l0 += p[0] + p[1];
-        l1 += p[2] + p[3];
-        const float f0 = F::kInt8 ? vsc[nt][0] * pm : pm, f1 = F::kInt8 ? vsc[nt][1] * pm : pm;
-        const float x0 = p[0] * f0, x1 = p[1] * f1, x2 = p[2] * f0, x3 = p[3] * f1;
+        {
+          float d0, d1, d2, d3;
+          f2unpack(f2sub(f2pack(s[nt][0], s[nt][1]), mm0), d0, d1);
+          f2unpack(f2sub(f2pack(s[nt][2], s[nt][3]), mm1), d2, d3);
+          p[0] = fast_exp2(d0);  // masked: exp2(-inf) = 0
+          p[1] = fast_exp2(d1);
+          p[2] = fast_exp2(d2);
+          p[3] = fast_exp2(d3);
+        }
+        const uint64_t p01 = f2pack(p[0], p[1]), p23 = f2pack(p[2], p[3]);
+        l0 = f2add(l0, p01);
+        l1 = f2add(l1, p23);
+        // x = p times the key's V scale (int8) and the power-of-two pre-scale
+        const uint64_t f01 = F::kInt8 ? f2mul(f2pack(vsc[nt][0], vsc[nt][1]), pm2) : pm2;
+        float x0, x1, x2, x3;
+        const uint64_t x01 = f2mul(p01, f01), x23 = f2mul(p23, f01);
+        f2unpack(x01, x0, x1);
+        f2unpack(x23, x2, x3);
+        float r0, r1, r2, r3;
         if (F::kBf16) {
           const __nv_bfloat162 a0 = __floats2bfloat162_rn(x0, x1), a1 = __floats2bfloat162_rn(x2, x3);
           pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&a0);
           pa[2 * nt + 1] = *reinterpret_cast<const uint32_t*>(&a1);
-          pl[2 * nt] = pack_bf162(x0 - __low2float(a0), x1 - __high2float(a0));
-          pl[2 * nt + 1] = pack_bf162(x2 - __low2float(a1), x3 - __high2float(a1));
+          f2unpack(f2sub(x01, f2pack(__low2float(a0), __high2float(a0))), r0, r1);
+          f2unpack(f2sub(x23, f2pack(__low2float(a1), __high2float(a1))), r2, r3);
+          pl[2 * nt] = pack_bf162(r0, r1);
+          pl[2 * nt + 1] = pack_bf162(r2, r3);
         } else {
           const __half2 a0 = __floats2half2_rn(x0, x1), a1 = __floats2half2_rn(x2, x3);
           pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&a0);
           pa[2 * nt + 1] = *reinterpret_cast<const uint32_t*>(&a1);
-          pl[2 * nt] = pack_half2(x0 - __low2float(a0), x1 - __high2float(a0));
-          pl[2 * nt + 1] = pack_half2(x2 - __low2float(a1), x3 - __high2float(a1));
+          f2unpack(f2sub(x01, f2pack(__low2float(a0), __high2float(a0))), r0, r1);
+          f2unpack(f2sub(x23, f2pack(__low2float(a1), __high2float(a1))), r2, r3);
+          pl[2 * nt] = pack_half2(r0, r1);
+          pl[2 * nt + 1] = pack_half2(r2, r3);
         }
       }
     }
@@ -656,14 +685,13 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         tmem_wait_ld(ob[0]);
         tmem_wait_ld(ob[1]);
         if (rescale) {
+          const uint64_t r00 = f2pack(rf0, rf0), r11 = f2pack(rf1, rf1);
 #pragma unroll
           for (int b = 0; b < 2; ++b)
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-              ob[b][4 * t] *= rf0;
-              ob[b][4 * t + 1] *= rf0;
-              ob[b][4 * t + 2] *= rf1;
-              ob[b][4 * t + 3] *= rf1;
+              f2scale(&ob[b][4 * t], r00);
+              f2scale(&ob[b][4 * t + 2], r11);
             }
         }
 #pragma unroll
@@ -693,8 +721,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   cp_async_wait<0>();
 #pragma unroll
   for (int off = 1; off <= 2; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    l0 = f2add(l0, __shfl_xor_sync(0xffffffffu, l0, off));
+    l1 = f2add(l1, __shfl_xor_sync(0xffffffffu, l1, off));
   }
   tmem_wait_st();
   __syncthreads();  // every warp is done with its ring: reuse the rings as the merge buffer
@@ -706,8 +734,11 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   if (c == 0) {
     sM[warp * 16 + h0] = mu0;
     sM[warp * 16 + h1] = mu1;
-    sL[warp * 16 + h0] = l0;
-    sL[warp * 16 + h1] = l1;
+    float a0, b0, a1, b1;
+    f2unpack(l0, a0, b0);
+    f2unpack(l1, a1, b1);
+    sL[warp * 16 + h0] = a0 + b0;
+    sL[warp * 16 + h1] = a1 + b1;
   }
   // the accumulators carry p times 2^(kPShift - eu) (int8) or 2^kPShift (E4M3); that power of
   // two is undone in the combine weights rather than on every accumulator value
@@ -778,19 +809,18 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       // d(k) = 4 part + 32 k, so that 8 consecutive threads read all 32 banks; others:
       // d(k) = 16 part + 4 k, stored at 40 (part / 2) + 16 (part % 2) + 4 k)
       if (hh < G) {
-        float res[16];
+        uint64_t res[8];  // 16 floats as packed pairs
 #pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) res[i2] = 0.f;
+        for (int i2 = 0; i2 < 8; ++i2) res[i2] = f2pack(0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
           const float* src = sO + (w * 16 + hh) * kORow + (F::kNatural ? 4 * part : 40 * (part >> 1) + 16 * (part & 1));
+          const uint64_t ww2 = f2pack(wo[w], wo[w]);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float4 x = *reinterpret_cast<const float4*>(src + (F::kNatural ? 32 * k : 4 * k));
-            res[4 * k] += wo[w] * x.x;
-            res[4 * k + 1] += wo[w] * x.y;
-            res[4 * k + 2] += wo[w] * x.z;
-            res[4 * k + 3] += wo[w] * x.w;
+            res[2 * k] = f2fma(f2pack(x.x, x.y), ww2, res[2 * k]);
+            res[2 * k + 1] = f2fma(f2pack(x.z, x.w), ww2, res[2 * k + 1]);
           }
         }
         const int64_t qhead = static_cast<int64_t>(h) * G + hh;
@@ -798,9 +828,12 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
                               : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
         dst += 128 * sw + (F::kNatural ? 4 * part : 16 * part);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<float4*>(dst + (F::kNatural ? 32 * k : 4 * k)) =
-              make_float4(res[4 * k], res[4 * k + 1], res[4 * k + 2], res[4 * k + 3]);
+        for (int k = 0; k < 4; ++k) {
+          float4 y;
+          f2unpack(res[2 * k], y.x, y.y);
+          f2unpack(res[2 * k + 1], y.z, y.w);
+          *reinterpret_cast<float4*>(dst + (F::kNatural ? 32 * k : 4 * k)) = y;
+        }
         if (sw == 0 && part == 0) {
           const float lse = lse_h;
           if (P == 1) {
