@@ -341,14 +341,22 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     int sg = 0;
     if (!F::kBf16) {
       // fp16 operands: a power of two puts the head's largest |q| in [2^14, 2^15)
-      uint32_t m = 0;
+      // packed bf16 |q| maximum over the thread's 32 dims (bf16 bits order like values when
+      // non-negative), then the larger half as fp32 bits
+      __nv_bfloat162 mh = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) m = max(m, max((w[i] & 0x7FFFu) << 16, w[i] & 0x7FFF0000u));
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t a16 = w[i] & 0x7FFF7FFFu;
+        mh = __hmax2(mh, *reinterpret_cast<const __nv_bfloat162*>(&a16));
+      }
+      const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mh);
+      uint32_t m = max((mw & 0xFFFFu) << 16, mw & 0xFFFF0000u);
 #pragma unroll
       for (int off = 1; off <= 4; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
       sg = m ? max(-64, min(64, 14 - (static_cast<int>(m >> 23) - 127))) : 0;
     }
     const float u = pow2f(sg);
+    const uint64_t uu = f2pack(u, u);
     // two head dims per 32-bit store: the pair that shares a B-fragment register of a code
     // word (int8: d, d + 2; E4M3 and bf16: d, d + 1) sits in adjacent k-indices
 #pragma unroll
@@ -364,7 +372,9 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         if (F::kBf16) {
           v32 = b0 | (b1 << 16);
         } else {
-          v32 = pack_half2(__uint_as_float(b0 << 16) * u, __uint_as_float(b1 << 16) * u);
+          float s0, s1;
+          f2unpack(f2mul(f2pack(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16)), uu), s0, s1);
+          v32 = pack_half2(s0, s1);
         }
         sts32(smem_u32(smem + L::kQ + q_off(blk * 4 + ks, qh, up * 8 + 2 * cc)), v32);
       }
@@ -465,7 +475,22 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     // ---- logits with the hoisted K scale; masked keys -> -inf
     float s[2][4];  // [nt][0..1: head h0 keys e=0,1; 2..3: head h1]
     float vsc[2][2];
-    float mx0 = -INFINITY, mx1 = -INFINITY, vmx = 0.f;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+    // int8: the tile's largest |V scale|, as fp32 bits (non-negative floats order as integers):
+    // lane k < 16 reads key k's scale, one warp-wide integer max reduces them
+    uint32_t vmx_bits = 0;
+    if (F::kInt8) {
+      uint32_t vb = 0;
+      if (lane < kKeys) {
+        if (F::kSide) {
+          vb = lds32(sbase + L::kStageKs + (kKeys + lane) * 4);
+        } else {
+          const int dl = lds_u8(sbase + L::kStageMeta + lane);
+          vb = lds32(sbase + v_row_off<FMT>(lane) + dl + kHeadDim);
+        }
+      }
+      vmx_bits = __reduce_max_sync(0xffffffffu, vb & 0x7FFFFFFFu);
+    }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       float ksc2[2];
@@ -486,7 +511,6 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         }
         // (padding keys already carry a zero V scale: their scale copies zero-fill)
         vsc[nt][e] = vs;
-        vmx = fmaxf(vmx, vs);
         ksc2[e] = ksc;
       }
       // logits of keys e = 0, 1 for heads h0 (acc 0, 1) and h1 (acc 2, 3), as fp32 pairs
@@ -505,7 +529,6 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     for (int off = 1; off <= 2; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      if (F::kInt8) vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, off));
     }
 
     // ---- lazy rescale: raise the max in use only past the threshold
@@ -520,17 +543,17 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       // to the fp16 subnormal range, where their absolute error stays below 2^-25 of the
       // 2^(eu - 3) unit -- far under the result's tolerance.
       int ne = eu;
-      if (F::kInt8 && vmx > 0.f) {
-        const int ev = static_cast<int>(__float_as_uint(vmx) >> 23) - 126;  // 2^ev > vmx
+      if (F::kInt8 && vmx_bits != 0u) {
+        const int ev = static_cast<int>(vmx_bits >> 23) - 126;  // 2^ev > the largest |V scale|
         if (ev > eu) ne = ev + kEuHeadroom;
       }
-      const float ov = F::kInt8 ? pow2f(max(eu - ne, -126)) : 1.f;
-      const float al0 = (nm0 == mu0) ? 1.f : fast_exp2(mu0 - nm0);  // mu0 = -inf gives 0
-      const float al1 = (nm1 == mu1) ? 1.f : fast_exp2(mu1 - nm1);
       // an accumulator row whose head has seen no valid key yet is still zero: it needs no rescale
       const bool live0 = mu0 != -INFINITY, live1 = mu1 != -INFINITY;
       rescale = __any_sync(0xffffffffu, (live0 && (nm0 != mu0 || ne != eu)) || (live1 && (nm1 != mu1 || ne != eu)));
-      if (rescale) {
+      if (rescale) {  // rare: the factors are only formed here
+        const float ov = F::kInt8 ? pow2f(max(eu - ne, -126)) : 1.f;
+        const float al0 = (nm0 == mu0) ? 1.f : fast_exp2(mu0 - nm0);  // mu0 = -inf gives 0
+        const float al1 = (nm1 == mu1) ? 1.f : fast_exp2(mu1 - nm1);
         rf0 = al0 * ov;
         rf1 = al1 * ov;
         l0 = f2mul(l0, f2pack(al0, al0));
