@@ -118,8 +118,7 @@ struct Smem {
   static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][kStages] stages
   static constexpr size_t kWarpRing = size_t(F::kStages) * kStageBytes;
   static constexpr size_t kTmem = kRing + kWarps * kWarpRing;  // TMEM base address
-  static constexpr size_t kMask = kTmem + 16;                     // [kWarps][kStages] uint32
-  static constexpr size_t kM = kMask + kWarps * F::kStages * 4;      // [kWarps][16] floats
+  static constexpr size_t kM = kTmem + 16;                         // [kWarps][16] floats
   static constexpr size_t kL = kM + kWarps * 16 * 4;                 // [kWarps][16] floats
   static constexpr size_t kPost = kL + kWarps * 16 * 4;             // [kWarps] floats
   static constexpr size_t kTotal = kPost + kWarps * 4;
@@ -191,7 +190,6 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const int col0 = min(a.topk, split * per_split);
   const int col1 = min(a.topk, col0 + per_split);
   float* sFac = reinterpret_cast<float*>(smem + L::kFac);
-  uint32_t* sMask = reinterpret_cast<uint32_t*>(smem + L::kMask) + warp * F::kStages;
   uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
   const uint32_t sQ = smem_u32(smem + L::kQ);
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kTmem);
@@ -240,12 +238,12 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT>(key_sub) + 16 * chunk_sub;
   const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(key_sub) - L::kStageV + 16 * chunk_sub;
 
-  // Copy one 16-key tile into ring stage i % kStages.
-  auto issue = [&](int i, int raw_idx) {
+  // Copy one 16-key tile into ring stage i % kStages; returns the tile's valid-key mask.
+  static_assert(F::kStages == 2, "the valid-key masks ride one tile ahead in registers");
+  auto issue = [&](int i, int raw_idx) -> uint32_t {
     const int idxv = checked(raw_idx);
     const int st = i % F::kStages;
     const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
-    if (lane == 0) sMask[st] = mask;
     uint8_t* sb = ring + size_t(st) * L::kStageBytes;
     const uint32_t sbase = smem_u32(sb);
     // record number (slot * H + h; the host keeps it below 2^31) of key `lane`, -1 = padding
@@ -304,21 +302,18 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       const float* gs = (lane >> 4) ? a.v_scale_tok : a.k_scale_tok;
       cp_async4(sbase + L::kStageKs + lane * 4, gs + max(rec, 0), rec >= 0 ? 4 : 0);
     }
+    return mask;
   };
 
   // Start the first tiles' index loads and copies before staging the query, so their
   // latencies overlap the query's.
   int nidx;
+  uint32_t mask_cur = 0;  // valid keys of the tile being computed (bit k = key k)
   {
-    int first[F::kStages];
-#pragma unroll
-    for (int t = 0; t < F::kStages; ++t) first[t] = load_idx(t);
-#pragma unroll
-    for (int t = 0; t < F::kStages - 1; ++t) {
-      if (t < my) issue(t, first[t]);
-      cp_async_commit();
-    }
-    nidx = first[F::kStages - 1];
+    const int first = load_idx(0);
+    nidx = load_idx(1);
+    if (0 < my) mask_cur = issue(0, first);
+    cp_async_commit();
   }
 
   // ---------------- stage the query once: 8 threads per head, 32 head dims each
@@ -408,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
   int eu = -100;                           // int8: 2^eu > every V scale seen
   for (int i = 0; i < my; ++i) {
-    if (i + F::kStages - 1 < my) issue(i + F::kStages - 1, nidx);
+    const uint32_t mask_next = (i + 1 < my) ? issue(i + 1, nidx) : 0u;
     cp_async_commit();
     nidx = load_idx(i + F::kStages);
     cp_async_wait<F::kStages - 1>();
@@ -417,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 
     const uint8_t* sb = ring + size_t(st) * L::kStageBytes;
     const uint32_t sbase = smem_u32(sb);
-    const uint32_t mask = lds32(smem_u32(sMask + st));
+    const uint32_t mask = mask_cur;
 
     // ---- q . K^T for this warp's 16 keys: one accumulator per N-tile (the two chains
     //      interleave; splitting each further measured no faster)
@@ -737,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         tmem_st32(tacc + 64 * sw + 32, ob[1]);
       }
     }
+    mask_cur = mask_next;
     __syncwarp();
   }
 
