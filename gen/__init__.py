@@ -10,6 +10,7 @@ from .workloads import (  # noqa: F401
     f32_to_bf16_bits,
     long_context_decode,
     page1_shape,
+    small_paged,
     small_random,
     tiny,
 )

@@ -61,18 +61,24 @@ class Workload:
     v_tokens: np.ndarray  # uint16 bf16 bits [T, Hkv, D]
     slot_mapping: np.ndarray  # int64 [T], token -> slot, -1 = skip
     q: np.ndarray  # uint16 bf16 bits [R, Hq, D]
-    topk: np.ndarray  # int32 [R, k], slot ids, -1 = padding
+    topk: Optional[np.ndarray]  # int32 [R, k], slot ids, -1 = padding (None: paged rows only)
     softmax_scale: float
     num_splits: int = 1
     # Per-step write of new tokens (decode step): bf16 bits [Tn, Hkv, D] and slots [Tn].
     step_k: Optional[np.ndarray] = None
     step_v: Optional[np.ndarray] = None
     step_slots: Optional[np.ndarray] = None
+    # Paged pools: block table int32 [num_seqs, max_blocks], each row's sequence int32 [R] and
+    # its entries as logical positions int32 [R, k] (-1 = padding), blocks of block_size slots.
+    block_table: Optional[np.ndarray] = None
+    row_seq: Optional[np.ndarray] = None
+    topk_pos: Optional[np.ndarray] = None
+    block_size: int = 0
     notes: str = ""
 
     @property
     def rows(self) -> int:
-        return int(self.topk.shape[0])
+        return int((self.topk if self.topk is not None else self.topk_pos).shape[0])
 
     @property
     def topk_len(self) -> int:
@@ -207,6 +213,7 @@ def long_context_decode(seed: int = 3, num_seqs: int = 8, context: int = 131072,
     R = num_seqs * rows_per_seq
     q = f32_to_bf16_bits(_normals(rng, (R, H * G, D)))
     idx = np.empty((R, topk), dtype=np.int32)
+    pos_out = np.empty((R, topk), dtype=np.int32)
     older = context - recent
     for b in range(num_seqs):
         base = b * context
@@ -216,10 +223,15 @@ def long_context_decode(seed: int = 3, num_seqs: int = 8, context: int = 131072,
             far = rng.choice(older, size=topk - recent_picks, replace=False)
             positions = np.concatenate([near, far])
             idx[r] = slot_mapping[base + positions]
+            pos_out[r] = positions
+    block_table = block_perm.reshape(num_seqs, n_blocks_seq).astype(np.int32)
+    row_seq = np.repeat(np.arange(num_seqs, dtype=np.int32), rows_per_seq)
     return Workload(f"long-context decode (8 x {context} ctx, paged blocks of {block}, R={R}, k={topk})",
                     seed, S, H, H * G, D, k, v, slot_mapping, q, idx,
                     softmax_scale=1.0 / 16.0, num_splits=num_splits,
-                    notes="block table applied in the generator; kernel sees slot ids")
+                    block_table=block_table, row_seq=row_seq, topk_pos=pos_out, block_size=block,
+                    notes="topk holds the slot ids placed by the generator; topk_pos/block_table/row_seq "
+                          "give the same rows as logical positions of a paged pool")
 
 
 def chunked_prefill(seed: int = 4, new_tokens: int = 8192, num_slots: int = 524288,
@@ -281,6 +293,36 @@ def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: i
                     seed, S, H, num_q_heads, D, _scaled_bf16(k, factor), _scaled_bf16(v, factor),
                     slot_mapping, q, idx, softmax_scale=softmax_scale, num_splits=num_splits)
 
+
+
+def small_paged(seed: int, num_seqs: int = 3, max_blocks: int = 6, block_size: int = 16, rows: int = 5,
+                topk: int = 40, pad_frac: float = 0.1, unallocated_frac: float = 0.15,
+                num_q_heads: int = 16, num_kv_heads: int = 1) -> Workload:
+    """A small paged pool: num_seqs x max_blocks blocks of block_size slots, each sequence's
+    blocks a random permutation of the pool's blocks, some table entries unallocated (-1).
+
+    Rows draw distinct positions of their sequence (some landing in unallocated blocks, which
+    the library must flag) plus -1 padding. Slot ids are left to the oracle's translation.
+    """
+    H, D, Hq = num_kv_heads, HEAD_DIM, num_q_heads
+    rng = np.random.default_rng(seed)
+    total_blocks = num_seqs * max_blocks
+    S = total_blocks * block_size
+    k = f32_to_bf16_bits(_normals(rng, (S, H, D)))
+    v = f32_to_bf16_bits(_normals(rng, (S, H, D)))
+    slot_mapping = np.arange(S, dtype=np.int64)  # token t lives in slot t
+    table = rng.permutation(total_blocks).astype(np.int32).reshape(num_seqs, max_blocks)
+    table[rng.random(table.shape) < unallocated_frac] = -1
+    q = f32_to_bf16_bits(_normals(rng, (rows, Hq, D)))
+    row_seq = rng.integers(0, num_seqs, size=rows).astype(np.int32)
+    pos = np.empty((rows, topk), dtype=np.int32)
+    for r in range(rows):
+        pos[r] = rng.choice(max_blocks * block_size, size=topk, replace=False)
+        pos[r, rng.random(topk) < pad_frac] = -1
+    return Workload(f"small paged pool (seed {seed}, {num_seqs} seqs x {max_blocks} blocks of {block_size})",
+                    seed, S, H, Hq, D, k, v, slot_mapping, q, None, softmax_scale=1.0 / 16.0,
+                    block_table=table, row_seq=row_seq, topk_pos=pos, block_size=block_size,
+                    notes="paged rows only: slot ids come from the block table")
 
 CONFIGS = {
     1: tiny,

@@ -196,6 +196,35 @@ qkv_status qsa_gather_attn_splitk_noalloc(const void* q, int64_t rows, int num_q
                                           int num_splits, float* out, float* lse,
                                           uint32_t* dev_status, void* stream);
 
+/*
+ * qsa_gather_attn_paged -- qsa_gather_attn over a paged pool: rows give logical token
+ * positions in their sequence, and the kernel maps them to slots through a block table.
+ *                       [E4M3-PR §Implementation scope: the KV reads run over paged
+ *                        ("page4") storage; the block-table interface is the usual
+ *                        vLLM-style one, not defined on the pages]
+ *   For row r with sequence s = row_seq[r] and entry p = topk_pos[r, j]:
+ *     slot = block_table[s * max_blocks + p / block_size] * block_size + p % block_size,
+ *   then exactly as qsa_gather_attn with that slot. p = -1 is padding. These are flagged
+ *   with QKV_DEV_BAD_INDEX and treated as padding: p < -1 or p >= max_blocks * block_size,
+ *   a block id < 0 (unallocated), and a slot >= num_slots. A row whose s lies outside
+ *   [0, num_seqs) is flagged once and is empty (o = 0, lse = -inf).
+ *   block_table  int32 [num_seqs, max_blocks], block ids in units of block_size slots.
+ *   row_seq      int32 [rows].
+ *   topk_pos     int32 [rows, topk].
+ *   block_size   >= 1; max_blocks >= 1; num_seqs >= 1; max_blocks * block_size < 2^31.
+ *   Everything else -- formats, scales, splits, outputs, errors -- as qsa_gather_attn. The
+ *   result equals qsa_gather_attn on the translated slot ids, bit for bit.
+ */
+qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                                 int head_dim, qkv_format fmt, const void* k_cache,
+                                 const void* v_cache, const float* k_scale_tok,
+                                 const float* v_scale_tok, float k_scale_layer, float v_scale_layer,
+                                 int64_t num_slots, const int32_t* block_table, int64_t num_seqs,
+                                 int max_blocks, int block_size, const int32_t* row_seq,
+                                 const int32_t* topk_pos, int topk, float softmax_scale,
+                                 int num_splits, float* out, float* lse, float* o_part,
+                                 float* lse_part, uint32_t* dev_status, void* stream);
+
 /* Static, human-readable name of a status code. Never NULL. */
 const char* qkv_status_str(qkv_status s);
 

@@ -12,6 +12,7 @@ It is written to be read against the pages, not to be fast:
                E4M3 bytes).
 * attention.py fp64 dequantisation of a slot pool, top-k gather attention with a
                max-subtracted softmax, the split-K partition and the log-sum-exp merge.
+* paging.py    logical positions of a paged pool -> slot ids through a block table.
 
 Pages cited (by title):
   [INT8-PR]  "int8 per-(token,head) KV cache for the Qwen3.8-Flash-Next QSA path"
@@ -24,4 +25,4 @@ Every function is pinned by a test under tests/ that does not re-derive it (clos
 library routines on special cases, brute force, invariants, hand-worked fixtures).
 """
 
-from . import attention, quant  # noqa: F401
+from . import attention, paging, quant  # noqa: F401

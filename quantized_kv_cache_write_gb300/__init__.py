@@ -40,6 +40,8 @@ _SIGS = {
     "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
     "qsa_gather_attn_splitk_noalloc": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p,
                                        _i32, _f32, _i32, _p, _p, _p, _p],
+    "qsa_gather_attn_paged": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i64, _i32,
+                              _i32, _p, _p, _i32, _f32, _i32, _p, _p, _p, _p, _p, _p],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -140,6 +142,31 @@ def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: floa
                              _ptr(topk_idx), topk, float(softmax_scale), num_splits, _ptr(out), _ptr(lse),
                              _ptr(o_part), _ptr(lse_part), _ptr(dev_status), _stream(stream))
     _check("qsa_gather_attn", st)
+
+
+def qsa_gather_attn_paged(q, fmt: int, k_cache, v_cache, block_table, row_seq, topk_pos, block_size: int,
+                          softmax_scale: float, *, num_kv_heads: int = 1, num_slots: Optional[int] = None,
+                          k_scale_tok=None, v_scale_tok=None, k_scale_layer: float = 1.0,
+                          v_scale_layer: float = 1.0, num_splits: int = 1, out=None, lse=None, o_part=None,
+                          lse_part=None, dev_status=None, stream=None):
+    """Top-k gather decode attention over a paged pool.
+
+    block_table int32 [num_seqs, max_blocks]; row_seq int32 [R]; topk_pos int32 [R, k] logical
+    positions (-1 padding); slot = block_table[seq, pos // block_size] * block_size + pos % block_size.
+    """
+    _check_gather_shapes(q, topk_pos, num_splits, out, lse, o_part, lse_part)
+    R, Hq, D = q.shape
+    if block_table.dim() != 2 or row_seq.dim() != 1 or row_seq.shape[0] != R:
+        raise ValueError(f"block_table must be [num_seqs, max_blocks] and row_seq [{R}]")
+    S = k_cache.shape[0] if num_slots is None else num_slots
+    topk = topk_pos.shape[1] if topk_pos is not None else 0
+    st = lib.qsa_gather_attn_paged(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer),
+                                   float(v_scale_layer), S, _ptr(block_table), block_table.shape[0],
+                                   block_table.shape[1], int(block_size), _ptr(row_seq), _ptr(topk_pos), topk,
+                                   float(softmax_scale), num_splits, _ptr(out), _ptr(lse), _ptr(o_part),
+                                   _ptr(lse_part), _ptr(dev_status), _stream(stream))
+    _check("qsa_gather_attn_paged", st)
 
 
 def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1.0, stream=None):

@@ -31,6 +31,10 @@ SOURCES = [
     "gather_e4m3.cu",
     "gather_bf16.cu",
     "gather_noalloc.cu",
+    "gather_paged_int8_side.cu",
+    "gather_paged_int8_inline.cu",
+    "gather_paged_e4m3.cu",
+    "gather_paged_bf16.cu",
 ]
 HEADERS = ["qkv_internal.cuh", "gather_attn.cuh"]
 

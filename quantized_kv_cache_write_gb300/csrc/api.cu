@@ -87,12 +87,31 @@ qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, flo
   return cuda_status(qkv::launch_e4m3_calibrate(x, n, amax_bits, scale_out, static_cast<cudaStream_t>(stream)));
 }
 
-qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
-                           qkv_format fmt, const void* k_cache, const void* v_cache, const float* k_scale_tok,
-                           const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
-                           const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
-                           float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Paged-pool arguments of qsa_gather_attn_paged (absent for qsa_gather_attn).
+struct Paging {
+  const int32_t* block_table;
+  const int32_t* row_seq;
+  int64_t num_seqs;
+  int max_blocks;
+  int block_size;
+};
+
+qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
+                       qkv_format fmt, const void* k_cache, const void* v_cache, const float* k_scale_tok,
+                       const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
+                       const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
+                       float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream,
+                       const Paging* pg) {
   if (rows < 0 || topk < 0 || num_splits < 1 || num_slots < 0) return QKV_ERR_ARG;
+  if (pg != nullptr) {
+    if (pg->num_seqs < 1 || pg->max_blocks < 1 || pg->block_size < 1) return QKV_ERR_ARG;
+    if (static_cast<int64_t>(pg->max_blocks) * pg->block_size > INT32_MAX) return QKV_ERR_ARG;
+    if (pg->num_seqs * pg->max_blocks > INT32_MAX) return QKV_ERR_ARG;
+  }
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return QKV_ERR_ARG;
   if (head_dim != kHeadDim || num_q_heads / num_kv_heads > kMaxGroup) return QKV_ERR_UNSUPPORTED;
   if (fmt != QKV_BF16 && fmt != QKV_INT8_SIDE && fmt != QKV_INT8_INLINE && fmt != QKV_E4M3) return QKV_ERR_ARG;
@@ -118,6 +137,10 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
   if ((out && !aligned(out, 16)) || (o_part && !aligned(o_part, 16))) return QKV_ERR_ALIGN;
   if ((lse && !aligned(lse, 4)) || (lse_part && !aligned(lse_part, 4))) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
+  if (pg != nullptr) {
+    if (!pg->block_table || !pg->row_seq) return QKV_ERR_ARG;
+    if (!aligned(pg->block_table, 4) || !aligned(pg->row_seq, 4)) return QKV_ERR_ALIGN;
+  }
 
   qkv::GatherArgs a;
   a.q = static_cast<const __nv_bfloat16*>(q);
@@ -141,6 +164,20 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
   a.lse_part = lse_part;
   a.dev_status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (pg != nullptr) {
+    a.block_table = pg->block_table;
+    a.row_seq = pg->row_seq;
+    a.num_seqs = pg->num_seqs;
+    a.max_blocks = pg->max_blocks;
+    a.block_size = pg->block_size;
+    switch (fmt) {
+      case QKV_BF16: return cuda_status(qkv::launch_gather_paged_bf16(a, s));
+      case QKV_INT8_SIDE: return cuda_status(qkv::launch_gather_paged_int8_side(a, s));
+      case QKV_INT8_INLINE: return cuda_status(qkv::launch_gather_paged_int8_inline(a, s));
+      case QKV_E4M3: return cuda_status(qkv::launch_gather_paged_e4m3(a, s));
+    }
+    return QKV_ERR_ARG;
+  }
   switch (fmt) {
     case QKV_BF16: return cuda_status(qkv::launch_gather_bf16(a, s));
     case QKV_INT8_SIDE: return cuda_status(qkv::launch_gather_int8_side(a, s));
@@ -148,6 +185,34 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
     case QKV_E4M3: return cuda_status(qkv::launch_gather_e4m3(a, s));
   }
   return QKV_ERR_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
+                           qkv_format fmt, const void* k_cache, const void* v_cache, const float* k_scale_tok,
+                           const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
+                           const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
+                           float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream) {
+  return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
+                     k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, num_splits, out, lse,
+                     o_part, lse_part, dev_status, stream, nullptr);
+}
+
+qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
+                                 qkv_format fmt, const void* k_cache, const void* v_cache,
+                                 const float* k_scale_tok, const float* v_scale_tok, float k_scale_layer,
+                                 float v_scale_layer, int64_t num_slots, const int32_t* block_table,
+                                 int64_t num_seqs, int max_blocks, int block_size, const int32_t* row_seq,
+                                 const int32_t* topk_pos, int topk, float softmax_scale, int num_splits,
+                                 float* out, float* lse, float* o_part, float* lse_part, uint32_t* dev_status,
+                                 void* stream) {
+  const Paging pg{block_table, row_seq, num_seqs, max_blocks, block_size};
+  return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
+                     k_scale_layer, v_scale_layer, num_slots, topk_pos, topk, softmax_scale, num_splits, out, lse,
+                     o_part, lse_part, dev_status, stream, &pg);
 }
 
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows, int num_q_heads,

@@ -172,7 +172,9 @@ __device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
   return k * 512 + hd * 32 + ((((kappa >> 3) ^ ((hd >> 2) & 1))) << 4) + (kappa & 7) * 2;
 }
 
-template <int FMT>
+// PAGED: topk_idx holds logical positions of the row's sequence (a.row_seq), mapped to slots
+// through a.block_table; otherwise it holds slot ids.
+template <int FMT, bool PAGED>
 __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_kernel(const GatherArgs a) {
   using F = Fmt<FMT>;
   using L = Smem<FMT>;
@@ -201,7 +203,15 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   // ---------------- this warp's tiles: split tiles warp, warp + 4, ... (an empty pool has
   // no valid index: every row is empty)
   const int ntiles = (col1 - col0 + kKeys - 1) / kKeys;
-  const int my = (ntiles > warp && a.num_slots > 0) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  // paged: the row's sequence picks its block-table row; a row outside [0, num_seqs) is empty
+  int64_t seq = 0;
+  bool seq_ok = true;
+  if (PAGED) {
+    seq = __ldg(a.row_seq + r);
+    seq_ok = seq >= 0 && seq < a.num_seqs;
+    if (!seq_ok && tid == 0 && split == 0 && a.dev_status != nullptr) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+  }
+  const int my = (ntiles > warp && a.num_slots > 0 && seq_ok) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   const int32_t* idx_row = a.topk_idx + r * a.topk;
   if (a.num_slots == 0 && a.dev_status != nullptr) {  // no tiles run: still flag every non-padding entry
     for (int col = col0 + tid; col < col1; col += kThreads)
@@ -223,6 +233,29 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     }
     return v;
   };
+  // Paged pools: a position's block-table entry is loaded one tile before its slot is formed
+  // (positions themselves two tiles before), so neither dependent load stalls the warp.
+  const int32_t* tbl_row = PAGED ? a.block_table + seq * a.max_blocks : nullptr;
+  const int bsz = PAGED ? a.block_size : 1;
+  const int max_pos = PAGED ? a.max_blocks * a.block_size : 0;  // < 2^31, checked on the host
+  const bool bsz_pow2 = (bsz & (bsz - 1)) == 0;
+  const int bsz_shift = __ffs(bsz) - 1;
+  auto block_of = [&](int pos) -> int { return bsz_pow2 ? pos >> bsz_shift : pos / bsz; };
+  auto lookup = [&](int pos) -> int {  // the block id of position pos (-1: none loaded)
+    if (!PAGED || pos < 0 || pos >= max_pos) return -1;
+    return __ldg(tbl_row + block_of(pos));
+  };
+  // The slot of position pos in block blk; -1 for padding. Flags positions outside
+  // [-1, max_pos), unallocated blocks (id < 0) and slots past the pool.
+  auto checked_paged = [&](int pos, int blk) -> int {
+    if (pos == -1) return -1;
+    const int64_t slot = static_cast<int64_t>(blk) * bsz + (pos - block_of(pos) * bsz);
+    if (pos < -1 || pos >= max_pos || blk < 0 || slot >= a.num_slots) {
+      if (a.dev_status != nullptr) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+      return -1;
+    }
+    return static_cast<int>(slot);
+  };
 
   // Fixed per-lane parts of the copies of 256 B / 512 B rows. One copy instruction covers
   // four keys, one 128 B line of each (8 consecutive lanes on 8 consecutive 16 B chunks):
@@ -240,8 +273,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 
   // Copy one 16-key tile into ring stage i % kStages; returns the tile's valid-key mask.
   static_assert(F::kStages == 2, "the valid-key masks ride one tile ahead in registers");
-  auto issue = [&](int i, int raw_idx) -> uint32_t {
-    const int idxv = checked(raw_idx);
+  auto issue = [&](int i, int idxv) -> uint32_t {  // idxv: this lane's checked slot (or -1)
     const int st = i % F::kStages;
     const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
     uint8_t* sb = ring + size_t(st) * L::kStageBytes;
@@ -307,12 +339,21 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 
   // Start the first tiles' index loads and copies before staging the query, so their
   // latencies overlap the query's.
-  int nidx;
+  // index pipeline: nidx = tile i + 1's entry (slot id, or position when paged); paged also
+  // carries nblk = its block id and ppos = tile i + 2's position
+  int nidx, nblk = -1, ppos = -1;
   uint32_t mask_cur = 0;  // valid keys of the tile being computed (bit k = key k)
   {
     const int first = load_idx(0);
     nidx = load_idx(1);
-    if (0 < my) mask_cur = issue(0, first);
+    if (PAGED) {
+      ppos = load_idx(2);
+      const int fblk = lookup(first);
+      nblk = lookup(nidx);
+      if (0 < my) mask_cur = issue(0, checked_paged(first, fblk));
+    } else {
+      if (0 < my) mask_cur = issue(0, checked(first));
+    }
     cp_async_commit();
   }
 
@@ -403,9 +444,15 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
   int eu = -100;                           // int8: 2^eu > every V scale seen
   for (int i = 0; i < my; ++i) {
-    const uint32_t mask_next = (i + 1 < my) ? issue(i + 1, nidx) : 0u;
+    const uint32_t mask_next = (i + 1 < my) ? issue(i + 1, PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : 0u;
     cp_async_commit();
-    nidx = load_idx(i + F::kStages);
+    if (PAGED) {
+      nidx = ppos;
+      nblk = lookup(ppos);
+      ppos = load_idx(i + 3);
+    } else {
+      nidx = load_idx(i + F::kStages);
+    }
     cp_async_wait<F::kStages - 1>();
     const int st = i % F::kStages;
     __syncwarp();
@@ -872,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   if (warp == 0) tmem_dealloc(*sTmem, kTmemCols);
 }
 
-template <int FMT>
+template <int FMT, bool PAGED = false>
 cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
   constexpr size_t smem = Smem<FMT>::kTotal;
   static bool attr_done[64] = {};
@@ -881,13 +928,13 @@ cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(gather_attn_kernel<FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
   const int64_t grid = a.rows * a.num_kv_heads * a.num_splits;
-  gather_attn_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+  gather_attn_kernel<FMT, PAGED><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -52,12 +52,22 @@ struct GatherArgs {
   float* o_part;    // [rows, P, Hq, D] when num_splits > 1
   float* lse_part;  // [rows, P, Hq]
   uint32_t* dev_status;
+  // paged pools only (the paged launchers): topk_idx then holds logical positions
+  const int32_t* block_table = nullptr;  // [num_seqs, max_blocks]
+  const int32_t* row_seq = nullptr;      // [rows]
+  int64_t num_seqs = 0;
+  int max_blocks = 0;
+  int block_size = 0;
 };
 
 cudaError_t launch_gather_bf16(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_int8_side(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_int8_inline(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_e4m3(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_paged_bf16(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_paged_int8_side(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_paged_int8_inline(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_paged_e4m3(const GatherArgs& a, cudaStream_t stream);
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -139,3 +139,27 @@ def test_binding_rejects_buffers_that_disagree_with_q(lib):
     with pytest.raises(ValueError):
         lib.qsa_gather_attn_splitk_noalloc(q, lib.QKV_INT8_SIDE, kc, kc, idx_ok, 0.0625, num_splits=2,
                                            out=torch.zeros((2, 16, 256)))
+
+
+def _gather_paged(lib, **over):
+    a = dict(q=FAKE, rows=4, hq=16, hkv=1, d=256, fmt=lib.QKV_INT8_SIDE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE,
+             ksl=1.0, vsl=1.0, S=100, bt=FAKE, nseq=2, mb=8, bs=16, rs=FAKE, pos=FAKE, topk=8, sm=0.0625, P=1,
+             out=FAKE, lse=None, op=None, lp=None)
+    a.update(over)
+    return lib.lib.qsa_gather_attn_paged(a["q"], a["rows"], a["hq"], a["hkv"], a["d"], a["fmt"], a["kc"], a["vc"],
+                                         a["ks"], a["vs"], a["ksl"], a["vsl"], a["S"], a["bt"], a["nseq"], a["mb"],
+                                         a["bs"], a["rs"], a["pos"], a["topk"], a["sm"], a["P"], a["out"], a["lse"],
+                                         a["op"], a["lp"], None, None)
+
+
+def test_paged_gather_host_validation(lib):
+    E = lib
+    assert _gather_paged(lib, bs=0) == E.QKV_ERR_ARG
+    assert _gather_paged(lib, mb=0) == E.QKV_ERR_ARG
+    assert _gather_paged(lib, nseq=0) == E.QKV_ERR_ARG
+    assert _gather_paged(lib, mb=1 << 20, bs=1 << 12) == E.QKV_ERR_ARG  # positions would pass 2^31
+    assert _gather_paged(lib, bt=None) == E.QKV_ERR_ARG
+    assert _gather_paged(lib, rs=None) == E.QKV_ERR_ARG
+    assert _gather_paged(lib, rs=FAKE + 2) == E.QKV_ERR_ALIGN
+    assert _gather_paged(lib, d=128) == E.QKV_ERR_UNSUPPORTED  # the common checks still apply
+    assert _gather_paged(lib, rows=0) == E.QKV_OK
