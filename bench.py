@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=1, help="K-splits of each row (1 = unsplit)")
     ap.add_argument("--no-formats", action="store_true", help="skip the per-format side measurements")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the side measurements of the split-K, long-context and chunked-prefill workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample-rows", type=int, default=0, help="oracle rows per sample (0 = auto)")
     return ap.parse_args()
@@ -384,6 +386,9 @@ def main():
     if not args.no_formats and rank == 0:
         result["formats"] = measure_formats(q, wl, q_dev, idx, flush, stream, max(5, min(args.steps, 30)), peak)
 
+    if not args.no_workloads and rank == 0:
+        result["workloads"] = measure_workloads(q, flush, stream, max(5, min(args.steps, 20)), peak)
+
     if rank == 0 and not args.no_cpu_baseline:
         K, V = oracle_setup(wl)
         n = args.cpu_sample_rows or 64
@@ -458,6 +463,164 @@ def measure_formats(q, wl, q_dev, idx, flush, stream, steps, peak):
                     "rows_per_s": round(ROWS / (m * 1e-3), 1), "bytes_per_slot": SLOT_BYTES[fmt]}
         del kc, vc
         torch.cuda.empty_cache()
+    return res
+
+
+def _device_pool(q, wl, fmt):
+    """Write a workload's tokens into a device pool with the library's own write kernels."""
+    import numpy as np
+    import torch
+    S, H, D = wl.num_slots, wl.num_kv_heads, HEAD_DIM
+    bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    k_tok, v_tok = bf(wl.k_tokens), bf(wl.v_tokens)
+    slots = torch.from_numpy(wl.slot_mapping).cuda()
+    if fmt == "int8_side":
+        kc = torch.zeros((S, H, D), dtype=torch.int8, device="cuda")
+        vc = torch.zeros_like(kc)
+        ks = torch.zeros((S, H), dtype=torch.float32, device="cuda")
+        vs = torch.zeros_like(ks)
+        q.qkv_write_int8(k_tok, v_tok, slots, kc, vc, ks, vs)
+        return kc, vc, dict(k_scale_tok=ks, v_scale_tok=vs), 1.0
+    amax = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sc = torch.zeros(2, dtype=torch.float32, device="cuda")
+    q.qkv_e4m3_calibrate(k_tok, amax, sc[0:1])
+    q.qkv_e4m3_calibrate(v_tok, amax, sc[1:2])
+    ksl, vsl = sc.tolist()
+    kc = torch.zeros((S, H, D), dtype=torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    q.qkv_write_e4m3(k_tok, v_tok, slots, kc, vc, ksl, vsl)
+    return kc, vc, dict(k_scale_layer=ksl, v_scale_layer=vsl), vsl
+
+
+def _time_events(fn, flush, stream, reps):
+    """Mean device time of fn() in ms (CUDA events on `stream`), L2 flushed before every rep."""
+    import torch
+    for _ in range(3):
+        fn()
+    ms = []
+    for i in range(reps):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return sum(ms) / len(ms)
+
+
+def measure_workloads(q, flush, stream, reps, peak):
+    """The pages' other workload shapes, gather path only (context; the metric is the page-1 shape).
+
+    split-K workloads: the split gather followed by qsa_splitk_merge (two launches) against
+    qsa_gather_attn_splitk_fused (one launch); chunked prefill: the 8192-token writes and the
+    8192-row causal gather, whose 4.3 MB of distinct slots stay in L2.
+    """
+    import numpy as np
+    import torch
+    from gen import E4M3_SPLITK_LAYERS, chunked_prefill, e4m3_splitk_layer, long_context_decode
+    res = {}
+
+    def split_variants(wl, fmt, kc, vc, kw, vpost):
+        R, Hq, D, P = wl.rows, wl.num_q_heads, HEAD_DIM, wl.num_splits
+        qd = torch.from_numpy(np.ascontiguousarray(wl.q).view(np.int16)).view(torch.bfloat16).cuda()
+        idx = torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
+        out = torch.empty((R, Hq, D), dtype=torch.float32, device="cuda")
+        o_part = torch.empty((R, P, Hq, D), dtype=torch.float32, device="cuda")
+        lse_part = torch.empty((R, P, Hq), dtype=torch.float32, device="cuda")
+        counters = torch.zeros((R, wl.num_kv_heads), dtype=torch.int32, device="cuda")
+        code = q.FORMATS[fmt]
+
+        def two():
+            q.qsa_gather_attn(qd, code, kc, vc, idx, wl.softmax_scale, num_splits=P, o_part=o_part,
+                              lse_part=lse_part, **kw)
+            q.qsa_splitk_merge(o_part, lse_part, out, v_scale_post=vpost)
+
+        def fused():
+            q.qsa_gather_attn_splitk_fused(qd, code, kc, vc, idx, wl.softmax_scale, num_splits=P, out=out,
+                                           o_part=o_part, lse_part=lse_part, counters=counters, **kw)
+
+        def unsplit():
+            q.qsa_gather_attn(qd, code, kc, vc, idx, wl.softmax_scale, out=out, **kw)
+
+        t = {"split_plus_merge_ms": _time_events(two, flush, stream, reps),
+             "fused_ms": _time_events(fused, flush, stream, reps),
+             "unsplit_ms": _time_events(unsplit, flush, stream, reps)}
+        return t, (qd, idx, out)
+
+    # calibrated E4M3 split-K: 12 layers, each its own 131072-slot pool
+    per_layer = []
+    for layer in range(E4M3_SPLITK_LAYERS):
+        wl = e4m3_splitk_layer(layer)
+        kc, vc, kw, vpost = _device_pool(q, wl, "e4m3")
+        t, _ = split_variants(wl, "e4m3", kc, vc, kw, vpost)
+        per_layer.append(t)
+        del kc, vc
+    tot = {k: sum(t[k] for t in per_layer) for k in per_layer[0]}
+    bytes_layer = 64 * 2051 * SLOT_BYTES["e4m3"]
+    res["e4m3_splitk_12_layers"] = {
+        "shape": "12 layers x (64 rows, top-k 2051, 8 splits) over 131072-slot E4M3 pools, 16 query heads",
+        "sum_ms": {k: round(v, 5) for k, v in tot.items()},
+        "per_layer_ms": {k: [round(t[k], 5) for t in per_layer] for k in per_layer[0]},
+        "fused_gathered_GBps": round(E4M3_SPLITK_LAYERS * bytes_layer / (tot["fused_ms"] * 1e-3) / 1e9, 2),
+        "note": "each layer timed alone after an L2 flush"}
+
+    # long-context decode: 8 x 131072 tokens, 40 rows x top-k 2048, 16 splits; also the paged kernel
+    wl = long_context_decode(3)
+    kc, vc, kw, vpost = _device_pool(q, wl, "int8_side")
+    t, (qd, idx, out) = split_variants(wl, "int8_side", kc, vc, kw, vpost)
+    table = torch.from_numpy(np.ascontiguousarray(wl.block_table, dtype=np.int32)).cuda()
+    rs = torch.from_numpy(np.ascontiguousarray(wl.row_seq, dtype=np.int32)).cuda()
+    pos = torch.from_numpy(np.ascontiguousarray(wl.topk_pos, dtype=np.int32)).cuda()
+    P = wl.num_splits
+    o_part = torch.empty((wl.rows, P, wl.num_q_heads, HEAD_DIM), dtype=torch.float32, device="cuda")
+    lse_part = torch.empty((wl.rows, P, wl.num_q_heads), dtype=torch.float32, device="cuda")
+
+    def paged():
+        q.qsa_gather_attn_paged(qd, q.QKV_INT8_SIDE, kc, vc, table, rs, pos, wl.block_size, wl.softmax_scale,
+                                num_splits=P, o_part=o_part, lse_part=lse_part, **kw)
+        q.qsa_splitk_merge(o_part, lse_part, out)
+
+    t["paged_split_plus_merge_ms"] = _time_events(paged, flush, stream, reps)
+    bytes_lc = wl.rows * wl.topk.shape[1] * SLOT_BYTES["int8_side"]
+    res["long_context_decode"] = {
+        "shape": "8 seq x 131072 tokens (paged, blocks of 16), 40 rows x top-k 2048, 16 splits, int8 side",
+        **{k: round(v, 5) for k, v in t.items()},
+        "fused_gathered_GBps": round(bytes_lc / (t["fused_ms"] * 1e-3) / 1e9, 2),
+        "note": "42.6 MB gathered per step: launch latency and the wave tail dominate"}
+    del kc, vc
+    torch.cuda.empty_cache()
+
+    # chunked prefill: 8192 new tokens written, then 8192 causal rows of up to 1024 entries
+    wl = chunked_prefill(4)
+    bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+    k_tok, v_tok = bf(wl.k_tokens), bf(wl.v_tokens)
+    slots = torch.from_numpy(wl.slot_mapping).cuda()
+    S, D = wl.num_slots, HEAD_DIM
+    kc = torch.zeros((S, 1, D), dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((S, 1), dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    ec = torch.zeros((S, 1, D), dtype=torch.uint8, device="cuda")
+    evc = torch.zeros_like(ec)
+    w8 = _time_events(lambda: q.qkv_write_int8(k_tok, v_tok, slots, kc, vc, ks, vs), flush, stream, reps)
+    we = _time_events(lambda: q.qkv_write_e4m3(k_tok, v_tok, slots, ec, evc, 0.01, 0.01), flush, stream, reps)
+    qd = bf(wl.q)
+    idx = torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
+    out = torch.empty((wl.rows, wl.num_q_heads, D), dtype=torch.float32, device="cuda")
+    g = _time_events(lambda: q.qsa_gather_attn(qd, q.QKV_INT8_SIDE, kc, vc, idx, wl.softmax_scale, out=out,
+                                               k_scale_tok=ks, v_scale_tok=vs), flush, stream, reps)
+    visits = int((wl.topk >= 0).sum())
+    res["chunked_prefill"] = {
+        "shape": "8192 new tokens into a 524288-slot pool; 8192 rows, row i attends min(1024, i) earlier tokens",
+        "write_int8_ms": round(w8, 5), "write_e4m3_ms": round(we, 5),
+        "write_int8_GBps": round(8192 * (1024 + 520) / (w8 * 1e-3) / 1e9, 2),
+        "gather_int8_side_ms": round(g, 5), "slot_visits": visits,
+        "gather_GBps": round(visits * SLOT_BYTES["int8_side"] / (g * 1e-3) / 1e9, 2),
+        "note": "the 8192 written slots (4.3 MB) stay in L2: gathered GB/s is bounded by L2, not HBM "
+                f"(measured HBM peak {peak} GB/s)"}
+    del kc, vc, ec, evc
+    torch.cuda.empty_cache()
     return res
 
 

@@ -161,6 +161,38 @@ qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t 
                             float* out, float* lse, void* stream);
 
 /*
+ * qsa_gather_attn_splitk_fused -- qsa_gather_attn with num_splits > 1 and the split-K merge
+ * fused into the same launch.     [E4M3-PR §Implementation scope: split-K workspace and merge;
+ *                                  HOIST-PR §Changes: the V scale is applied after the merge]
+ *   Every split CTA of a (row, KV head) writes its partial to o_part / lse_part exactly as
+ *   qsa_gather_attn does, then increments counters[row * num_kv_heads + kv_head]. The CTA
+ *   that brings the counter to num_splits merges the num_splits partials of that (row, KV
+ *   head) into out / lse (E4M3: times v_scale_layer) and resets the counter to 0. No CTA
+ *   waits for another. The result is bit-identical to qsa_gather_attn followed by
+ *   qsa_splitk_merge on the same partials; it saves the second launch and its gap.
+ *
+ *   Arguments as qsa_gather_attn, plus:
+ *   out        fp32 [rows, num_q_heads, head_dim] (16 B-aligned) and lse fp32
+ *              [rows, num_q_heads] or NULL: the merged result.
+ *   o_part, lse_part  the split workspace, laid out as for qsa_gather_attn; left holding the
+ *              partials.
+ *   counters   uint32 [rows, num_kv_heads], 4 B-aligned, owned by the caller. They must all
+ *              be 0 before the first call; every call leaves them 0 again.
+ *   num_splits == 1 runs the unsplit kernel (o_part, lse_part and counters are not touched and
+ *   may be NULL). num_splits > 1 with counters NULL is QKV_ERR_ARG.
+ *   Calls that overlap on the GPU must not share counters or workspace.
+ */
+qkv_status qsa_gather_attn_splitk_fused(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                                        int head_dim, qkv_format fmt, const void* k_cache,
+                                        const void* v_cache, const float* k_scale_tok,
+                                        const float* v_scale_tok, float k_scale_layer,
+                                        float v_scale_layer, int64_t num_slots,
+                                        const int32_t* topk_idx, int topk, float softmax_scale,
+                                        int num_splits, float* out, float* lse, float* o_part,
+                                        float* lse_part, uint32_t* counters, uint32_t* dev_status,
+                                        void* stream);
+
+/*
  * qsa_gather_attn_splitk_noalloc -- qsa_gather_attn with num_splits > 1 followed by
  * qsa_splitk_merge, for callers that cannot allocate device memory. The pages have no
  * counterpart: this is a packaging of the two calls above, not a step of the method.

@@ -40,6 +40,8 @@ _SIGS = {
     "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
     "qsa_gather_attn_splitk_noalloc": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p,
                                        _i32, _f32, _i32, _p, _p, _p, _p],
+    "qsa_gather_attn_splitk_fused": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32,
+                                     _f32, _i32, _p, _p, _p, _p, _p, _p, _p],
     "qsa_gather_attn_paged": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i64, _i32,
                               _i32, _p, _p, _i32, _f32, _i32, _p, _p, _p, _p, _p, _p],
 }
@@ -167,6 +169,29 @@ def qsa_gather_attn_paged(q, fmt: int, k_cache, v_cache, block_table, row_seq, t
                                    float(softmax_scale), num_splits, _ptr(out), _ptr(lse), _ptr(o_part),
                                    _ptr(lse_part), _ptr(dev_status), _stream(stream))
     _check("qsa_gather_attn_paged", st)
+
+
+def qsa_gather_attn_splitk_fused(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: float, *, num_splits: int,
+                                 out, o_part, lse_part, counters, lse=None, num_kv_heads: int = 1,
+                                 num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
+                                 k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, dev_status=None,
+                                 stream=None):
+    """Split-K gather with the merge fused into the same launch (the last split CTA merges).
+
+    counters: int32/uint32 [R, num_kv_heads], all zero before the first call and left zero.
+    """
+    _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
+    R, Hq, D = q.shape
+    if counters is not None and counters.numel() != R * num_kv_heads:
+        raise ValueError(f"counters must hold {R} x {num_kv_heads} entries, got {counters.numel()}")
+    S = k_cache.shape[0] if num_slots is None else num_slots
+    topk = topk_idx.shape[1] if topk_idx is not None else 0
+    st = lib.qsa_gather_attn_splitk_fused(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer),
+                                          float(v_scale_layer), S, _ptr(topk_idx), topk, float(softmax_scale),
+                                          num_splits, _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part),
+                                          _ptr(counters), _ptr(dev_status), _stream(stream))
+    _check("qsa_gather_attn_splitk_fused", st)
 
 
 def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1.0, stream=None):

@@ -105,7 +105,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
                        const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
                        const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
                        float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream,
-                       const Paging* pg) {
+                       const Paging* pg, uint32_t* counters = nullptr) {
   if (rows < 0 || topk < 0 || num_splits < 1 || num_slots < 0) return QKV_ERR_ARG;
   if (pg != nullptr) {
     if (pg->num_seqs < 1 || pg->max_blocks < 1 || pg->block_size < 1) return QKV_ERR_ARG;
@@ -121,7 +121,10 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   const bool side = fmt == QKV_INT8_SIDE;
   if (side != (k_scale_tok != nullptr) || side != (v_scale_tok != nullptr)) return QKV_ERR_ARG;
   if (num_splits == 1) {
-    if (!out || o_part || lse_part) return QKV_ERR_ARG;
+    if (!out || o_part || lse_part || counters) return QKV_ERR_ARG;
+  } else if (counters != nullptr) {  // fused merge: partials and the merged output
+    if (!out || !o_part || !lse_part) return QKV_ERR_ARG;
+    if (!aligned(counters, 4)) return QKV_ERR_ALIGN;
   } else {
     if (out || lse || !o_part || !lse_part) return QKV_ERR_ARG;
   }
@@ -163,6 +166,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   a.o_part = o_part;
   a.lse_part = lse_part;
   a.dev_status = dev_status;
+  a.counters = num_splits > 1 ? counters : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pg != nullptr) {
     a.block_table = pg->block_table;
@@ -213,6 +217,23 @@ qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, i
   return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
                      k_scale_layer, v_scale_layer, num_slots, topk_pos, topk, softmax_scale, num_splits, out, lse,
                      o_part, lse_part, dev_status, stream, &pg);
+}
+
+qkv_status qsa_gather_attn_splitk_fused(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                                        int head_dim, qkv_format fmt, const void* k_cache, const void* v_cache,
+                                        const float* k_scale_tok, const float* v_scale_tok, float k_scale_layer,
+                                        float v_scale_layer, int64_t num_slots, const int32_t* topk_idx, int topk,
+                                        float softmax_scale, int num_splits, float* out, float* lse,
+                                        float* o_part, float* lse_part, uint32_t* counters, uint32_t* dev_status,
+                                        void* stream) {
+  if (num_splits == 1)  // unsplit: the kernel writes out / lse itself; no workspace is touched
+    return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok,
+                       v_scale_tok, k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, 1, out,
+                       lse, nullptr, nullptr, dev_status, stream, nullptr);
+  if (num_splits > 1 && counters == nullptr) return QKV_ERR_ARG;
+  return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
+                     k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, num_splits, out, lse,
+                     o_part, lse_part, dev_status, stream, nullptr, counters);
 }
 
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows, int num_q_heads,

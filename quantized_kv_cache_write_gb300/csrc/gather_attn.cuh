@@ -912,6 +912,31 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     }
     __syncthreads();  // the merge buffer is rewritten by the next half
   }
+
+  // ---------------- fused split-K merge: the split CTA of this (row, KV head) that finishes
+  // last merges all P partials into out / lse. No CTA waits for another: the others just leave.
+  if (P > 1 && a.counters != nullptr) {
+    uint32_t* sLast = reinterpret_cast<uint32_t*>(smem + L::kPost);  // the weights above are formed
+    __threadfence();  // this CTA's partial is visible device-wide before it is announced
+    __syncthreads();
+    if (tid == 0) sLast[0] = (atomicAdd(a.counters + rh, 1u) == static_cast<uint32_t>(P - 1)) ? 1u : 0u;
+    __syncthreads();
+    if (sLast[0] != 0u) {
+      __threadfence();  // order the reads of the other CTAs' partials after their announcements
+      if (hh < G) {
+        // thread (hh, part) merges head hh's float4 columns part + 8 i: 8 threads of a head
+        // read one contiguous 128 B line per load
+        int col4[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) col4[i] = part + 8 * i;
+        const int64_t qhead = static_cast<int64_t>(h) * G + hh;
+        merge_head<8>(a.o_part + (r * P * Hq + qhead) * kHeadDim, a.lse_part + r * P * Hq + qhead, Hq, P,
+                      F::kE4m3 ? a.v_scale_layer : 1.f, col4, a.out + (r * Hq + qhead) * kHeadDim,
+                      (a.lse != nullptr && part == 0) ? a.lse + r * Hq + qhead : nullptr);
+      }
+      if (tid == 0) a.counters[rh] = 0u;  // every split has arrived: ready for the next call
+    }
+  }
   // every warp's TMEM accesses are complete (the loads above were waited for): free the columns
   tmem_fence_before_sync();
   __syncthreads();

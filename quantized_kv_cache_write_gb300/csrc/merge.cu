@@ -23,36 +23,10 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int64_t r = item / num_q_heads;
   const int g = static_cast<int>(item - r * num_q_heads);
 
-  const float* lp = lse_part + r * num_splits * num_q_heads + g;
-  float m = -INFINITY;
-  for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lp[static_cast<int64_t>(s) * num_q_heads]);
-
-  float acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  float* dst = out + item * kHeadDim + lane * 8;
-  if (m == -INFINITY) {
-    reinterpret_cast<float4*>(dst)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    reinterpret_cast<float4*>(dst)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (lse != nullptr && lane == 0) lse[item] = -INFINITY;
-    return;
-  }
-  float wsum = 0.f;
-  for (int s = 0; s < num_splits; ++s) {
-    const float ls = lp[static_cast<int64_t>(s) * num_q_heads];
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - m);
-    wsum += w;
-    const float4* src =
-        reinterpret_cast<const float4*>(o_part + ((r * num_splits + s) * num_q_heads + g) * kHeadDim + lane * 8);
-    const float4 a = src[0], b = src[1];
-    acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-    acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
-  }
-  const float f = v_scale_post / wsum;
-  reinterpret_cast<float4*>(dst)[0] = make_float4(acc[0] * f, acc[1] * f, acc[2] * f, acc[3] * f);
-  reinterpret_cast<float4*>(dst)[1] = make_float4(acc[4] * f, acc[5] * f, acc[6] * f, acc[7] * f);
-  if (lse != nullptr && lane == 0) lse[item] = m + logf(wsum);
+  const int col4[2] = {2 * lane, 2 * lane + 1};  // lane owns columns 8 lane .. 8 lane + 7
+  merge_head<2>(o_part + (r * num_splits * num_q_heads + g) * kHeadDim, lse_part + r * num_splits * num_q_heads + g,
+                num_q_heads, num_splits, v_scale_post, col4, out + item * kHeadDim,
+                (lse != nullptr && lane == 0) ? lse + item : nullptr);
 }
 
 }  // namespace

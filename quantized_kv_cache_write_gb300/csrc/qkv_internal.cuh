@@ -52,6 +52,9 @@ struct GatherArgs {
   float* o_part;    // [rows, P, Hq, D] when num_splits > 1
   float* lse_part;  // [rows, P, Hq]
   uint32_t* dev_status;
+  // fused split-K merge (num_splits > 1 only): arrival counters [rows, Hkv], zero on entry and
+  // left zero; the last split CTA of a (row, KV head) merges into out / lse. Null = no merge.
+  uint32_t* counters = nullptr;
   // paged pools only (the paged launchers): topk_idx then holds logical positions
   const int32_t* block_table = nullptr;  // [num_seqs, max_blocks]
   const int32_t* row_seq = nullptr;      // [rows]
@@ -231,6 +234,53 @@ __device__ __forceinline__ void f2scale(float* v, uint64_t s) {
   f2unpack(f2mul(f2pack(v[0], v[1]), s), a, b);
   v[0] = a;
   v[1] = b;
+}
+
+// Split-K merge of one (row, query head) over the NV float4 column groups col4[0..NV):
+//   lse = log sum_s exp(lse_s),  o = v_scale_post * sum_s exp(lse_s - lse) o_s,
+// with empty splits (lse_s = -inf) skipped and an all-empty row giving o = 0, lse = -inf.
+// o_head = o_part at (row, split 0, head): splits are Hq * kHeadDim floats apart; lp = lse_part
+// at (row, split 0, head): splits are Hq floats apart. Partials are read through L2
+// (ld.global.cg) because in the fused gather other CTAs of the same launch wrote them. Every
+// caller runs this same arithmetic, so a column's result does not depend on which thread or
+// kernel merges it.
+template <int NV>
+__device__ __forceinline__ void merge_head(const float* o_head, const float* lp, int Hq, int P, float v_scale_post,
+                                           const int (&col4)[NV], float* out_head, float* lse_out) {
+  float m = -INFINITY;
+  for (int s = 0; s < P; ++s) m = fmaxf(m, __ldcg(lp + static_cast<int64_t>(s) * Hq));
+  float4* dst = reinterpret_cast<float4*>(out_head);
+  if (m == -INFINITY) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) dst[col4[v]] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lse_out != nullptr) *lse_out = -INFINITY;
+    return;
+  }
+  float acc[4 * NV];
+#pragma unroll
+  for (int i = 0; i < 4 * NV; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  const int64_t sstride = static_cast<int64_t>(Hq) * kHeadDim;
+  for (int s = 0; s < P; ++s) {
+    const float ls = __ldcg(lp + static_cast<int64_t>(s) * Hq);
+    if (ls == -INFINITY) continue;
+    const float w = expf(ls - m);
+    wsum += w;
+    const float4* src = reinterpret_cast<const float4*>(o_head + s * sstride);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+      const float4 x = __ldcg(src + col4[v]);
+      acc[4 * v] += w * x.x;
+      acc[4 * v + 1] += w * x.y;
+      acc[4 * v + 2] += w * x.z;
+      acc[4 * v + 3] += w * x.w;
+    }
+  }
+  const float f = v_scale_post / wsum;
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+    dst[col4[v]] = make_float4(acc[4 * v] * f, acc[4 * v + 1] * f, acc[4 * v + 2] * f, acc[4 * v + 3] * f);
+  if (lse_out != nullptr) *lse_out = m + logf(wsum);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

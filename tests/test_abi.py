@@ -163,3 +163,30 @@ def test_paged_gather_host_validation(lib):
     assert _gather_paged(lib, rs=FAKE + 2) == E.QKV_ERR_ALIGN
     assert _gather_paged(lib, d=128) == E.QKV_ERR_UNSUPPORTED  # the common checks still apply
     assert _gather_paged(lib, rows=0) == E.QKV_OK
+
+
+def _gather_fused(lib, **over):
+    a = dict(q=FAKE, rows=4, hq=16, hkv=1, d=256, fmt=lib.QKV_INT8_SIDE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE,
+             ksl=1.0, vsl=1.0, S=100, idx=FAKE, topk=8, sm=0.0625, P=4, out=FAKE, lse=None, op=FAKE, lp=FAKE,
+             cnt=FAKE)
+    a.update(over)
+    return lib.lib.qsa_gather_attn_splitk_fused(a["q"], a["rows"], a["hq"], a["hkv"], a["d"], a["fmt"], a["kc"],
+                                                a["vc"], a["ks"], a["vs"], a["ksl"], a["vsl"], a["S"], a["idx"],
+                                                a["topk"], a["sm"], a["P"], a["out"], a["lse"], a["op"], a["lp"],
+                                                a["cnt"], None, None)
+
+
+def test_fused_gather_host_validation(lib):
+    E = lib
+    assert _gather_fused(lib, cnt=None) == E.QKV_ERR_ARG  # a split call needs the arrival counters
+    assert _gather_fused(lib, cnt=FAKE + 2) == E.QKV_ERR_ALIGN
+    assert _gather_fused(lib, out=None) == E.QKV_ERR_ARG  # ... the merged output
+    assert _gather_fused(lib, op=None) == E.QKV_ERR_ARG  # ... and the partial workspace
+    assert _gather_fused(lib, lp=None) == E.QKV_ERR_ARG
+    assert _gather_fused(lib, out=FAKE + 4) == E.QKV_ERR_ALIGN
+    assert _gather_fused(lib, P=0) == E.QKV_ERR_ARG
+    assert _gather_fused(lib, d=128) == E.QKV_ERR_UNSUPPORTED
+    assert _gather_fused(lib, fmt=E.QKV_E4M3, ks=None, vs=None, ksl=0.0) == E.QKV_ERR_SCALE
+    assert _gather_fused(lib, rows=0) == E.QKV_OK
+    # unsplit: workspace and counters are neither needed nor allowed to be required
+    assert _gather_fused(lib, P=1, op=None, lp=None, cnt=None, rows=0) == E.QKV_OK
