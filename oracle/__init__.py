@@ -13,6 +13,9 @@ It is written to be read against the pages, not to be fast:
 * attention.py fp64 dequantisation of a slot pool, top-k gather attention with a
                max-subtracted softmax, the split-K partition and the log-sum-exp merge.
 * paging.py    logical positions of a paged pool -> slot ids through a block table.
+* calibration.py  per-tensor calibration statistics: max-abs, nearest-rank p99.9 / p99.99 of
+               |x|, the calibrated scale amax/448, and the counts of scaled magnitudes below
+               E4M3's smallest subnormal, in its subnormal range, and clipped by saturation.
 
 Pages cited (by title):
   [INT8-PR]  "int8 per-(token,head) KV cache for the Qwen3.8-Flash-Next QSA path"
@@ -25,4 +28,4 @@ Every function is pinned by a test under tests/ that does not re-derive it (clos
 library routines on special cases, brute force, invariants, hand-worked fixtures).
 """
 
-from . import attention, paging, quant  # noqa: F401
+from . import attention, calibration, paging, quant  # noqa: F401
