@@ -621,6 +621,21 @@ def measure_workloads(q, flush, stream, reps, peak):
                 f"(measured HBM peak {peak} GB/s)"}
     del kc, vc, ec, evc
     torch.cuda.empty_cache()
+
+    # calibration statistics of one layer's K tensor (the E4M3 split-K layer 0 pool, 67 MB of
+    # bf16): the histogram pass is HBM-bound at 2 B per element; the stats pass reads 256 KB
+    wl = e4m3_splitk_layer(0)
+    x = bf(wl.k_tokens)
+    hist = torch.zeros(q.CALIB_BINS, dtype=torch.int64, device="cuda")
+    rec = torch.zeros(8, dtype=torch.int64, device="cuda")
+    h_ms = _time_events(lambda: q.qkv_calib_histogram(x, hist), flush, stream, reps)
+    s_ms = _time_events(lambda: q.qkv_calib_stats(hist, rec), flush, stream, reps)
+    res["calibration"] = {
+        "shape": f"one layer's K: {x.numel()} bf16 values (131072 slots x 256)",
+        "histogram_ms": round(h_ms, 5), "stats_ms": round(s_ms, 5),
+        "histogram_GBps": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9, 2),
+        "histogram_frac_of_hbm_peak": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9 / peak, 4)}
+    del x
     return res
 
 

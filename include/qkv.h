@@ -109,6 +109,54 @@ qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, flo
                               void* stream);
 
 /*
+ * Calibration statistics of one K or V tensor (one layer's K, say), computed on the device.
+ *                       [SCALES §Calibration: scale = max envelope / 448, and max-abs,
+ *                        p99.9, p99.99 and saturation per tensor; E4M3-PR §Why calibrated
+ *                        scale is part of this contract: nonzero elements below E4M3's
+ *                        smallest subnormal 2^-9 and in the subnormal band below 2^-6]
+ *
+ * qkv_calib_histogram adds the counts of the bf16 magnitudes (bits & 0x7FFF) of x to hist.
+ * Calls accumulate, so one histogram can cover a tensor seen over many steps; zero hist
+ * before the first call. A bf16 magnitude has 15 bits, so the histogram is exact.
+ *   x      bf16 [n], 16 B-aligned (n may be 0; n <= 2^40).
+ *   hist   uint64 [QKV_CALIB_BINS], 8 B-aligned, owned by the caller.
+ *
+ * qkv_calib_stats reads a histogram and writes one qkv_calib_summary record (device memory):
+ *   count            finite elements; zeros: elements equal to +-0; nonfinite: inf / NaN
+ *                    elements (they take part in nothing else)
+ *   amax             max |x| over the finite elements
+ *   p99_9, p99_99    nearest-rank percentiles of |x| over the finite elements: with the
+ *                    magnitudes sorted ascending, element ceil(q count), q = 999/1000 and
+ *                    9999/10000 as exact fractions (0 when count is 0)
+ *   scale            the scale the counts below refer to: `scale` when it is > 0, or, when
+ *                    `scale` is 0, the calibrated amax / 448 (fp32 IEEE division)
+ *   With y = |x| / scale (fp32 IEEE division) for each finite element:
+ *   below_subnormal  nonzero elements with y < 2^-9
+ *   subnormal        elements with 2^-9 <= y < 2^-6
+ *   saturated        elements with y > 464: the ones the saturating encoder clips, whose
+ *                    nearest value on the E4M3 grid continued past 448 would be above 448
+ *                    (so at the calibrated scale it is always 0)
+ *   A scale of 0 (an all-zero tensor) leaves those three counts at 0.
+ *   scale  0 or finite and > 0, else QKV_ERR_SCALE.
+ */
+#define QKV_CALIB_BINS 32768
+typedef struct {
+  uint64_t count;
+  uint64_t zeros;
+  uint64_t nonfinite;
+  uint64_t below_subnormal;
+  uint64_t subnormal;
+  uint64_t saturated;
+  float amax;
+  float p99_9;
+  float p99_99;
+  float scale;
+} qkv_calib_summary;
+
+qkv_status qkv_calib_histogram(const void* x, int64_t n, uint64_t* hist, void* stream);
+qkv_status qkv_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream);
+
+/*
  * qsa_gather_attn -- top-k gather decode attention over a quantized slot pool.
  *                       [INT8-PR §The finding worth upstreaming; HOIST-PR §Changes]
  *   For row r, query head g (KV head g / G, G = num_q_heads / num_kv_heads) and the valid

@@ -35,6 +35,8 @@ _SIGS = {
     "qkv_write_int8": [_p, _p, _i64, _i32, _i32, _i64, _p, _i32, _p, _p, _p, _p, _i64, _p, _p],
     "qkv_write_e4m3": [_p, _p, _i64, _i32, _i32, _i64, _p, _p, _p, _f32, _f32, _i64, _p, _p],
     "qkv_e4m3_calibrate": [_p, _i64, _p, _p, _p],
+    "qkv_calib_histogram": [_p, _i64, _p, _p],
+    "qkv_calib_stats": [_p, _f32, _p, _p],
     "qsa_gather_attn": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
                         _i32, _p, _p, _p, _p, _p, _p],
     "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
@@ -112,6 +114,41 @@ def qkv_e4m3_calibrate(x, amax_bits, scale_out, *, stream=None):
     """Device amax/448 over a bf16 tensor; result in scale_out[0] (fp32)."""
     st = lib.qkv_e4m3_calibrate(_ptr(x), x.numel(), _ptr(amax_bits), _ptr(scale_out), _stream(stream))
     _check("qkv_e4m3_calibrate", st)
+
+
+CALIB_BINS = 32768  # QKV_CALIB_BINS in include/qkv.h
+CALIB_STATS_BYTES = 64  # sizeof(qkv_calib_summary): six uint64 counts, then four fp32 values
+_CALIB_COUNTS = ("count", "zeros", "nonfinite", "below_subnormal", "subnormal", "saturated")
+_CALIB_VALUES = ("amax", "p99_9", "p99_99", "scale")
+
+
+def qkv_calib_histogram(x, hist, *, stream=None):
+    """Add the bf16 magnitude counts of x (any shape, contiguous) to hist (int64 [32768], device)."""
+    if x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 tensor")
+    if hist.numel() != CALIB_BINS or hist.element_size() != 8:
+        raise ValueError(f"hist must hold {CALIB_BINS} 64-bit counts")
+    st = lib.qkv_calib_histogram(_ptr(x), x.numel(), _ptr(hist), _stream(stream))
+    _check("qkv_calib_histogram", st)
+
+
+def qkv_calib_stats(hist, stats, scale: float = 0.0, *, stream=None):
+    """Statistics of a histogram into stats (a 64-byte device buffer, e.g. int64 [8]).
+
+    scale 0 uses the calibrated amax / 448; read the record with decode_calib_stats.
+    """
+    if stats.numel() * stats.element_size() < CALIB_STATS_BYTES:
+        raise ValueError(f"stats must hold {CALIB_STATS_BYTES} bytes")
+    st = lib.qkv_calib_stats(_ptr(hist), float(scale), _ptr(stats), _stream(stream))
+    _check("qkv_calib_stats", st)
+
+
+def decode_calib_stats(stats) -> dict:
+    """The qkv_calib_summary record in a device or host buffer, as a dict (copies to the host)."""
+    raw = stats.detach().contiguous().view(torch.uint8)[:CALIB_STATS_BYTES].cpu()
+    counts = raw[:48].view(torch.int64).tolist()
+    values = raw[48:64].view(torch.float32).tolist()
+    return {**dict(zip(_CALIB_COUNTS, counts)), **dict(zip(_CALIB_VALUES, values))}
 
 
 def _expect_shape(name: str, t, shape):

@@ -26,6 +26,7 @@ SOURCES = [
     "api.cu",
     "write.cu",
     "merge.cu",
+    "calib.cu",
     "gather_int8_side.cu",
     "gather_int8_inline.cu",
     "gather_e4m3.cu",

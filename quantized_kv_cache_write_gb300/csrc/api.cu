@@ -87,6 +87,20 @@ qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, flo
   return cuda_status(qkv::launch_e4m3_calibrate(x, n, amax_bits, scale_out, static_cast<cudaStream_t>(stream)));
 }
 
+qkv_status qkv_calib_histogram(const void* x, int64_t n, uint64_t* hist, void* stream) {
+  if (n < 0 || n > (int64_t(1) << 40) || !hist || (n > 0 && !x)) return QKV_ERR_ARG;
+  if ((n > 0 && !aligned(x, 16)) || !aligned(hist, 8)) return QKV_ERR_ALIGN;
+  if (n == 0) return QKV_OK;
+  return cuda_status(qkv::launch_calib_histogram(x, n, hist, static_cast<cudaStream_t>(stream)));
+}
+
+qkv_status qkv_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream) {
+  if (!hist || !stats) return QKV_ERR_ARG;
+  if (!(scale == 0.f || finite_positive(scale))) return QKV_ERR_SCALE;
+  if (!aligned(hist, 8) || !aligned(stats, 8)) return QKV_ERR_ALIGN;
+  return cuda_status(qkv::launch_calib_stats(hist, scale, stats, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 namespace {

@@ -26,6 +26,8 @@ cudaError_t launch_write_e4m3(const void* k, const void* v, int64_t num_tokens, 
                               uint32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out,
                                   cudaStream_t stream);
+cudaError_t launch_calib_histogram(const void* x, int64_t n, uint64_t* hist, cudaStream_t stream);
+cudaError_t launch_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, cudaStream_t stream);
 cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
                                 int num_q_heads, int num_splits, float v_scale_post, float* out,
                                 float* lse, cudaStream_t stream);

@@ -190,3 +190,17 @@ def test_fused_gather_host_validation(lib):
     assert _gather_fused(lib, rows=0) == E.QKV_OK
     # unsplit: workspace and counters are neither needed nor allowed to be required
     assert _gather_fused(lib, P=1, op=None, lp=None, cnt=None, rows=0) == E.QKV_OK
+
+
+def test_calibration_host_validation(lib):
+    E, L = lib, lib.lib
+    assert L.qkv_calib_histogram(FAKE, -1, FAKE, None) == E.QKV_ERR_ARG
+    assert L.qkv_calib_histogram(FAKE, 1 << 41, FAKE, None) == E.QKV_ERR_ARG
+    assert L.qkv_calib_histogram(FAKE, 10, None, None) == E.QKV_ERR_ARG
+    assert L.qkv_calib_histogram(FAKE + 2, 10, FAKE, None) == E.QKV_ERR_ALIGN
+    assert L.qkv_calib_histogram(FAKE, 10, FAKE + 4, None) == E.QKV_ERR_ALIGN
+    assert L.qkv_calib_histogram(None, 0, FAKE, None) == E.QKV_OK  # nothing to count
+    for bad in (-1.0, float("nan"), float("inf")):
+        assert L.qkv_calib_stats(FAKE, bad, FAKE, None) == E.QKV_ERR_SCALE
+    assert L.qkv_calib_stats(None, 0.0, FAKE, None) == E.QKV_ERR_ARG
+    assert L.qkv_calib_stats(FAKE, 0.0, FAKE + 4, None) == E.QKV_ERR_ALIGN
