@@ -19,7 +19,8 @@
  *     trapped: the offending entry is skipped and a bit is OR-ed into the optional
  *     caller-provided device word `dev_status` (may be NULL).
  *   - head_dim must be 256 (256 B of int8 data per head, [INT8-PR §The finding worth
- *     upstreaming]); num_q_heads / num_kv_heads (the GQA group) must be 1..16.
+ *     upstreaming]); num_q_heads / num_kv_heads (the GQA group) must be 1..128 (groups above 16
+ *     run as one CTA per 16 query heads, each gathering the row's slots).
  *   - Pool layouts, S = num_slots, H = num_kv_heads, D = head_dim:
  *       QKV_BF16        K, V: bf16 [S, H, D]
  *       QKV_INT8_SIDE   K, V: int8 [S, H, D]; k_scale, v_scale: fp32 [S, H] (side tensors)
@@ -40,7 +41,7 @@ typedef enum {
   QKV_OK = 0,
   QKV_ERR_ARG = 1,         /* null pointer, negative size, bad enum, unsupported shape mix */
   QKV_ERR_SCALE = 2,       /* a per-layer scale that is not finite or is <= 0 */
-  QKV_ERR_UNSUPPORTED = 3, /* head_dim != 256 or GQA group outside 1..16 */
+  QKV_ERR_UNSUPPORTED = 3, /* head_dim != 256 or GQA group outside 1..128 */
   QKV_ERR_ALIGN = 4,       /* a base pointer or stride breaks the required alignment */
   QKV_ERR_CUDA = 5         /* a kernel launch or attribute call failed */
 } qkv_status;
@@ -213,9 +214,9 @@ qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t 
  * fused into the same launch.     [E4M3-PR §Implementation scope: split-K workspace and merge;
  *                                  HOIST-PR §Changes: the V scale is applied after the merge]
  *   Every split CTA of a (row, KV head) writes its partial to o_part / lse_part exactly as
- *   qsa_gather_attn does, then increments counters[row * num_kv_heads + kv_head]. The CTA
- *   that brings the counter to num_splits merges the num_splits partials of that (row, KV
- *   head) into out / lse (E4M3: times v_scale_layer) and resets the counter to 0. No CTA
+ *   qsa_gather_attn does, then increments the counter of its (row, KV head, chunk of 16 query
+ *   heads). The CTA that brings the counter to num_splits merges the num_splits partials of
+ *   those heads into out / lse (E4M3: times v_scale_layer) and resets the counter to 0. No CTA
  *   waits for another. The result is bit-identical to qsa_gather_attn followed by
  *   qsa_splitk_merge on the same partials; it saves the second launch and its gap.
  *
@@ -224,8 +225,9 @@ qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t 
  *              [rows, num_q_heads] or NULL: the merged result.
  *   o_part, lse_part  the split workspace, laid out as for qsa_gather_attn; left holding the
  *              partials.
- *   counters   uint32 [rows, num_kv_heads], 4 B-aligned, owned by the caller. They must all
- *              be 0 before the first call; every call leaves them 0 again.
+ *   counters   uint32 [rows, num_kv_heads, ceil(G / 16)] (G = num_q_heads / num_kv_heads),
+ *              4 B-aligned, owned by the caller. They must all be 0 before the first call;
+ *              every call leaves them 0 again.
  *   num_splits == 1 runs the unsplit kernel (o_part, lse_part and counters are not touched and
  *   may be NULL). num_splits > 1 with counters NULL is QKV_ERR_ARG.
  *   Calls that overlap on the GPU must not share counters or workspace.

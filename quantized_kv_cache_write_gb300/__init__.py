@@ -215,12 +215,14 @@ def qsa_gather_attn_splitk_fused(q, fmt: int, k_cache, v_cache, topk_idx, softma
                                  stream=None):
     """Split-K gather with the merge fused into the same launch (the last split CTA merges).
 
-    counters: int32/uint32 [R, num_kv_heads], all zero before the first call and left zero.
+    counters: int32/uint32 [R, num_kv_heads, ceil(G / 16)], all zero before the first call and
+    left zero (G = num_q_heads / num_kv_heads).
     """
     _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
     R, Hq, D = q.shape
-    if counters is not None and counters.numel() != R * num_kv_heads:
-        raise ValueError(f"counters must hold {R} x {num_kv_heads} entries, got {counters.numel()}")
+    chunks = (Hq // num_kv_heads + 15) // 16
+    if counters is not None and counters.numel() != R * num_kv_heads * chunks:
+        raise ValueError(f"counters must hold {R} x {num_kv_heads} x {chunks} entries, got {counters.numel()}")
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_idx.shape[1] if topk_idx is not None else 0
     st = lib.qsa_gather_attn_splitk_fused(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),

@@ -143,7 +143,8 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
     if (out || lse || !o_part || !lse_part) return QKV_ERR_ARG;
   }
   if (static_cast<int64_t>(topk) + num_splits > INT32_MAX) return QKV_ERR_ARG;
-  if (rows * num_kv_heads * static_cast<int64_t>(num_splits) > INT32_MAX) return QKV_ERR_ARG;
+  const int64_t head_chunks = (num_q_heads / num_kv_heads + 15) / 16;  // CTAs per (row, KV head, split)
+  if (rows * num_kv_heads * head_chunks * static_cast<int64_t>(num_splits) > INT32_MAX) return QKV_ERR_ARG;
   // the kernels number records (slot * H + head) in 32 bits
   if (num_slots * num_kv_heads > INT32_MAX) return QKV_ERR_UNSUPPORTED;
   if (rows == 0) return QKV_OK;

@@ -7,7 +7,8 @@
 // split-K merge); "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache" §Implementation
 // scope (split-K workspace).
 //
-// Work decomposition: one CTA (4 warps) per (query row, KV head, K-split). The split's index
+// Work decomposition: one CTA (4 warps) per (query row, KV head, K-split) -- and per chunk of
+// 16 query heads when the GQA group is larger than 16. The split's index
 // columns are cut into tiles of 16 keys, dealt round-robin to the warps; every warp then runs
 // on its own -- its own copy ring, online softmax and accumulators -- with no block barrier
 // in the main loop. The four partial results are merged once, at the end, through shared
@@ -34,8 +35,8 @@
 //          follows how a code word unpacks and the staged query uses the same permutation.
 //   softmax  logits times the hoisted K scale (per slot for int8; E4M3's per-layer scale is
 //          folded into the per-head factor). The running max is only raised when a tile's max
-//          exceeds it by more than 2^12 (log2 domain), so the accumulators are rescaled a few
-//          times per row rather than every tile; p <= 2^12 is sized for that.
+//          exceeds it by more than 2^8 (log2 domain), so the accumulators are rescaled a few
+//          times per row rather than every tile; p <= 2^8 is sized for that.
 //   p.V    p comes straight from the q.K^T accumulators (the m16n8 C layout of two N-tiles is
 //          the m16k16 A layout) as an fp16 hi + lo pair (bf16 pair for the bf16 layout): with
 //          outlier tokens a row can be a near-even mix of two large V rows of opposite sign,
@@ -54,12 +55,19 @@ namespace gather {
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kKeys = 16;  // keys per warp tile
+constexpr int kHeadsPerCta = 16;  // query heads per CTA: the M = 16 of the MMAs
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kMaxFinite = 3.4028234663852886e38f;  // largest finite fp32
-constexpr float kTau = 12.0f;  // lazy-rescale threshold (log2 units): p <= 2^12
-constexpr int kPShift = 3;     // p * 2^3 <= 2^15 stays a finite fp16; p >= 2^-17 stays normal
-constexpr int kEuHeadroom = 6;  // int8: the V-scale bound 2^eu is raised 2^6 past the largest scale seen
+// p.V operand range. p <= 2^kTau (lazy rescale) and, for int8, a V scale < 2^eu, so the fp16
+// operand x = p (v_scale) 2^(kPShift - eu) stays below 2^(kTau + kPShift) = 2^15, finite in
+// fp16. The hi + lo pair keeps ~22 bits only while x is well above fp16's normal floor 2^-14;
+// below it the pair's absolute error is 2^-25 (x units). So the shift is as large as the
+// ceiling allows, and the int8 bound eu sits only 2^2 above the largest scale seen: an
+// outlier token's ~16x larger scale costs one rescale instead of 4 bits of every other key.
+constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units): p <= 2^8
+constexpr int kPShift = 7;      // x < 2^15; a key 2^-21 below the running max still has a normal hi
+constexpr int kEuHeadroom = 2;  // int8: the V-scale bound 2^eu is raised 2^2 past the largest scale seen
 constexpr int kTmemCols = 128;  // per CTA: 4 warps x (their 32 lanes) x 128 fp32 columns
 
 // kRowBytes: bytes of one K (or V) row in shared memory (the inline layout keeps the 272 B
@@ -183,11 +191,18 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const int c = lane & 3, hn = lane >> 2;
   const int h0 = hn, h1 = hn + 8;
   const int P = a.num_splits, H = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / H;
+  // a GQA group above 16 query heads runs as chunks of 16, one CTA each (adjacent in launch
+  // order, so a chunk's second gather of the same slots mostly hits L2)
+  const int QC = (G + kHeadsPerCta - 1) / kHeadsPerCta;
   const int64_t bid = blockIdx.x;
   const int split = static_cast<int>(bid % P);
-  const int64_t rh = bid / P;
+  const int64_t unit = bid / P;  // (row, KV head, head chunk): the fused merge's counter index
+  const int qc = static_cast<int>(unit % QC);
+  const int64_t rh = unit / QC;
   const int h = static_cast<int>(rh % H);
   const int64_t r = rh / H;
+  const int hq0 = h * G + kHeadsPerCta * qc;            // first query head of this CTA
+  const int Gc = min(kHeadsPerCta, G - kHeadsPerCta * qc);  // query heads of this CTA (1..16)
   const int per_split = (a.topk + P - 1) / P;
   const int col0 = min(a.topk, split * per_split);
   const int col1 = min(a.topk, col0 + per_split);
@@ -360,10 +375,10 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   // ---------------- stage the query once: 8 threads per head, 32 head dims each
   {
     const int qh = tid >> 3, part = tid & 7;
-    const bool live = qh < G;
+    const bool live = qh < Gc;
     uint32_t w[16];
     if (live) {
-      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + static_cast<int64_t>(h) * G + qh) * kHeadDim +
+      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + hq0 + qh) * kHeadDim +
                                                       32 * part);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -579,11 +594,8 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     {
       const float nm0 = (mx0 > mu0 + kTau) ? mx0 : mu0;
       const float nm1 = (mx1 > mu1 + kTau) ? mx1 : mu1;
-      // int8: when a V scale reaches 2^eu, raise eu to kEuHeadroom past it, so that later,
-      // larger scales (outlier tokens run ~16x) do not force another rescale. Terms
-      // p v 2^(3 - eu) stay below 2^15; the headroom only moves the smallest ones 2^6 closer
-      // to the fp16 subnormal range, where their absolute error stays below 2^-25 of the
-      // 2^(eu - 3) unit -- far under the result's tolerance.
+      // int8: when a V scale reaches 2^eu, raise eu to kEuHeadroom past it (and rescale), so
+      // that every V scale stays below 2^eu and x below 2^15.
       int ne = eu;
       if (F::kInt8 && vmx_bits != 0u) {
         const int ev = static_cast<int>(vmx_bits >> 23) - 126;  // 2^ev > the largest |V scale|
@@ -815,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const int hh = tid >> 3, part = tid & 7;
   float wo[kWarps];
   float lse_h = -INFINITY;
-  if (hh < G) {
+  if (hh < Gc) {
     float mw[kWarps], M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
@@ -874,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
       // part covers the local head dims d(k) .. d(k) + 3, k = 0..3 (natural layouts:
       // d(k) = 4 part + 32 k, so that 8 consecutive threads read all 32 banks; others:
       // d(k) = 16 part + 4 k, stored at 40 (part / 2) + 16 (part % 2) + 4 k)
-      if (hh < G) {
+      if (hh < Gc) {
         uint64_t res[8];  // 16 floats as packed pairs
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) res[i2] = f2pack(0.f, 0.f);
@@ -889,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
             res[2 * k + 1] = f2fma(f2pack(x.z, x.w), ww2, res[2 * k + 1]);
           }
         }
-        const int64_t qhead = static_cast<int64_t>(h) * G + hh;
+        const int64_t qhead = hq0 + hh;
         float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
                               : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
         dst += 128 * sw + (F::kNatural ? 4 * part : 16 * part);
@@ -919,22 +931,22 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
     uint32_t* sLast = reinterpret_cast<uint32_t*>(smem + L::kPost);  // the weights above are formed
     __threadfence();  // this CTA's partial is visible device-wide before it is announced
     __syncthreads();
-    if (tid == 0) sLast[0] = (atomicAdd(a.counters + rh, 1u) == static_cast<uint32_t>(P - 1)) ? 1u : 0u;
+    if (tid == 0) sLast[0] = (atomicAdd(a.counters + unit, 1u) == static_cast<uint32_t>(P - 1)) ? 1u : 0u;
     __syncthreads();
     if (sLast[0] != 0u) {
       __threadfence();  // order the reads of the other CTAs' partials after their announcements
-      if (hh < G) {
+      if (hh < Gc) {
         // thread (hh, part) merges head hh's float4 columns part + 8 i: 8 threads of a head
         // read one contiguous 128 B line per load
         int col4[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) col4[i] = part + 8 * i;
-        const int64_t qhead = static_cast<int64_t>(h) * G + hh;
+        const int64_t qhead = hq0 + hh;
         merge_head<8>(a.o_part + (r * P * Hq + qhead) * kHeadDim, a.lse_part + r * P * Hq + qhead, Hq, P,
                       F::kE4m3 ? a.v_scale_layer : 1.f, col4, a.out + (r * Hq + qhead) * kHeadDim,
                       (a.lse != nullptr && part == 0) ? a.lse + r * Hq + qhead : nullptr);
       }
-      if (tid == 0) a.counters[rh] = 0u;  // every split has arrived: ready for the next call
+      if (tid == 0) a.counters[unit] = 0u;  // every split has arrived: ready for the next call
     }
   }
   // every warp's TMEM accesses are complete (the loads above were waited for): free the columns
@@ -958,7 +970,8 @@ cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t grid = a.rows * a.num_kv_heads * a.num_splits;
+  const int64_t chunks = (a.num_q_heads / a.num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
+  const int64_t grid = a.rows * a.num_kv_heads * chunks * a.num_splits;
   gather_attn_kernel<FMT, PAGED><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }

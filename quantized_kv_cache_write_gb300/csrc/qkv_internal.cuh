@@ -12,7 +12,7 @@
 namespace qkv {
 
 constexpr int kHeadDim = 256;
-constexpr int kMaxGroup = 16;
+constexpr int kMaxGroup = 128;  // GQA group; above 16 the gather runs one CTA per 16 query heads
 constexpr int kInlineRecord = kHeadDim + 4;  // 256 code bytes + fp32 scale
 
 // ------------------------------------------------------------------ launchers
@@ -54,8 +54,9 @@ struct GatherArgs {
   float* o_part;    // [rows, P, Hq, D] when num_splits > 1
   float* lse_part;  // [rows, P, Hq]
   uint32_t* dev_status;
-  // fused split-K merge (num_splits > 1 only): arrival counters [rows, Hkv], zero on entry and
-  // left zero; the last split CTA of a (row, KV head) merges into out / lse. Null = no merge.
+  // fused split-K merge (num_splits > 1 only): arrival counters [rows, Hkv, ceil(G / 16)], zero
+  // on entry and left zero; the last split CTA of a (row, KV head, head chunk) merges into
+  // out / lse. Null = no merge.
   uint32_t* counters = nullptr;
   // paged pools only (the paged launchers): topk_idx then holds logical positions
   const int32_t* block_table = nullptr;  // [num_seqs, max_blocks]

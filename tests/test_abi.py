@@ -60,7 +60,8 @@ def _gather(lib, **over):
 def test_gather_host_validation(lib):
     E = lib
     assert _gather(lib, d=128) == E.QKV_ERR_UNSUPPORTED
-    assert _gather(lib, hq=34, hkv=2) == E.QKV_ERR_UNSUPPORTED  # group 17
+    assert _gather(lib, hq=258, hkv=2) == E.QKV_ERR_UNSUPPORTED  # group 129
+    assert _gather(lib, hq=256, hkv=2, rows=0) == E.QKV_OK  # group 128 is supported
     assert _gather(lib, hq=15, hkv=2) == E.QKV_ERR_ARG
     assert _gather(lib, fmt=7) == E.QKV_ERR_ARG
     assert _gather(lib, ks=None) == E.QKV_ERR_ARG  # side format needs per-slot scales

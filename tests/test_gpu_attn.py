@@ -68,6 +68,28 @@ def test_gqa8_and_two_kv_heads(fmt):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (20, 1), (4, 1), (64, 2), (128, 1)])
+def test_gqa_groups_beyond_and_below_16(fmt, hq, hkv):
+    # groups above 16 run one CTA per 16 query heads (the last chunk ragged for 20)
+    wl = small_random(52, num_slots=3000, rows=3, topk=150, num_q_heads=hq, num_kv_heads=hkv, pad_frac=0.1,
+                      outlier_frac=0.02)
+    _check(wl, fmt)
+    if hq // hkv > 16:
+        _check(wl, fmt, num_splits=3)
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_outlier_heavy_seed_sweep(fmt):
+    # Rows dominated by a few 16x outlier keys, the rest of the weight spread thin: the regime
+    # where the small keys' p.V operands sit lowest in fp16's range. Twelve seeds, 2 - 5 %
+    # outlier tokens, top-k from 64 to 1024.
+    for seed in range(12):
+        wl = small_random(300 + seed, num_slots=4000, rows=4, topk=64 + 80 * seed, pad_frac=0.05,
+                          outlier_frac=0.02 + 0.0025 * seed)
+        _check(wl, fmt)
+
+
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_empty_rows_and_zero_topk(fmt):
     wl = small_random(46, num_slots=2000, rows=4, topk=50)
     wl.topk[1] = -1

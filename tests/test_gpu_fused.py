@@ -25,7 +25,8 @@ def _fused(gp, wl, P, counters=None, with_lse=True, dev_status=None):
     idx = torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
     R, Hq, D = qd.shape
     if counters is None:
-        counters = torch.zeros((R, wl.num_kv_heads), dtype=torch.int32, device="cuda")
+        chunks = (Hq // wl.num_kv_heads + 15) // 16
+        counters = torch.zeros((R, wl.num_kv_heads, chunks), dtype=torch.int32, device="cuda")
     out = torch.full((R, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
     lse = torch.full((R, Hq), float("nan"), dtype=torch.float32, device="cuda") if with_lse else None
     o_part = torch.full((R, P, Hq, D), float("nan"), dtype=torch.float32, device="cuda")
@@ -77,6 +78,19 @@ def test_counters_are_reused_across_calls_and_kv_heads():
     ro, rl = OraclePool(wl, "int8_side").attend(wl)
     assert_close(second[0], ro, "out")
     assert_close(second[1], rl, "lse")
+
+
+@pytest.mark.parametrize("hq,hkv", [(32, 1), (40, 2)])
+def test_fused_with_head_chunks(hq, hkv):
+    wl = small_random(64, num_slots=3000, rows=4, topk=400, num_q_heads=hq, num_kv_heads=hkv, pad_frac=0.05)
+    gp = GpuPool(wl, "int8_side")
+    out, lse, o_part, lse_part, counters = _fused(gp, wl, 6)
+    ref = gp.attend(wl, num_splits=6)
+    _same(out, ref[0], "out")
+    _same(lse, ref[1], "lse")
+    assert int(counters.abs().sum().item()) == 0
+    ro, rl = OraclePool(wl, "int8_side").attend(wl)
+    assert_close(out, ro, "out")
 
 
 def test_lse_is_optional_and_single_split_runs_unsplit():
