@@ -582,11 +582,23 @@ def measure_workloads(q, flush, stream, reps, peak):
         q.qsa_splitk_merge(o_part, lse_part, out)
 
     t["paged_split_plus_merge_ms"] = _time_events(paged, flush, stream, reps)
+    # the split count qsa_suggest_num_splits picks for this shape (one wave of resident CTAs)
+    Pa = q.qsa_suggest_num_splits(q.QKV_INT8_SIDE, wl.rows, wl.num_q_heads, wl.num_kv_heads, wl.topk.shape[1])
+    o_pa = torch.empty((wl.rows, Pa, wl.num_q_heads, HEAD_DIM), dtype=torch.float32, device="cuda")
+    l_pa = torch.empty((wl.rows, Pa, wl.num_q_heads), dtype=torch.float32, device="cuda")
+    cnt = torch.zeros((wl.rows, 1, 1), dtype=torch.int32, device="cuda")
+    t["fused_suggested_splits_ms"] = _time_events(
+        lambda: q.qsa_gather_attn_splitk_fused(qd, q.QKV_INT8_SIDE, kc, vc, idx, wl.softmax_scale, num_splits=Pa,
+                                               out=out, o_part=o_pa, lse_part=l_pa, counters=cnt, **kw),
+        flush, stream, reps)
+    t["suggested_splits"] = Pa
     bytes_lc = wl.rows * wl.topk.shape[1] * SLOT_BYTES["int8_side"]
     res["long_context_decode"] = {
         "shape": "8 seq x 131072 tokens (paged, blocks of 16), 40 rows x top-k 2048, 16 splits, int8 side",
-        **{k: round(v, 5) for k, v in t.items()},
+        **{k: (round(v, 5) if isinstance(v, float) else v) for k, v in t.items()},
         "fused_gathered_GBps": round(bytes_lc / (t["fused_ms"] * 1e-3) / 1e9, 2),
+        "fused_suggested_gathered_GBps": round(bytes_lc / (t["fused_suggested_splits_ms"] * 1e-3) / 1e9, 2),
+        "rows_per_s_suggested": round(wl.rows / (t["fused_suggested_splits_ms"] * 1e-3), 1),
         "note": "42.6 MB gathered per step: launch latency and the wave tail dominate"}
     del kc, vc
     torch.cuda.empty_cache()

@@ -243,6 +243,21 @@ qkv_status qsa_gather_attn_splitk_fused(const void* q, int64_t rows, int num_q_h
                                         void* stream);
 
 /*
+ * qsa_suggest_num_splits -- a split count for a gather launch of this shape on the current
+ * device: enough splits to fill one wave of resident CTAs, so that a launch with few rows
+ * still spreads over every SM.       [E4M3-PR §Implementation scope: split-K workspace; the
+ *                                     pages tune the partition per route, P256 / P1024]
+ *   P = floor(SMs * C / (rows * num_kv_heads * ceil(G / 16))), at most ceil(topk / 128) (at
+ *   least 8 tiles of 16 keys per split) and at least 1, where C is the occupancy of the
+ *   layout's gather kernel (CTAs per SM) capped at 2. Any P gives the same result up to
+ *   rounding.
+ *   Host-only (queries the device, launches nothing). Errors as qsa_gather_attn's shape checks;
+ *   a failed device query is QKV_ERR_CUDA.
+ */
+qkv_status qsa_suggest_num_splits(qkv_format fmt, int64_t rows, int num_q_heads, int num_kv_heads,
+                                  int topk, int* num_splits);
+
+/*
  * qsa_gather_attn_splitk_noalloc -- qsa_gather_attn with num_splits > 1 followed by
  * qsa_splitk_merge, for callers that cannot allocate device memory. The pages have no
  * counterpart: this is a packaging of the two calls above, not a step of the method.

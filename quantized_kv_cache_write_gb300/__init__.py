@@ -40,6 +40,7 @@ _SIGS = {
     "qsa_gather_attn": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
                         _i32, _p, _p, _p, _p, _p, _p],
     "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
+    "qsa_suggest_num_splits": [_i32, _i64, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int)],
     "qsa_gather_attn_splitk_noalloc": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p,
                                        _i32, _f32, _i32, _p, _p, _p, _p],
     "qsa_gather_attn_splitk_fused": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32,
@@ -231,6 +232,14 @@ def qsa_gather_attn_splitk_fused(q, fmt: int, k_cache, v_cache, topk_idx, softma
                                           num_splits, _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part),
                                           _ptr(counters), _ptr(dev_status), _stream(stream))
     _check("qsa_gather_attn_splitk_fused", st)
+
+
+def qsa_suggest_num_splits(fmt: int, rows: int, num_q_heads: int, num_kv_heads: int, topk: int) -> int:
+    """Split count that fills one wave of resident CTAs on the current device."""
+    out = ctypes.c_int(0)
+    st = lib.qsa_suggest_num_splits(fmt, rows, num_q_heads, num_kv_heads, topk, ctypes.byref(out))
+    _check("qsa_suggest_num_splits", st)
+    return out.value
 
 
 def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1.0, stream=None):

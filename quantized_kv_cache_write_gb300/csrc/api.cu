@@ -251,6 +251,36 @@ qkv_status qsa_gather_attn_splitk_fused(const void* q, int64_t rows, int num_q_h
                      o_part, lse_part, dev_status, stream, nullptr, counters);
 }
 
+qkv_status qsa_suggest_num_splits(qkv_format fmt, int64_t rows, int num_q_heads, int num_kv_heads, int topk,
+                                  int* num_splits) {
+  if (!num_splits || rows < 0 || topk < 0) return QKV_ERR_ARG;
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return QKV_ERR_ARG;
+  if (num_q_heads / num_kv_heads > kMaxGroup) return QKV_ERR_UNSUPPORTED;
+  int per_sm = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (fmt) {
+    case QKV_BF16: e = qkv::gather_ctas_per_sm_bf16(&per_sm); break;
+    case QKV_INT8_SIDE: e = qkv::gather_ctas_per_sm_int8_side(&per_sm); break;
+    case QKV_INT8_INLINE: e = qkv::gather_ctas_per_sm_int8_inline(&per_sm); break;
+    case QKV_E4M3: e = qkv::gather_ctas_per_sm_e4m3(&per_sm); break;
+    default: return QKV_ERR_ARG;
+  }
+  if (e != cudaSuccess) return QKV_ERR_CUDA;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return QKV_ERR_CUDA;
+  const int64_t units = rows * num_kv_heads * ((num_q_heads / num_kv_heads + 15) / 16);  // CTAs per split
+  // one wave at up to two CTAs per SM: on the long-context and split-K workloads fewer, longer
+  // CTAs per SM beat a third resident CTA (its prologue, epilogue and merge contend)
+  const int64_t slots = static_cast<int64_t>(sms) * (per_sm < 1 ? 1 : (per_sm > 2 ? 2 : per_sm));
+  int64_t p = units > 0 ? slots / units : 1;
+  const int64_t cap = (static_cast<int64_t>(topk) + 127) / 128;  // at least 128 keys (8 tiles) per split
+  if (p > cap) p = cap;
+  if (p < 1) p = 1;
+  *num_splits = static_cast<int>(p);
+  return QKV_OK;
+}
+
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows, int num_q_heads,
                             int head_dim, int num_splits, float v_scale_post, float* out, float* lse,
                             void* stream) {

@@ -108,7 +108,7 @@ __host__ __device__ constexpr int v_region_shift(int i) {
 template <int FMT>
 __host__ __device__ constexpr int merge_row() { return Fmt<FMT>::kNatural ? 136 : 164; }
 
-template <int FMT>
+template <int FMT, int STAGES = Fmt<FMT>::kStages>
 struct Smem {
   using F = Fmt<FMT>;
   static constexpr size_t kQ = 0;  // [16 k-steps][16 heads][16] 16-bit, fragment order
@@ -122,9 +122,11 @@ struct Smem {
   static constexpr size_t kStageV = kKArea;
   static constexpr size_t kStageKs = kStageV + kVArea;
   static constexpr size_t kStageMeta = kStageKs + (F::kSide ? 2 * kKeys * 4 : 0);
-  static constexpr size_t kStageBytes = ((kStageMeta + (F::kInline ? kKeys : 0)) + 15) / 16 * 16;
-  static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][kStages] stages
-  static constexpr size_t kWarpRing = size_t(F::kStages) * kStageBytes;
+  // deeper rings keep each stage's valid-key mask here (a two-stage ring keeps it in registers)
+  static constexpr size_t kStageMask = (kStageMeta + (F::kInline ? kKeys : 0) + 3) / 4 * 4;
+  static constexpr size_t kStageBytes = ((kStageMask + (STAGES > 2 ? 4 : 0)) + 15) / 16 * 16;
+  static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][STAGES] stages
+  static constexpr size_t kWarpRing = size_t(STAGES) * kStageBytes;
   static constexpr size_t kTmem = kRing + kWarps * kWarpRing;  // TMEM base address
   static constexpr size_t kM = kTmem + 16;                         // [kWarps][16] floats
   static constexpr size_t kL = kM + kWarps * 16 * 4;                 // [kWarps][16] floats
@@ -182,10 +184,14 @@ __device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
 
 // PAGED: topk_idx holds logical positions of the row's sequence (a.row_seq), mapped to slots
 // through a.block_table; otherwise it holds slot ids.
-template <int FMT, bool PAGED>
-__global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_kernel(const GatherArgs a) {
+// STAGES: depth of each warp's copy ring (tiles in flight); MINB: CTAs per SM the register
+// budget is sized for. The default (2, the format's) suits full-GPU launches; a deeper ring
+// with fewer CTAs per SM suits launches with too few CTAs to fill the GPU.
+template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks>
+__global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const GatherArgs a) {
   using F = Fmt<FMT>;
-  using L = Smem<FMT>;
+  using L = Smem<FMT, STAGES>;
+  static_assert(STAGES >= 2, "the ring needs a stage in flight while one is computed");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, hn = lane >> 2;
@@ -286,13 +292,14 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT>(key_sub) + 16 * chunk_sub;
   const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(key_sub) - L::kStageV + 16 * chunk_sub;
 
-  // Copy one 16-key tile into ring stage i % kStages; returns the tile's valid-key mask.
-  static_assert(F::kStages == 2, "the valid-key masks ride one tile ahead in registers");
+  // Copy one 16-key tile into ring stage i % STAGES; returns the tile's valid-key mask (a
+  // two-stage ring carries it one tile ahead in a register, a deeper one in the stage).
   auto issue = [&](int i, int idxv) -> uint32_t {  // idxv: this lane's checked slot (or -1)
-    const int st = i % F::kStages;
+    const int st = i % STAGES;
     const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
     uint8_t* sb = ring + size_t(st) * L::kStageBytes;
     const uint32_t sbase = smem_u32(sb);
+    if (STAGES > 2 && lane == 0) sts32(sbase + L::kStageMask, mask);
     // record number (slot * H + h; the host keeps it below 2^31) of key `lane`, -1 = padding
     const int rec_l = idxv >= 0 ? idxv * H + h : -1;
     if (!F::kInline) {
@@ -356,20 +363,35 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   // latencies overlap the query's.
   // index pipeline: nidx = tile i + 1's entry (slot id, or position when paged); paged also
   // carries nblk = its block id and ppos = tile i + 2's position
+  // The prologue issues tiles 0 .. STAGES - 2 (one commit group each) and loads tile
+  // STAGES - 1's entry for the first loop iteration.
   int nidx, nblk = -1, ppos = -1;
-  uint32_t mask_cur = 0;  // valid keys of the tile being computed (bit k = key k)
+  uint32_t mask_cur = 0;  // two-stage ring: valid keys of the tile being computed (bit k = key k)
   {
-    const int first = load_idx(0);
-    nidx = load_idx(1);
+    int ent[STAGES - 1];
+#pragma unroll
+    for (int t = 0; t < STAGES - 1; ++t) ent[t] = load_idx(t);
+    nidx = load_idx(STAGES - 1);
     if (PAGED) {
-      ppos = load_idx(2);
-      const int fblk = lookup(first);
+      ppos = load_idx(STAGES);
+      int blk[STAGES - 1];
+#pragma unroll
+      for (int t = 0; t < STAGES - 1; ++t) blk[t] = lookup(ent[t]);
       nblk = lookup(nidx);
-      if (0 < my) mask_cur = issue(0, checked_paged(first, fblk));
+#pragma unroll
+      for (int t = 0; t < STAGES - 1; ++t) {
+        const uint32_t m = (t < my) ? issue(t, checked_paged(ent[t], blk[t])) : 0u;
+        if (t == 0) mask_cur = m;
+        cp_async_commit();
+      }
     } else {
-      if (0 < my) mask_cur = issue(0, checked(first));
+#pragma unroll
+      for (int t = 0; t < STAGES - 1; ++t) {
+        const uint32_t m = (t < my) ? issue(t, checked(ent[t])) : 0u;
+        if (t == 0) mask_cur = m;
+        cp_async_commit();
+      }
     }
-    cp_async_commit();
   }
 
   // ---------------- stage the query once: 8 threads per head, 32 head dims each
@@ -459,22 +481,24 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
   int eu = -100;                           // int8: 2^eu > every V scale seen
   for (int i = 0; i < my; ++i) {
-    const uint32_t mask_next = (i + 1 < my) ? issue(i + 1, PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : 0u;
+    const int inext = i + STAGES - 1;  // the tile issued now, into the stage freed last iteration
+    const uint32_t mask_next =
+        (inext < my) ? issue(inext, PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : 0u;
     cp_async_commit();
     if (PAGED) {
       nidx = ppos;
       nblk = lookup(ppos);
-      ppos = load_idx(i + 3);
+      ppos = load_idx(i + STAGES + 1);
     } else {
-      nidx = load_idx(i + F::kStages);
+      nidx = load_idx(i + STAGES);
     }
-    cp_async_wait<F::kStages - 1>();
-    const int st = i % F::kStages;
+    cp_async_wait<STAGES - 1>();
+    const int st = i % STAGES;
     __syncwarp();
 
     const uint8_t* sb = ring + size_t(st) * L::kStageBytes;
     const uint32_t sbase = smem_u32(sb);
-    const uint32_t mask = mask_cur;
+    const uint32_t mask = (STAGES == 2) ? mask_cur : lds32(sbase + L::kStageMask);
 
     // ---- q . K^T for this warp's 16 keys: one accumulator per N-tile (the two chains
     //      interleave; splitting each further measured no faster)
@@ -791,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
         tmem_st32(tacc + 64 * sw + 32, ob[1]);
       }
     }
-    mask_cur = mask_next;
+    if (STAGES == 2) mask_cur = mask_next;
     __syncwarp();
   }
 
@@ -942,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
 #pragma unroll
         for (int i = 0; i < 8; ++i) col4[i] = part + 8 * i;
         const int64_t qhead = hq0 + hh;
-        merge_head<8>(a.o_part + (r * P * Hq + qhead) * kHeadDim, a.lse_part + r * P * Hq + qhead, Hq, P,
+        merge_head<8, 2>(a.o_part + (r * P * Hq + qhead) * kHeadDim, a.lse_part + r * P * Hq + qhead, Hq, P,
                       F::kE4m3 ? a.v_scale_layer : 1.f, col4, a.out + (r * Hq + qhead) * kHeadDim,
                       (a.lse != nullptr && part == 0) ? a.lse + r * Hq + qhead : nullptr);
       }
@@ -956,24 +980,68 @@ __global__ void __launch_bounds__(kThreads, Fmt<FMT>::kMinBlocks) gather_attn_ke
   if (warp == 0) tmem_dealloc(*sTmem, kTmemCols);
 }
 
-template <int FMT, bool PAGED = false>
-cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
-  constexpr size_t smem = Smem<FMT>::kTotal;
+// CTAs of one launch: (row, KV head, 16-head chunk, split).
+inline int64_t gather_grid(const GatherArgs& a) {
+  const int64_t chunks = (a.num_q_heads / a.num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
+  return a.rows * a.num_kv_heads * chunks * a.num_splits;
+}
+
+// Opt the kernel into its dynamic shared memory, once per device.
+template <int FMT, bool PAGED, int STAGES, int MINB>
+cudaError_t prepare_variant() {
   static bool attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem));
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(Smem<FMT, STAGES>::kTotal));
+    if (e != cudaSuccess) return e;
+    // all of the unified L1 / shared array as shared memory: the copies bypass L1 anyway, and
+    // the occupancy query then sees the CTAs per SM that a launch gets
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
   }
-  const int64_t chunks = (a.num_q_heads / a.num_kv_heads + kHeadsPerCta - 1) / kHeadsPerCta;
-  const int64_t grid = a.rows * a.num_kv_heads * chunks * a.num_splits;
-  gather_attn_kernel<FMT, PAGED><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+  return cudaSuccess;
+}
+
+template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks>
+cudaError_t launch_variant(const GatherArgs& a, cudaStream_t stream) {
+  cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB>();
+  if (e != cudaSuccess) return e;
+  gather_attn_kernel<FMT, PAGED, STAGES, MINB>
+      <<<static_cast<unsigned>(gather_grid(a)), kThreads, Smem<FMT, STAGES>::kTotal, stream>>>(a);
   return cudaGetLastError();
+}
+
+// CTAs of the default kernel of this layout that one SM holds at once: the smaller of its
+// shared-memory and register limits (allocated per warp in units of 256 registers).
+template <int FMT>
+cudaError_t resident_ctas_per_sm(int* n) {
+  constexpr int S = Fmt<FMT>::kStages, B = Fmt<FMT>::kMinBlocks;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, gather_attn_kernel<FMT, false, S, B>);
+  if (e != cudaSuccess) return e;
+  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess) return e;
+  const size_t per_cta = Smem<FMT, S>::kTotal + fa.sharedSizeBytes + static_cast<size_t>(reserved);
+  const int by_smem = static_cast<int>(static_cast<size_t>(smem_sm) / per_cta);
+  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+  const int by_regs = regs_warp > 0 ? regs_sm / (regs_warp * kWarps) : by_smem;
+  *n = by_smem < by_regs ? by_smem : by_regs;
+  return cudaSuccess;
+}
+
+template <int FMT, bool PAGED = false>
+cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
+  return launch_variant<FMT, PAGED>(a, stream);
 }
 
 }  // namespace gather

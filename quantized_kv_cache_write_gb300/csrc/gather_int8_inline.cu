@@ -6,4 +6,5 @@ namespace qkv {
 cudaError_t launch_gather_int8_inline(const GatherArgs& a, cudaStream_t stream) {
   return gather::launch<QKV_INT8_INLINE>(a, stream);
 }
+cudaError_t gather_ctas_per_sm_int8_inline(int* n) { return gather::resident_ctas_per_sm<QKV_INT8_INLINE>(n); }
 }  // namespace qkv

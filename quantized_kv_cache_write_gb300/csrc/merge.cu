@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kMergeThreads)
   const int g = static_cast<int>(item - r * num_q_heads);
 
   const int col4[2] = {2 * lane, 2 * lane + 1};  // lane owns columns 8 lane .. 8 lane + 7
-  merge_head<2>(o_part + (r * num_splits * num_q_heads + g) * kHeadDim, lse_part + r * num_splits * num_q_heads + g,
+  merge_head<2, 4>(o_part + (r * num_splits * num_q_heads + g) * kHeadDim, lse_part + r * num_splits * num_q_heads + g,
                 num_q_heads, num_splits, v_scale_post, col4, out + item * kHeadDim,
                 (lse != nullptr && lane == 0) ? lse + item : nullptr);
 }

@@ -74,6 +74,10 @@ cudaError_t launch_gather_paged_bf16(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_paged_int8_side(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_paged_int8_inline(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_paged_e4m3(const GatherArgs& a, cudaStream_t stream);
+cudaError_t gather_ctas_per_sm_bf16(int* n);
+cudaError_t gather_ctas_per_sm_int8_side(int* n);
+cudaError_t gather_ctas_per_sm_int8_inline(int* n);
+cudaError_t gather_ctas_per_sm_e4m3(int* n);
 
 // ------------------------------------------------------------------ device helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -244,13 +248,15 @@ __device__ __forceinline__ void f2scale(float* v, uint64_t s) {
 // with empty splits (lse_s = -inf) skipped and an all-empty row giving o = 0, lse = -inf.
 // o_head = o_part at (row, split 0, head): splits are Hq * kHeadDim floats apart; lp = lse_part
 // at (row, split 0, head): splits are Hq floats apart. Partials are read through L2
-// (ld.global.cg) because in the fused gather other CTAs of the same launch wrote them. Every
-// caller runs this same arithmetic, so a column's result does not depend on which thread or
-// kernel merges it.
-template <int NV>
+// (ld.global.cg) because in the fused gather other CTAs of the same launch wrote them. The
+// loads of U splits are issued together (U * NV 16 B loads in flight per thread); the sums
+// still run over s = 0, 1, ... in order, so a column's result does not depend on which thread
+// or kernel merges it, nor on U.
+template <int NV, int U>
 __device__ __forceinline__ void merge_head(const float* o_head, const float* lp, int Hq, int P, float v_scale_post,
                                            const int (&col4)[NV], float* out_head, float* lse_out) {
   float m = -INFINITY;
+#pragma unroll 4
   for (int s = 0; s < P; ++s) m = fmaxf(m, __ldcg(lp + static_cast<int64_t>(s) * Hq));
   float4* dst = reinterpret_cast<float4*>(out_head);
   if (m == -INFINITY) {
@@ -264,19 +270,29 @@ __device__ __forceinline__ void merge_head(const float* o_head, const float* lp,
   for (int i = 0; i < 4 * NV; ++i) acc[i] = 0.f;
   float wsum = 0.f;
   const int64_t sstride = static_cast<int64_t>(Hq) * kHeadDim;
-  for (int s = 0; s < P; ++s) {
-    const float ls = __ldcg(lp + static_cast<int64_t>(s) * Hq);
-    if (ls == -INFINITY) continue;
-    const float w = expf(ls - m);
-    wsum += w;
-    const float4* src = reinterpret_cast<const float4*>(o_head + s * sstride);
+  for (int s0 = 0; s0 < P; s0 += U) {
+    float4 x[U][NV];
+    float ls[U];
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-      const float4 x = __ldcg(src + col4[v]);
-      acc[4 * v] += w * x.x;
-      acc[4 * v + 1] += w * x.y;
-      acc[4 * v + 2] += w * x.z;
-      acc[4 * v + 3] += w * x.w;
+    for (int u = 0; u < U; ++u) {
+      const bool in = s0 + u < P;
+      ls[u] = in ? __ldcg(lp + static_cast<int64_t>(s0 + u) * Hq) : -INFINITY;
+      const float4* src = reinterpret_cast<const float4*>(o_head + (in ? s0 + u : s0) * sstride);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) x[u][v] = __ldcg(src + col4[v]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (ls[u] == -INFINITY) continue;
+      const float w = expf(ls[u] - m);
+      wsum += w;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        acc[4 * v] += w * x[u][v].x;
+        acc[4 * v + 1] += w * x[u][v].y;
+        acc[4 * v + 2] += w * x[u][v].z;
+        acc[4 * v + 3] += w * x[u][v].w;
+      }
     }
   }
   const float f = v_scale_post / wsum;

@@ -205,3 +205,14 @@ def test_calibration_host_validation(lib):
         assert L.qkv_calib_stats(FAKE, bad, FAKE, None) == E.QKV_ERR_SCALE
     assert L.qkv_calib_stats(None, 0.0, FAKE, None) == E.QKV_ERR_ARG
     assert L.qkv_calib_stats(FAKE, 0.0, FAKE + 4, None) == E.QKV_ERR_ALIGN
+
+
+def test_suggest_num_splits_host_validation(lib):
+    import ctypes
+    E, L = lib, lib.lib
+    out = ctypes.c_int(0)
+    assert L.qsa_suggest_num_splits(E.QKV_INT8_SIDE, 40, 16, 1, 2048, None) == E.QKV_ERR_ARG
+    assert L.qsa_suggest_num_splits(E.QKV_INT8_SIDE, -1, 16, 1, 2048, ctypes.byref(out)) == E.QKV_ERR_ARG
+    assert L.qsa_suggest_num_splits(E.QKV_INT8_SIDE, 40, 15, 2, 2048, ctypes.byref(out)) == E.QKV_ERR_ARG
+    assert L.qsa_suggest_num_splits(E.QKV_INT8_SIDE, 40, 258, 2, 2048, ctypes.byref(out)) == E.QKV_ERR_UNSUPPORTED
+    assert L.qsa_suggest_num_splits(7, 40, 16, 1, 2048, ctypes.byref(out)) == E.QKV_ERR_ARG

@@ -131,3 +131,16 @@ def test_long_context_decode_fused():
     ro, rl = OraclePool(wl, "int8_side").attend(wl)
     assert_close(out, ro, "out")
     assert_close(lse, rl, "lse")
+
+
+def test_suggested_split_counts():
+    import quantized_kv_cache_write_gb300 as q
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # occupancy 3, 3, 2, 1 CTAs per SM, capped at 2
+    for fmt, per_sm in (("int8_side", 2), ("e4m3", 2), ("int8_inline", 2), ("bf16", 1)):
+        code = q.FORMATS[fmt]
+        # 40 decode rows x top-k 2048: one wave of resident CTAs
+        assert q.qsa_suggest_num_splits(code, 40, 16, 1, 2048) == max(1, min(16, sms * per_sm // 40))
+        assert q.qsa_suggest_num_splits(code, 20, 32, 1, 2048) == max(1, min(16, sms * per_sm // 40))
+        assert q.qsa_suggest_num_splits(code, 4, 16, 1, 100) == 1  # at least 128 keys per split
+        assert q.qsa_suggest_num_splits(code, 100000, 16, 1, 1024) == 1  # the rows already fill the GPU
