@@ -8,6 +8,7 @@ from .workloads import (  # noqa: F401
     chunked_prefill,
     e4m3_splitk_layer,
     f32_to_bf16_bits,
+    f32_to_f16_bits,
     long_context_decode,
     page1_shape,
     small_paged,

@@ -47,6 +47,12 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out.reshape(np.shape(x))
 
 
+def f32_to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to IEEE half (numpy's conversion: nearest, ties to even) and
+    return the uint16 bits. Inputs here are finite and far below the fp16 range's end."""
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
 @dataclasses.dataclass
 class Workload:
     """One synthetic problem: tokens written into a slot pool, then query rows gathering it."""
@@ -75,6 +81,9 @@ class Workload:
     topk_pos: Optional[np.ndarray] = None
     block_size: int = 0
     notes: str = ""
+    # 16-bit type of q and of the new K/V tokens: "bf16", or "f16" for the FP16-activation
+    # contract of "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache" (§Purpose)
+    act_dtype: str = "bf16"
 
     @property
     def rows(self) -> int:
@@ -261,11 +270,12 @@ def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: i
                  num_kv_heads: int = 1, pad_frac: float = 0.0, outlier_frac: float = 0.0,
                  outlier_factor: float = 16.0, num_tokens: Optional[int] = None,
                  num_splits: int = 1, softmax_scale: float = 1.0 / 16.0,
-                 zero_tokens: int = 0) -> Workload:
+                 zero_tokens: int = 0, act_dtype: str = "bf16") -> Workload:
     """Generic small case for parity tests: ragged top-k, -1 padding, optional outliers.
 
     `zero_tokens` tokens (chosen after the outliers) get all-zero K and V vectors, the
-    degenerate absmax = 0 case.
+    degenerate absmax = 0 case. act_dtype 'f16' rounds q, K and V to IEEE half instead of
+    bf16 (same draws).
     """
     S, H, D = num_slots, num_kv_heads, HEAD_DIM
     T = S if num_tokens is None else num_tokens
@@ -279,7 +289,8 @@ def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: i
     if zero_tokens:
         factor[rng.choice(T, size=zero_tokens, replace=False)] = np.float32(0.0)
     slot_mapping = rng.choice(S, size=T, replace=False).astype(np.int64)
-    q = f32_to_bf16_bits(_normals(rng, (rows, num_q_heads, D)))
+    to16 = f32_to_f16_bits if act_dtype == "f16" else f32_to_bf16_bits
+    q = to16(_normals(rng, (rows, num_q_heads, D)))
     written = slot_mapping
     kk = min(topk, T)
     idx = np.full((rows, topk), -1, dtype=np.int32)
@@ -289,9 +300,13 @@ def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: i
             drop = rng.random(kk) < pad_frac
             picks = np.where(drop, -1, picks)
         idx[r, :kk] = picks
-    return Workload(f"small random (S={S}, T={T}, R={rows}, k={topk}, Hq={num_q_heads}, Hkv={H})",
-                    seed, S, H, num_q_heads, D, _scaled_bf16(k, factor), _scaled_bf16(v, factor),
-                    slot_mapping, q, idx, softmax_scale=softmax_scale, num_splits=num_splits)
+    if act_dtype == "f16":
+        kt, vt = to16(k * factor[:, None, None]), to16(v * factor[:, None, None])
+    else:
+        kt, vt = _scaled_bf16(k, factor), _scaled_bf16(v, factor)
+    return Workload(f"small random (S={S}, T={T}, R={rows}, k={topk}, Hq={num_q_heads}, Hkv={H}, {act_dtype})",
+                    seed, S, H, num_q_heads, D, kt, vt,
+                    slot_mapping, q, idx, softmax_scale=softmax_scale, num_splits=num_splits, act_dtype=act_dtype)
 
 
 

@@ -33,7 +33,7 @@ import math
 
 import numpy as np
 
-from .quant import bf16_bits_to_f32, e4m3_decode
+from .quant import act_bits_to_f32, bf16_bits_to_f32, e4m3_decode, f16_bits_to_f32
 
 
 # --------------------------------------------------------------------------- dequantisation
@@ -61,6 +61,11 @@ def bf16_pool_fp64(bits: np.ndarray) -> np.ndarray:
     return bf16_bits_to_f32(bits).astype(np.float64)
 
 
+def f16_pool_fp64(bits: np.ndarray) -> np.ndarray:
+    """Unquantised fp16 pool (the FP16-activation contract's baseline cache) -> fp64."""
+    return f16_bits_to_f32(bits).astype(np.float64)
+
+
 # --------------------------------------------------------------------------- attention
 
 def _row_attention(qr: np.ndarray, K: np.ndarray, V: np.ndarray, sel: np.ndarray,
@@ -86,10 +91,11 @@ def _row_attention(qr: np.ndarray, K: np.ndarray, V: np.ndarray, sel: np.ndarray
 
 
 def gather_attention(q_bits: np.ndarray, K: np.ndarray, V: np.ndarray, topk: np.ndarray,
-                     softmax_scale: float, rows=None, col_range=None):
+                     softmax_scale: float, rows=None, col_range=None, q_dtype: str = "bf16"):
     """Top-k gather attention over a dequantised pool.
 
-    q_bits: uint16 bf16 [R, Hq, D]; K, V: fp64 [S, Hkv, D]; topk: int [R, k] (-1 = pad).
+    q_bits: uint16 bf16 (or fp16, q_dtype='f16') [R, Hq, D]; K, V: fp64 [S, Hkv, D];
+    topk: int [R, k] (-1 = pad).
     rows: optional iterable of row ids to compute (others left at 0 / -inf).
     col_range: optional (a, b) restricting each row to index columns [a, b).
     Returns o fp64 [R, Hq, D] and lse fp64 [R, Hq].
@@ -97,7 +103,7 @@ def gather_attention(q_bits: np.ndarray, K: np.ndarray, V: np.ndarray, topk: np.
     R, Hq, D = q_bits.shape
     S, Hkv, _ = K.shape
     group = Hq // Hkv
-    q = bf16_bits_to_f32(q_bits).astype(np.float64)
+    q = act_bits_to_f32(q_bits, q_dtype).astype(np.float64)
     o = np.zeros((R, Hq, D), dtype=np.float64)
     lse = np.full((R, Hq), -np.inf, dtype=np.float64)
     row_ids = range(R) if rows is None else rows
@@ -115,13 +121,14 @@ def split_bounds(k: int, num_splits: int):
     return [(min(k, s * c), min(k, (s + 1) * c)) for s in range(num_splits)]
 
 
-def gather_attention_splits(q_bits, K, V, topk, softmax_scale, num_splits: int, rows=None):
+def gather_attention_splits(q_bits, K, V, topk, softmax_scale, num_splits: int, rows=None, q_dtype: str = "bf16"):
     """Per-split normalised partials: o_part [R, P, Hq, D], lse_part [R, P, Hq]."""
     R, Hq, D = q_bits.shape
     o_part = np.zeros((R, num_splits, Hq, D), dtype=np.float64)
     lse_part = np.full((R, num_splits, Hq), -np.inf, dtype=np.float64)
     for s, (a, b) in enumerate(split_bounds(topk.shape[1], num_splits)):
-        o_s, l_s = gather_attention(q_bits, K, V, topk, softmax_scale, rows=rows, col_range=(a, b))
+        o_s, l_s = gather_attention(q_bits, K, V, topk, softmax_scale, rows=rows, col_range=(a, b),
+                                    q_dtype=q_dtype)
         o_part[:, s] = o_s
         lse_part[:, s] = l_s
     return o_part, lse_part

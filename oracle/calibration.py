@@ -9,8 +9,8 @@ in the subnormal range [2^-9, 2^-6).
 [E4M3-PR §Implementation scope] The statistics are per layer and per tensor.
 
 Readings (the pages do not define the statistics further):
-  * Inputs are bf16 values, widened exactly to fp32. Infinite and NaN inputs are counted
-    apart and take part in nothing else.
+  * Inputs are bf16 (or fp16) values, widened exactly to fp32. Infinite and NaN inputs are
+    counted apart and take part in nothing else.
   * max-abs, p99.9 and p99.99 are order statistics of |x| over the finite elements. A
     percentile is the nearest rank: with the finite magnitudes sorted ascending
     a_1 <= ... <= a_N, p_q = a_ceil(q N), q = 999/1000 or 9999/10000 taken as exact
@@ -35,16 +35,20 @@ E4M3_MAX = np.float32(448.0)
 MIN_SUBNORMAL = np.float32(2.0 ** -9)
 MIN_NORMAL = np.float32(2.0 ** -6)
 SATURATION_EDGE = np.float32(464.0)  # midpoint of 448 and 480 on the continued E4M3 grid
-NUM_BINS = 1 << 15  # bf16 magnitudes: the 15 bits below the sign
+NUM_BINS = 1 << 15  # 16-bit magnitudes: the 15 bits below the sign
 
 
-def _f32(bits: np.ndarray) -> np.ndarray:
+def _f32(bits: np.ndarray, dtype: str) -> np.ndarray:
     b = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
-    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    if dtype == "f16":
+        return b.view(np.float16).astype(np.float32)
+    if dtype == "bf16":
+        return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    raise ValueError(f"unknown activation type {dtype!r}")
 
 
 def magnitude_histogram(x_bits: np.ndarray) -> np.ndarray:
-    """Counts of each bf16 magnitude bit pattern (bits & 0x7FFF): int64 [32768]."""
+    """Counts of each 16-bit magnitude bit pattern (bits & 0x7FFF): int64 [32768]."""
     b = np.ascontiguousarray(x_bits, dtype=np.uint16).ravel()
     return np.bincount((b & np.uint16(0x7FFF)).astype(np.int64), minlength=NUM_BINS).astype(np.int64)
 
@@ -58,9 +62,9 @@ def nearest_rank(sorted_values: np.ndarray, num: int, den: int):
     return np.float32(sorted_values[max(rank, 1) - 1])
 
 
-def calibration_stats(x_bits: np.ndarray, scale=None) -> dict:
-    """Statistics of one tensor given as bf16 bit patterns (any shape)."""
-    x = _f32(x_bits)
+def calibration_stats(x_bits: np.ndarray, scale=None, dtype: str = "bf16") -> dict:
+    """Statistics of one tensor given as bf16 (or fp16, dtype='f16') bit patterns (any shape)."""
+    x = _f32(x_bits, dtype)
     finite = np.isfinite(x)
     a = np.abs(x[finite]).astype(np.float32)
     a_sorted = np.sort(a)

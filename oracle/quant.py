@@ -40,6 +40,24 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Widen IEEE half bit patterns (uint16) to float32. Exact: every half is a float32."""
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def act_bits_to_f32(bits: np.ndarray, dtype: str = "bf16") -> np.ndarray:
+    """Widen 16-bit activations of the given type ('bf16' or 'f16') to float32, exactly.
+
+    [E4M3-PR §Purpose: the first validated contract runs FP16 activations] -- the same quantisers apply to
+    fp16 K/V; only the widening differs.
+    """
+    if dtype == "bf16":
+        return bf16_bits_to_f32(bits)
+    if dtype == "f16":
+        return f16_bits_to_f32(bits)
+    raise ValueError(f"unknown activation type {dtype!r}")
+
+
 # --------------------------------------------------------------------------- int8
 
 def int8_quantize(x: np.ndarray):
@@ -68,16 +86,17 @@ def int8_inline_records(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
     return rec
 
 
-def write_int8(k_bits, v_bits, slot_mapping, num_slots: int, layout: str):
+def write_int8(k_bits, v_bits, slot_mapping, num_slots: int, layout: str, dtype: str = "bf16"):
     """Quantise the tokens' K and V heads and store them in a fresh, zeroed slot pool.
 
-    k_bits, v_bits: uint16 bf16 [T, Hkv, D]; slot_mapping: int [T], -1 skips the token.
+    k_bits, v_bits: uint16 bf16 (or fp16, dtype='f16') [T, Hkv, D]; slot_mapping: int [T],
+    -1 skips the token.
     layout 'side' returns (k_codes, v_codes, k_scale, v_scale) with codes int8 [S, Hkv, D]
     and scales fp32 [S, Hkv]; 'inline' returns (k_records, v_records) uint8 [S, Hkv, D + 4].
     """
     T, H, D = k_bits.shape
-    kc, ks = int8_quantize(bf16_bits_to_f32(k_bits))
-    vc, vs = int8_quantize(bf16_bits_to_f32(v_bits))
+    kc, ks = int8_quantize(act_bits_to_f32(k_bits, dtype))
+    vc, vs = int8_quantize(act_bits_to_f32(v_bits, dtype))
     sm = np.asarray(slot_mapping, dtype=np.int64)
     take = sm >= 0
     dst = sm[take]
@@ -146,9 +165,9 @@ def e4m3_encode(y: np.ndarray) -> np.ndarray:
     return (code | sign).astype(np.uint8)
 
 
-def e4m3_calibrated_scale(x_bits: np.ndarray) -> np.float32:
-    """Per-layer, per-tensor scale = amax / 448 in fp32 over bf16 values (the max envelope)."""
-    amax = np.max(np.abs(bf16_bits_to_f32(x_bits)))
+def e4m3_calibrated_scale(x_bits: np.ndarray, dtype: str = "bf16") -> np.float32:
+    """Per-layer, per-tensor scale = amax / 448 in fp32 over 16-bit values (the max envelope)."""
+    amax = np.max(np.abs(act_bits_to_f32(x_bits, dtype)))
     return np.float32(np.float32(amax) / np.float32(E4M3_MAX))
 
 
@@ -159,14 +178,14 @@ def e4m3_quantize(x: np.ndarray, scale) -> np.ndarray:
     return e4m3_encode(y)
 
 
-def write_e4m3(k_bits, v_bits, slot_mapping, num_slots: int, k_scale, v_scale):
+def write_e4m3(k_bits, v_bits, slot_mapping, num_slots: int, k_scale, v_scale, dtype: str = "bf16"):
     """Quantise K and V with their per-layer scales into a fresh, zeroed E4M3 slot pool.
 
-    Returns (k_cache, v_cache) uint8 [S, Hkv, D].
+    k_bits, v_bits: uint16 bf16 (or fp16, dtype='f16'). Returns (k_cache, v_cache) uint8 [S, Hkv, D].
     """
     T, H, D = k_bits.shape
-    kq = e4m3_quantize(bf16_bits_to_f32(k_bits), k_scale)
-    vq = e4m3_quantize(bf16_bits_to_f32(v_bits), v_scale)
+    kq = e4m3_quantize(act_bits_to_f32(k_bits, dtype), k_scale)
+    vq = e4m3_quantize(act_bits_to_f32(v_bits, dtype), v_scale)
     sm = np.asarray(slot_mapping, dtype=np.int64)
     take = sm >= 0
     k_cache = np.zeros((num_slots, H, D), dtype=np.uint8)
@@ -177,7 +196,7 @@ def write_e4m3(k_bits, v_bits, slot_mapping, num_slots: int, k_scale, v_scale):
 
 
 def write_bf16(k_bits, v_bits, slot_mapping, num_slots: int):
-    """Unquantised bf16 pool: the tokens' bits copied to their slots."""
+    """Unquantised 16-bit pool (bf16, or fp16 bits alike): the tokens' bits copied to their slots."""
     T, H, D = k_bits.shape
     sm = np.asarray(slot_mapping, dtype=np.int64)
     take = sm >= 0
