@@ -27,6 +27,10 @@
  *       QKV_INT8_INLINE K, V: bytes [S, H, D + 4]: D int8 codes then the fp32 scale,
  *                       little-endian (the 260 B record of [INT8-PR])
  *       QKV_E4M3        K, V: E4M3 bytes [S, H, D]; one fp32 K and one fp32 V scale per layer
+ *       QKV_F16         K, V: IEEE half [S, H, D] (the unquantised cache of the FP16-activation
+ *                       contract; gathered by qsa_gather_attn_f16 only)
+ *   - Activations (q and new K/V tokens) are bf16; the *_f16 entry points take IEEE half
+ *     instead, for the FP16-activation contract of [E4M3-PR §Purpose]. Widening is exact either way.
  */
 #ifndef QKV_H
 #define QKV_H
@@ -50,7 +54,8 @@ typedef enum {
   QKV_BF16 = 0,
   QKV_INT8_SIDE = 1,
   QKV_INT8_INLINE = 2,
-  QKV_E4M3 = 3
+  QKV_E4M3 = 3,
+  QKV_F16 = 4 /* unquantised IEEE-half pool; only with an fp16 query (qsa_gather_attn_f16) */
 } qkv_format;
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -99,6 +104,22 @@ qkv_status qkv_write_e4m3(const void* k, const void* v, int64_t num_tokens, int 
                           int64_t num_slots, uint32_t* dev_status, void* stream);
 
 /*
+ * qkv_write_int8_f16, qkv_write_e4m3_f16 -- the same writes from IEEE-half tokens (k, v fp16
+ * [num_tokens, num_kv_heads, head_dim]) for the FP16-activation contract [E4M3-PR §Purpose].
+ * Each half widens exactly to fp32, so the arithmetic, the stored bytes and every other
+ * argument are those of qkv_write_int8 / qkv_write_e4m3.
+ */
+qkv_status qkv_write_int8_f16(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                              int head_dim, int64_t token_stride, const int64_t* slot_mapping,
+                              qkv_format layout, void* k_cache, void* v_cache, float* k_scale,
+                              float* v_scale, int64_t num_slots, uint32_t* dev_status,
+                              void* stream);
+qkv_status qkv_write_e4m3_f16(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
+                              int head_dim, int64_t token_stride, const int64_t* slot_mapping,
+                              void* k_cache, void* v_cache, float k_scale, float v_scale,
+                              int64_t num_slots, uint32_t* dev_status, void* stream);
+
+/*
  * qkv_e4m3_calibrate -- per-tensor calibrated E4M3 scale = (max |x|) / 448 over n bf16
  * values, computed on the device.                             [SCALES §Calibration]
  *   x          bf16 [n], 16 B-aligned.
@@ -116,10 +137,10 @@ qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, flo
  *                        scale is part of this contract: nonzero elements below E4M3's
  *                        smallest subnormal 2^-9 and in the subnormal band below 2^-6]
  *
- * qkv_calib_histogram adds the counts of the bf16 magnitudes (bits & 0x7FFF) of x to hist.
+ * qkv_calib_histogram adds the counts of the 16-bit magnitudes (bits & 0x7FFF) of x to hist.
  * Calls accumulate, so one histogram can cover a tensor seen over many steps; zero hist
  * before the first call. A bf16 magnitude has 15 bits, so the histogram is exact.
- *   x      bf16 [n], 16 B-aligned (n may be 0; n <= 2^40).
+ *   x      bf16 (or IEEE half) [n], 16 B-aligned (n may be 0; n <= 2^40).
  *   hist   uint64 [QKV_CALIB_BINS], 8 B-aligned, owned by the caller.
  *
  * qkv_calib_stats reads a histogram and writes one qkv_calib_summary record (device memory):
@@ -156,6 +177,9 @@ typedef struct {
 
 qkv_status qkv_calib_histogram(const void* x, int64_t n, uint64_t* hist, void* stream);
 qkv_status qkv_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream);
+/* The same for a histogram of IEEE-half values (the histogram call counts 15-bit magnitudes of
+ * either type; only the bins' values differ). */
+qkv_status qkv_calib_stats_f16(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream);
 
 /*
  * qsa_gather_attn -- top-k gather decode attention over a quantized slot pool.
@@ -172,7 +196,7 @@ qkv_status qkv_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary*
  *   qsa_splitk_merge (pass v_scale_layer as its v_scale_post).
  *
  *   q             bf16 [rows, num_q_heads, head_dim], contiguous, 16 B-aligned.
- *   fmt           pool layout (see above). k_cache / v_cache base pointers 16 B-aligned.
+ *   fmt           pool layout (see above); QKV_F16 is QKV_ERR_ARG here (qsa_gather_attn_f16). k_cache / v_cache base pointers 16 B-aligned.
  *                 S * num_kv_heads must stay <= 2^31 - 1 (else QKV_ERR_UNSUPPORTED).
  *   k_scale_tok, v_scale_tok  fp32 [S, H] for QKV_INT8_SIDE, else must be NULL.
  *   k_scale_layer, v_scale_layer  per-layer scales for QKV_E4M3 (finite, > 0, else
@@ -195,6 +219,21 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
                            int64_t num_slots, const int32_t* topk_idx, int topk,
                            float softmax_scale, int num_splits, float* out, float* lse,
                            float* o_part, float* lse_part, uint32_t* dev_status, void* stream);
+
+/*
+ * qsa_gather_attn_f16 -- qsa_gather_attn with an IEEE-half query, for the FP16-activation
+ * contract [E4M3-PR §Purpose]. q fp16 [rows, num_q_heads, head_dim]; fmt one of
+ * QKV_INT8_SIDE, QKV_INT8_INLINE, QKV_E4M3 or QKV_F16 (a half pool); QKV_BF16 is
+ * QKV_ERR_ARG (a bf16 pool takes a bf16 query). Everything else -- splits, outputs, errors --
+ * as qsa_gather_attn.
+ */
+qkv_status qsa_gather_attn_f16(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                               int head_dim, qkv_format fmt, const void* k_cache,
+                               const void* v_cache, const float* k_scale_tok,
+                               const float* v_scale_tok, float k_scale_layer, float v_scale_layer,
+                               int64_t num_slots, const int32_t* topk_idx, int topk,
+                               float softmax_scale, int num_splits, float* out, float* lse,
+                               float* o_part, float* lse_part, uint32_t* dev_status, void* stream);
 
 /*
  * qsa_splitk_merge -- merge split-K partials.      [HOIST-PR §Changes: the V scale is

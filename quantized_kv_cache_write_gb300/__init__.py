@@ -19,11 +19,12 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libqkv.so")
 
 QKV_OK, QKV_ERR_ARG, QKV_ERR_SCALE, QKV_ERR_UNSUPPORTED, QKV_ERR_ALIGN, QKV_ERR_CUDA = range(6)
-QKV_BF16, QKV_INT8_SIDE, QKV_INT8_INLINE, QKV_E4M3 = range(4)
+QKV_BF16, QKV_INT8_SIDE, QKV_INT8_INLINE, QKV_E4M3, QKV_F16 = range(5)
 QKV_DEV_BAD_SLOT = 1
 QKV_DEV_BAD_INDEX = 2
 HEAD_DIM = 256
-FORMATS = {"bf16": QKV_BF16, "int8_side": QKV_INT8_SIDE, "int8_inline": QKV_INT8_INLINE, "e4m3": QKV_E4M3}
+FORMATS = {"bf16": QKV_BF16, "int8_side": QKV_INT8_SIDE, "int8_inline": QKV_INT8_INLINE, "e4m3": QKV_E4M3,
+           "f16": QKV_F16}
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python quantized_kv_cache_write_gb300/build.py`")
@@ -34,15 +35,20 @@ _p, _i64, _i32, _f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_f
 _SIGS = {
     "qkv_write_int8": [_p, _p, _i64, _i32, _i32, _i64, _p, _i32, _p, _p, _p, _p, _i64, _p, _p],
     "qkv_write_e4m3": [_p, _p, _i64, _i32, _i32, _i64, _p, _p, _p, _f32, _f32, _i64, _p, _p],
+    "qkv_write_int8_f16": [_p, _p, _i64, _i32, _i32, _i64, _p, _i32, _p, _p, _p, _p, _i64, _p, _p],
+    "qkv_write_e4m3_f16": [_p, _p, _i64, _i32, _i32, _i64, _p, _p, _p, _f32, _f32, _i64, _p, _p],
     "qkv_e4m3_calibrate": [_p, _i64, _p, _p, _p],
     "qkv_calib_histogram": [_p, _i64, _p, _p],
     "qkv_calib_stats": [_p, _f32, _p, _p],
+    "qkv_calib_stats_f16": [_p, _f32, _p, _p],
     "qsa_gather_attn": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
                         _i32, _p, _p, _p, _p, _p, _p],
     "qsa_splitk_merge": [_p, _p, _i64, _i32, _i32, _i32, _f32, _p, _p, _p],
     "qsa_suggest_num_splits": [_i32, _i64, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int)],
     "qsa_gather_attn_splitk_noalloc": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p,
                                        _i32, _f32, _i32, _p, _p, _p, _p],
+    "qsa_gather_attn_f16": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
+                            _i32, _p, _p, _p, _p, _p, _p],
     "qsa_gather_attn_splitk_fused": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32,
                                      _f32, _i32, _p, _p, _p, _p, _p, _p, _p],
     "qsa_gather_attn_paged": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i64, _i32,
@@ -83,10 +89,13 @@ def _check(fn: str, status: int):
         raise QKVError(fn, status)
 
 
+_ACT16 = (torch.bfloat16, torch.float16)
+
+
 def _tokens(k: torch.Tensor, v: torch.Tensor):
     """[T, Hkv, D] views sharing one token stride; heads and dims contiguous."""
-    if k.dim() != 3 or k.shape != v.shape or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
-        raise ValueError("k and v must be bf16 [num_tokens, num_kv_heads, head_dim] of equal shape")
+    if k.dim() != 3 or k.shape != v.shape or k.dtype not in _ACT16 or v.dtype != k.dtype:
+        raise ValueError("k and v must be bf16 (or both fp16) [num_tokens, num_kv_heads, head_dim] of equal shape")
     if k.stride(2) != 1 or k.stride(1) != k.shape[2] or v.stride()[1:] != k.stride()[1:] or k.stride(0) != v.stride(0):
         raise ValueError("k and v need contiguous heads and one shared token stride")
     return k.shape[0], k.shape[1], k.shape[2], k.stride(0)
@@ -94,21 +103,23 @@ def _tokens(k: torch.Tensor, v: torch.Tensor):
 
 def qkv_write_int8(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None, *,
                    layout: int = QKV_INT8_SIDE, dev_status=None, stream=None):
-    """int8 per-(token, head) quantize-on-write (side scales or inline 260 B records)."""
+    """int8 per-(token, head) quantize-on-write (side scales or inline 260 B records); bf16 or fp16 tokens."""
     T, H, D, stride = _tokens(k, v)
-    st = lib.qkv_write_int8(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), layout, _ptr(k_cache),
+    name = "qkv_write_int8_f16" if k.dtype == torch.float16 else "qkv_write_int8"
+    st = getattr(lib, name)(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), layout, _ptr(k_cache),
                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), k_cache.shape[0], _ptr(dev_status),
                             _stream(stream))
-    _check("qkv_write_int8", st)
+    _check(name, st)
 
 
 def qkv_write_e4m3(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale: float, *,
                    dev_status=None, stream=None):
-    """FP8 E4M3 quantize-on-write with calibrated per-layer scales."""
+    """FP8 E4M3 quantize-on-write with calibrated per-layer scales; bf16 or fp16 tokens."""
     T, H, D, stride = _tokens(k, v)
-    st = lib.qkv_write_e4m3(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+    name = "qkv_write_e4m3_f16" if k.dtype == torch.float16 else "qkv_write_e4m3"
+    st = getattr(lib, name)(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                             float(k_scale), float(v_scale), k_cache.shape[0], _ptr(dev_status), _stream(stream))
-    _check("qkv_write_e4m3", st)
+    _check(name, st)
 
 
 def qkv_e4m3_calibrate(x, amax_bits, scale_out, *, stream=None):
@@ -125,23 +136,27 @@ _CALIB_VALUES = ("amax", "p99_9", "p99_99", "scale")
 
 def qkv_calib_histogram(x, hist, *, stream=None):
     """Add the bf16 magnitude counts of x (any shape, contiguous) to hist (int64 [32768], device)."""
-    if x.dtype != torch.bfloat16 or not x.is_contiguous():
-        raise ValueError("x must be a contiguous bf16 tensor")
+    if x.dtype not in _ACT16 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous bf16 or fp16 tensor")
     if hist.numel() != CALIB_BINS or hist.element_size() != 8:
         raise ValueError(f"hist must hold {CALIB_BINS} 64-bit counts")
     st = lib.qkv_calib_histogram(_ptr(x), x.numel(), _ptr(hist), _stream(stream))
     _check("qkv_calib_histogram", st)
 
 
-def qkv_calib_stats(hist, stats, scale: float = 0.0, *, stream=None):
+def qkv_calib_stats(hist, stats, scale: float = 0.0, *, dtype=torch.bfloat16, stream=None):
     """Statistics of a histogram into stats (a 64-byte device buffer, e.g. int64 [8]).
 
-    scale 0 uses the calibrated amax / 448; read the record with decode_calib_stats.
+    scale 0 uses the calibrated amax / 448; dtype is the type the histogram counted (bf16 or
+    fp16); read the record with decode_calib_stats.
     """
     if stats.numel() * stats.element_size() < CALIB_STATS_BYTES:
         raise ValueError(f"stats must hold {CALIB_STATS_BYTES} bytes")
-    st = lib.qkv_calib_stats(_ptr(hist), float(scale), _ptr(stats), _stream(stream))
-    _check("qkv_calib_stats", st)
+    if dtype not in _ACT16:
+        raise ValueError("dtype must be torch.bfloat16 or torch.float16")
+    name = "qkv_calib_stats_f16" if dtype == torch.float16 else "qkv_calib_stats"
+    st = getattr(lib, name)(_ptr(hist), float(scale), _ptr(stats), _stream(stream))
+    _check(name, st)
 
 
 def decode_calib_stats(stats) -> dict:
@@ -172,16 +187,17 @@ def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: floa
                     num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
                     k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, num_splits: int = 1, out=None,
                     lse=None, o_part=None, lse_part=None, dev_status=None, stream=None):
-    """Top-k gather decode attention. q bf16 [R, Hq, D]; topk_idx int32 [R, k]."""
+    """Top-k gather decode attention. q bf16 (or fp16: qsa_gather_attn_f16) [R, Hq, D]; topk_idx int32 [R, k]."""
     _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
     R, Hq, D = q.shape
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_idx.shape[1] if topk_idx is not None else 0
-    st = lib.qsa_gather_attn(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
-                             _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer), float(v_scale_layer), S,
-                             _ptr(topk_idx), topk, float(softmax_scale), num_splits, _ptr(out), _ptr(lse),
-                             _ptr(o_part), _ptr(lse_part), _ptr(dev_status), _stream(stream))
-    _check("qsa_gather_attn", st)
+    name = "qsa_gather_attn_f16" if q.dtype == torch.float16 else "qsa_gather_attn"
+    st = getattr(lib, name)(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
+                            _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer), float(v_scale_layer), S,
+                            _ptr(topk_idx), topk, float(softmax_scale), num_splits, _ptr(out), _ptr(lse),
+                            _ptr(o_part), _ptr(lse_part), _ptr(dev_status), _stream(stream))
+    _check(name, st)
 
 
 def qsa_gather_attn_paged(q, fmt: int, k_cache, v_cache, block_table, row_seq, topk_pos, block_size: int,

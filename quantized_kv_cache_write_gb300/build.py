@@ -36,6 +36,10 @@ SOURCES = [
     "gather_paged_int8_inline.cu",
     "gather_paged_e4m3.cu",
     "gather_paged_bf16.cu",
+    "gather_f16q_int8_side.cu",
+    "gather_f16q_int8_inline.cu",
+    "gather_f16q_e4m3.cu",
+    "gather_f16q_f16.cu",
 ]
 HEADERS = ["qkv_internal.cuh", "gather_attn.cuh"]
 

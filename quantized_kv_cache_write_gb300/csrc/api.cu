@@ -45,10 +45,14 @@ const char* qkv_status_str(qkv_status s) {
   return "unknown status";
 }
 
-qkv_status qkv_write_int8(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
-                          int64_t token_stride, const int64_t* slot_mapping, qkv_format layout, void* k_cache,
-                          void* v_cache, float* k_scale, float* v_scale, int64_t num_slots, uint32_t* dev_status,
-                          void* stream) {
+}  // extern "C"
+
+namespace {
+
+qkv_status write_int8_impl(const void* k, const void* v, bool f16, int64_t num_tokens, int num_kv_heads,
+                           int head_dim, int64_t token_stride, const int64_t* slot_mapping, qkv_format layout,
+                           void* k_cache, void* v_cache, float* k_scale, float* v_scale, int64_t num_slots,
+                           uint32_t* dev_status, void* stream) {
   qkv_status st = check_write_inputs(k, v, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping,
                                      k_cache, v_cache, num_slots);
   if (st != QKV_OK) return st;
@@ -60,14 +64,15 @@ qkv_status qkv_write_int8(const void* k, const void* v, int64_t num_tokens, int 
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (!inl && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_write_int8(k, v, num_tokens, num_kv_heads, token_stride, slot_mapping, inl,
+  return cuda_status(qkv::launch_write_int8(k, v, f16, num_tokens, num_kv_heads, token_stride, slot_mapping, inl,
                                             k_cache, v_cache, k_scale, v_scale, num_slots, dev_status,
                                             static_cast<cudaStream_t>(stream)));
 }
 
-qkv_status qkv_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
-                          int64_t token_stride, const int64_t* slot_mapping, void* k_cache, void* v_cache,
-                          float k_scale, float v_scale, int64_t num_slots, uint32_t* dev_status, void* stream) {
+qkv_status write_e4m3_impl(const void* k, const void* v, bool f16, int64_t num_tokens, int num_kv_heads,
+                           int head_dim, int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
+                           void* v_cache, float k_scale, float v_scale, int64_t num_slots, uint32_t* dev_status,
+                           void* stream) {
   qkv_status st = check_write_inputs(k, v, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping,
                                      k_cache, v_cache, num_slots);
   if (st != QKV_OK) return st;
@@ -75,9 +80,44 @@ qkv_status qkv_write_e4m3(const void* k, const void* v, int64_t num_tokens, int 
   if (num_tokens == 0) return QKV_OK;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_write_e4m3(k, v, num_tokens, num_kv_heads, token_stride, slot_mapping, k_cache,
+  return cuda_status(qkv::launch_write_e4m3(k, v, f16, num_tokens, num_kv_heads, token_stride, slot_mapping, k_cache,
                                             v_cache, k_scale, v_scale, num_slots, dev_status,
                                             static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+qkv_status qkv_write_int8(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
+                          int64_t token_stride, const int64_t* slot_mapping, qkv_format layout, void* k_cache,
+                          void* v_cache, float* k_scale, float* v_scale, int64_t num_slots, uint32_t* dev_status,
+                          void* stream) {
+  return write_int8_impl(k, v, false, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping, layout,
+                         k_cache, v_cache, k_scale, v_scale, num_slots, dev_status, stream);
+}
+
+qkv_status qkv_write_int8_f16(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
+                              int64_t token_stride, const int64_t* slot_mapping, qkv_format layout, void* k_cache,
+                              void* v_cache, float* k_scale, float* v_scale, int64_t num_slots,
+                              uint32_t* dev_status, void* stream) {
+  return write_int8_impl(k, v, true, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping, layout,
+                         k_cache, v_cache, k_scale, v_scale, num_slots, dev_status, stream);
+}
+
+qkv_status qkv_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
+                          int64_t token_stride, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                          float k_scale, float v_scale, int64_t num_slots, uint32_t* dev_status, void* stream) {
+  return write_e4m3_impl(k, v, false, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping, k_cache,
+                         v_cache, k_scale, v_scale, num_slots, dev_status, stream);
+}
+
+qkv_status qkv_write_e4m3_f16(const void* k, const void* v, int64_t num_tokens, int num_kv_heads, int head_dim,
+                              int64_t token_stride, const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                              float k_scale, float v_scale, int64_t num_slots, uint32_t* dev_status,
+                              void* stream) {
+  return write_e4m3_impl(k, v, true, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping, k_cache,
+                         v_cache, k_scale, v_scale, num_slots, dev_status, stream);
 }
 
 qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out, void* stream) {
@@ -94,11 +134,25 @@ qkv_status qkv_calib_histogram(const void* x, int64_t n, uint64_t* hist, void* s
   return cuda_status(qkv::launch_calib_histogram(x, n, hist, static_cast<cudaStream_t>(stream)));
 }
 
-qkv_status qkv_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream) {
+}  // extern "C"
+
+namespace {
+qkv_status calib_stats_impl(const uint64_t* hist, bool f16, float scale, qkv_calib_summary* stats, void* stream) {
   if (!hist || !stats) return QKV_ERR_ARG;
   if (!(scale == 0.f || finite_positive(scale))) return QKV_ERR_SCALE;
   if (!aligned(hist, 8) || !aligned(stats, 8)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_calib_stats(hist, scale, stats, static_cast<cudaStream_t>(stream)));
+  return cuda_status(qkv::launch_calib_stats(hist, f16, scale, stats, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+extern "C" {
+
+qkv_status qkv_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream) {
+  return calib_stats_impl(hist, false, scale, stats, stream);
+}
+
+qkv_status qkv_calib_stats_f16(const uint64_t* hist, float scale, qkv_calib_summary* stats, void* stream) {
+  return calib_stats_impl(hist, true, scale, stats, stream);
 }
 
 }  // extern "C"
@@ -119,8 +173,11 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
                        const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
                        const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
                        float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream,
-                       const Paging* pg, uint32_t* counters = nullptr) {
+                       const Paging* pg, uint32_t* counters = nullptr, bool q_f16 = false) {
   if (rows < 0 || topk < 0 || num_splits < 1 || num_slots < 0) return QKV_ERR_ARG;
+  // a 16-bit pool is multiplied in its own type, so it needs a query of that type
+  if ((fmt == QKV_F16 && !q_f16) || (fmt == QKV_BF16 && q_f16)) return QKV_ERR_ARG;
+  if (q_f16 && pg != nullptr) return QKV_ERR_ARG;
   if (pg != nullptr) {
     if (pg->num_seqs < 1 || pg->max_blocks < 1 || pg->block_size < 1) return QKV_ERR_ARG;
     if (static_cast<int64_t>(pg->max_blocks) * pg->block_size > INT32_MAX) return QKV_ERR_ARG;
@@ -128,7 +185,8 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   }
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return QKV_ERR_ARG;
   if (head_dim != kHeadDim || num_q_heads / num_kv_heads > kMaxGroup) return QKV_ERR_UNSUPPORTED;
-  if (fmt != QKV_BF16 && fmt != QKV_INT8_SIDE && fmt != QKV_INT8_INLINE && fmt != QKV_E4M3) return QKV_ERR_ARG;
+  if (fmt != QKV_BF16 && fmt != QKV_INT8_SIDE && fmt != QKV_INT8_INLINE && fmt != QKV_E4M3 && fmt != QKV_F16)
+    return QKV_ERR_ARG;
   if (!std::isfinite(softmax_scale)) return QKV_ERR_ARG;
   if (fmt == QKV_E4M3 && (!finite_positive(k_scale_layer) || !finite_positive(v_scale_layer)))
     return QKV_ERR_SCALE;
@@ -197,6 +255,15 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
     }
     return QKV_ERR_ARG;
   }
+  if (q_f16) {
+    switch (fmt) {
+      case QKV_INT8_SIDE: return cuda_status(qkv::launch_gather_f16q_int8_side(a, s));
+      case QKV_INT8_INLINE: return cuda_status(qkv::launch_gather_f16q_int8_inline(a, s));
+      case QKV_E4M3: return cuda_status(qkv::launch_gather_f16q_e4m3(a, s));
+      case QKV_F16: return cuda_status(qkv::launch_gather_f16q_f16(a, s));
+      default: return QKV_ERR_ARG;
+    }
+  }
   switch (fmt) {
     case QKV_BF16: return cuda_status(qkv::launch_gather_bf16(a, s));
     case QKV_INT8_SIDE: return cuda_status(qkv::launch_gather_int8_side(a, s));
@@ -218,6 +285,17 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
   return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
                      k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, num_splits, out, lse,
                      o_part, lse_part, dev_status, stream, nullptr);
+}
+
+qkv_status qsa_gather_attn_f16(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
+                               qkv_format fmt, const void* k_cache, const void* v_cache, const float* k_scale_tok,
+                               const float* v_scale_tok, float k_scale_layer, float v_scale_layer,
+                               int64_t num_slots, const int32_t* topk_idx, int topk, float softmax_scale,
+                               int num_splits, float* out, float* lse, float* o_part, float* lse_part,
+                               uint32_t* dev_status, void* stream) {
+  return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
+                     k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, num_splits, out, lse,
+                     o_part, lse_part, dev_status, stream, nullptr, nullptr, true);
 }
 
 qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
@@ -259,7 +337,8 @@ qkv_status qsa_suggest_num_splits(qkv_format fmt, int64_t rows, int num_q_heads,
   int per_sm = 0;
   cudaError_t e = cudaErrorInvalidValue;
   switch (fmt) {
-    case QKV_BF16: e = qkv::gather_ctas_per_sm_bf16(&per_sm); break;
+    case QKV_BF16:
+    case QKV_F16: e = qkv::gather_ctas_per_sm_bf16(&per_sm); break;  // the same 16-bit ring
     case QKV_INT8_SIDE: e = qkv::gather_ctas_per_sm_int8_side(&per_sm); break;
     case QKV_INT8_INLINE: e = qkv::gather_ctas_per_sm_int8_inline(&per_sm); break;
     case QKV_E4M3: e = qkv::gather_ctas_per_sm_e4m3(&per_sm); break;

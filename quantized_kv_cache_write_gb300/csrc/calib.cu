@@ -1,5 +1,6 @@
-// Calibration statistics of one K or V tensor: an exact magnitude histogram of its bf16
-// values, accumulated over any number of calls, then the statistics read from it.
+// Calibration statistics of one K or V tensor: an exact magnitude histogram of its 16-bit
+// values (bf16, or IEEE half for the FP16-activation contract), accumulated over any number of
+// calls, then the statistics read from it.
 //
 // Pages: "Qwen3.8 Flash Next NVFP4 QSA FP8 E4M3 KV Scales" §Calibration (scale = max
 // envelope / 448; max-abs, p99.9, p99.99 and saturation per tensor); "[Model][SM70][FP8] Add
@@ -7,7 +8,7 @@
 // scale, nonzero elements below E4M3's smallest subnormal 2^-9 and in the subnormal band
 // below 2^-6) and §Implementation scope (per-layer, per-tensor statistics).
 //
-// A bf16 magnitude is 15 bits, so 32768 bins of (bits & 0x7FFF) hold the tensor's
+// A bf16 or half magnitude is 15 bits, so 32768 bins of (bits & 0x7FFF) hold the tensor's
 // magnitudes exactly, and every statistic is an exact function of the histogram: order
 // statistics by prefix sums, and the scaled-magnitude counts by classifying each bin's value
 // (one fp32 IEEE division per bin, the same division an element would get).
@@ -24,7 +25,9 @@ namespace {
 
 constexpr int kBins = QKV_CALIB_BINS;
 constexpr int kHistThreads = 1024;
-constexpr uint32_t kFirstNonfinite = 0x7F80u;  // bf16 magnitude bits of +inf; above: NaN
+// magnitude bits of +inf (above: NaN): bf16 0x7F80, IEEE half 0x7C00
+template <bool F16>
+__device__ __forceinline__ uint32_t first_nonfinite() { return F16 ? 0x7C00u : 0x7F80u; }
 constexpr int64_t kMaxPerCta = int64_t(1) << 31;  // keeps every shared count below 2^32
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
@@ -97,10 +100,16 @@ __device__ __forceinline__ unsigned long long block_scan(unsigned long long v, u
   return v + before;
 }
 
-__device__ __forceinline__ float bin_value(uint32_t b) { return __uint_as_float(b << 16); }
+// the value of a magnitude bin (bf16, or IEEE half when F16), exactly
+template <bool F16>
+__device__ __forceinline__ float bin_value(uint32_t b) {
+  return F16 ? __half2float(__ushort_as_half(static_cast<unsigned short>(b))) : __uint_as_float(b << 16);
+}
 
+template <bool F16>
 __global__ void __launch_bounds__(1024) calib_stats_kernel(const unsigned long long* __restrict__ hist, float scale_in,
                                                            qkv_calib_summary* __restrict__ out) {
+  const uint32_t kFirstNonfinite = first_nonfinite<F16>();
   __shared__ unsigned long long sw[32];
   __shared__ float s_p[2];
   __shared__ uint32_t s_top;
@@ -136,12 +145,12 @@ __global__ void __launch_bounds__(1024) calib_stats_kernel(const unsigned long l
       const unsigned long long c = hist[b0 + j];
       const unsigned long long prev = run;
       run += c;
-      if (c != 0ull && prev < r999 && run >= r999) s_p[0] = bin_value(b0 + j);
-      if (c != 0ull && prev < r9999 && run >= r9999) s_p[1] = bin_value(b0 + j);
+      if (c != 0ull && prev < r999 && run >= r999) s_p[0] = bin_value<F16>(b0 + j);
+      if (c != 0ull && prev < r9999 && run >= r9999) s_p[1] = bin_value<F16>(b0 + j);
     }
   }
   __syncthreads();
-  const float amax = s_top ? bin_value(s_top - 1u) : 0.f;
+  const float amax = s_top ? bin_value<F16>(s_top - 1u) : 0.f;
   const float scale = scale_in > 0.f ? scale_in : __fdiv_rn(amax, 448.0f);
   // scaled-magnitude classes; a zero scale (an all-zero tensor) leaves them at 0
   unsigned long long below = 0, sub = 0, sat = 0;
@@ -152,7 +161,7 @@ __global__ void __launch_bounds__(1024) calib_stats_kernel(const unsigned long l
       const uint32_t b = b0 + j;
       const unsigned long long c = hist[b];
       if (c == 0ull) continue;
-      const float y = __fdiv_rn(bin_value(b), scale);
+      const float y = __fdiv_rn(bin_value<F16>(b), scale);
       if (b != 0u && y < kSub) below += c;
       if (y >= kSub && y < kNorm) sub += c;
       if (y > kSat) sat += c;
@@ -213,8 +222,10 @@ cudaError_t launch_calib_histogram(const void* x, int64_t n, uint64_t* hist, cud
   return cudaGetLastError();
 }
 
-cudaError_t launch_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, cudaStream_t stream) {
-  calib_stats_kernel<<<1, 1024, 0, stream>>>(reinterpret_cast<const unsigned long long*>(hist), scale, stats);
+cudaError_t launch_calib_stats(const uint64_t* hist, bool f16, float scale, qkv_calib_summary* stats,
+                               cudaStream_t stream) {
+  auto kern = f16 ? calib_stats_kernel<true> : calib_stats_kernel<false>;
+  kern<<<1, 1024, 0, stream>>>(reinterpret_cast<const unsigned long long*>(hist), scale, stats);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,7 @@ constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kKeys = 16;  // keys per warp tile
 constexpr int kHeadsPerCta = 16;  // query heads per CTA: the M = 16 of the MMAs
+constexpr int kQkChains = 4;      // q.K^T accumulator chains per N-tile (one per 64 head dims)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kMaxFinite = 3.4028234663852886e38f;  // largest finite fp32
@@ -79,28 +80,40 @@ template <>
 struct Fmt<QKV_INT8_SIDE> {
   static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
   static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false, kNatural = true;
+  static constexpr bool kWide = false, kF16 = false;
 };
 template <>
 struct Fmt<QKV_INT8_INLINE> {
   static constexpr int kRowBytes = 272, kGlobalRow = kInlineRecord, kStages = 2, kMinBlocks = 2, kKShift = 16;
   static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false, kNatural = false;
+  static constexpr bool kWide = false, kF16 = false;
 };
 template <>
 struct Fmt<QKV_E4M3> {
   static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false, kNatural = true;
+  static constexpr bool kWide = false, kF16 = false;
 };
 template <>
 struct Fmt<QKV_BF16> {
   static constexpr int kRowBytes = 512, kGlobalRow = 512, kStages = 2, kMinBlocks = 1, kKShift = 16;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true, kNatural = false;
+  static constexpr bool kWide = true, kF16 = false;
+};
+// fp16 pool: the unquantised cache of the FP16-activation contract; moved like bf16 rows,
+// multiplied as fp16 (q must be fp16 too)
+template <>
+struct Fmt<QKV_F16> {
+  static constexpr int kRowBytes = 512, kGlobalRow = 512, kStages = 2, kMinBlocks = 1, kKShift = 16;
+  static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = false, kNatural = false;
+  static constexpr bool kWide = true, kF16 = true;
 };
 
 // V region i (rows i and i + 8) starts 16 B further along the bank cycle than a plain packing
-// would put it: by i chunks for 256 B rows, by 0, 0, 1, 1, 4, 4, 5, 5 chunks for bf16 rows.
+// would put it: by i chunks for 256 B rows, by 0, 0, 1, 1, 4, 4, 5, 5 chunks for 16-bit rows.
 template <int FMT>
 __host__ __device__ constexpr int v_region_shift(int i) {
-  return Fmt<FMT>::kBf16 ? 16 * ((((i >> 1) & 1)) | (((i >> 2) & 1) << 2)) : 16 * i;
+  return Fmt<FMT>::kWide ? 16 * ((((i >> 1) & 1)) | (((i >> 2) & 1) << 2)) : 16 * i;
 }
 
 // floats per head row of the merge buffer (one 128-dim half), chosen bank-conflict free for the
@@ -187,11 +200,15 @@ __device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
 // STAGES: depth of each warp's copy ring (tiles in flight); MINB: CTAs per SM the register
 // budget is sized for. The default (2, the format's) suits full-GPU launches; a deeper ring
 // with fewer CTAs per SM suits launches with too few CTAs to fill the GPU.
-template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks>
+// QF16: q is IEEE half instead of bf16 (the FP16-activation contract); it only changes how
+// the query is staged.
+template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks,
+          bool QF16 = false>
 __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const GatherArgs a) {
   using F = Fmt<FMT>;
   using L = Smem<FMT, STAGES>;
   static_assert(STAGES >= 2, "the ring needs a stage in flight while one is computed");
+  static_assert(!(F::kBf16 && QF16) && !(F::kF16 && !QF16), "a 16-bit pool takes a query of its own type");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int c = lane & 3, hn = lane >> 2;
@@ -414,16 +431,27 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     int sg = 0;
     if (!F::kBf16) {
       // fp16 operands: a power of two puts the head's largest |q| in [2^14, 2^15)
-      // packed bf16 |q| maximum over the thread's 32 dims (bf16 bits order like values when
-      // non-negative), then the larger half as fp32 bits
-      __nv_bfloat162 mh = __floats2bfloat162_rn(0.f, 0.f);
+      // packed |q| maximum over the thread's 32 dims (16-bit float bits order like values
+      // when non-negative), then the larger half as fp32 bits
+      uint32_t m;
+      if (QF16) {
+        __half2 mh = __floats2half2_rn(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t a16 = w[i] & 0x7FFF7FFFu;
-        mh = __hmax2(mh, *reinterpret_cast<const __nv_bfloat162*>(&a16));
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t a16 = w[i] & 0x7FFF7FFFu;
+          mh = __hmax2(mh, *reinterpret_cast<const __half2*>(&a16));
+        }
+        m = __float_as_uint(fmaxf(__low2float(mh), __high2float(mh)));
+      } else {
+        __nv_bfloat162 mh = __floats2bfloat162_rn(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t a16 = w[i] & 0x7FFF7FFFu;
+          mh = __hmax2(mh, *reinterpret_cast<const __nv_bfloat162*>(&a16));
+        }
+        const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mh);
+        m = max((mw & 0xFFFFu) << 16, mw & 0xFFFF0000u);
       }
-      const uint32_t mw = *reinterpret_cast<const uint32_t*>(&mh);
-      uint32_t m = max((mw & 0xFFFFu) << 16, mw & 0xFFFF0000u);
 #pragma unroll
       for (int off = 1; off <= 4; off <<= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
       sg = m ? max(-64, min(64, 14 - (static_cast<int>(m >> 23) - 127))) : 0;
@@ -445,8 +473,15 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
         if (F::kBf16) {
           v32 = b0 | (b1 << 16);
         } else {
-          float s0, s1;
-          f2unpack(f2mul(f2pack(__uint_as_float(b0 << 16), __uint_as_float(b1 << 16)), uu), s0, s1);
+          float s0, s1, x0, x1;
+          if (QF16) {
+            x0 = __half2float(__ushort_as_half(static_cast<unsigned short>(b0)));
+            x1 = __half2float(__ushort_as_half(static_cast<unsigned short>(b1)));
+          } else {
+            x0 = __uint_as_float(b0 << 16);
+            x1 = __uint_as_float(b1 << 16);
+          }
+          f2unpack(f2mul(f2pack(x0, x1), uu), s0, s1);
           v32 = pack_half2(s0, s1);
         }
         sts32(smem_u32(smem + L::kQ + q_off(blk * 4 + ks, qh, up * 8 + 2 * cc)), v32);
@@ -500,11 +535,16 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     const uint32_t sbase = smem_u32(sb);
     const uint32_t mask = (STAGES == 2) ? mask_cur : lds32(sbase + L::kStageMask);
 
-    // ---- q . K^T for this warp's 16 keys: one accumulator per N-tile (the two chains
-    //      interleave; splitting each further measured no faster)
-    float acc[2][4];
+    // ---- q . K^T for this warp's 16 keys
+    // kQkChains independent accumulator chains per N-tile (64-dim blocks dealt round-robin),
+    // added at the end: shorter chains of smaller partial sums round less. Outlier keys give
+    // logits of ~2^4.5 (log2 units) built from partial sums ~10x larger, so a near-tie of two
+    // outlier keys with opposite V values turns the dot product's rounding into output error.
+    float accc[kQkChains][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int ch = 0; ch < kQkChains; ++ch)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) accc[ch][nt][0] = accc[ch][nt][1] = accc[ch][nt][2] = accc[ch][nt][3] = 0.f;
     uint32_t rowK[2];
     int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
 #pragma unroll
@@ -518,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       uint32_t kw[2][8];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        if (F::kBf16) {
+        if (F::kWide) {
           const uint4 x = lds128(rowK[nt] + (8 * blk + 2 * c) * 16);
           const uint4 y = lds128(rowK[nt] + (8 * blk + 2 * c + 1) * 16);
           kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
@@ -543,14 +583,29 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           if (F::kBf16) {
-            mma_bf16(acc[nt], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
+            mma_bf16(accc[blk % kQkChains][nt], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
+          } else if (F::kF16) {
+            mma_f16(accc[blk % kQkChains][nt], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
           } else if (F::kInt8) {
-            mma_f16(acc[nt], qa, i8pair_to_f16x2(kw[nt][ks]), i8pair_to_f16x2(kw[nt][ks] >> 8));
+            mma_f16(accc[blk % kQkChains][nt], qa, i8pair_to_f16x2(kw[nt][ks]), i8pair_to_f16x2(kw[nt][ks] >> 8));
           } else {
-            mma_f16(acc[nt], qa, e4m3pair_to_f16x2(kw[nt][ks]), e4m3pair_to_f16x2(kw[nt][ks] >> 16));
+            mma_f16(accc[blk % kQkChains][nt], qa, e4m3pair_to_f16x2(kw[nt][ks]), e4m3pair_to_f16x2(kw[nt][ks] >> 16));
           }
         }
       }
+    }
+
+    float acc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      uint64_t a01 = f2pack(accc[0][nt][0], accc[0][nt][1]), a23 = f2pack(accc[0][nt][2], accc[0][nt][3]);
+#pragma unroll
+      for (int ch = 1; ch < kQkChains; ++ch) {
+        a01 = f2add(a01, f2pack(accc[ch][nt][0], accc[ch][nt][1]));
+        a23 = f2add(a23, f2pack(accc[ch][nt][2], accc[ch][nt][3]));
+      }
+      f2unpack(a01, acc[nt][0], acc[nt][1]);
+      f2unpack(a23, acc[nt][2], acc[nt][3]);
     }
 
     // ---- logits with the hoisted K scale; masked keys -> -inf
@@ -645,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     // ---- p = exp2(s - m): fp32 sums, hi + lo A fragments
     uint32_t pa[4], pl[4];
     {
-      const float pm = F::kInt8 ? pow2f(kPShift - eu) : (F::kE4m3 ? pow2f(kPShift) : 1.f);
+      const float pm = F::kInt8 ? pow2f(kPShift - eu) : (F::kBf16 ? 1.f : pow2f(kPShift));
       // a head whose max is still -inf has only masked (-inf) logits: subtracting the most
       // negative finite float instead gives exp2(-inf) = 0 rather than exp2(NaN)
       const float m0 = fmaxf(mu0, -kMaxFinite), m1 = fmaxf(mu1, -kMaxFinite);
@@ -736,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
               }
             }
           }
-        } else if (F::kBf16) {
+        } else if (F::kWide) {
           uint32_t vw[4][8];
 #pragma unroll
           for (int ri = 0; ri < 4; ++ri) {
@@ -842,9 +897,9 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     sL[warp * 16 + h0] = a0 + b0;
     sL[warp * 16 + h1] = a1 + b1;
   }
-  // the accumulators carry p times 2^(kPShift - eu) (int8) or 2^kPShift (E4M3); that power of
+  // the accumulators carry p times 2^(kPShift - eu) (int8) or 2^kPShift (E4M3, fp16); that power of
   // two is undone in the combine weights rather than on every accumulator value
-  if (lane == 0) sPost[warp] = F::kInt8 ? pow2f(eu - kPShift) : (F::kE4m3 ? pow2f(-kPShift) : 1.f);
+  if (lane == 0) sPost[warp] = F::kInt8 ? pow2f(eu - kPShift) : (F::kBf16 ? 1.f : pow2f(-kPShift));
   __syncthreads();
   // combine weights, once per CTA: thread (hh, part) owns head hh and a quarter of each half's
   // head dims; warp w's partial enters with exp2(m_w - M) 2^(its pre-scale) / l
@@ -987,7 +1042,7 @@ inline int64_t gather_grid(const GatherArgs& a) {
 }
 
 // Opt the kernel into its dynamic shared memory, once per device.
-template <int FMT, bool PAGED, int STAGES, int MINB>
+template <int FMT, bool PAGED, int STAGES, int MINB, bool QF16 = false>
 cudaError_t prepare_variant() {
   static bool attr_done[64] = {};
   int dev = 0;
@@ -995,13 +1050,13 @@ cudaError_t prepare_variant() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB>,
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Smem<FMT, STAGES>::kTotal));
     if (e != cudaSuccess) return e;
     // all of the unified L1 / shared array as shared memory: the copies bypass L1 anyway, and
     // the occupancy query then sees the CTAs per SM that a launch gets
-    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB>,
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16>,
                              cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -1009,13 +1064,20 @@ cudaError_t prepare_variant() {
   return cudaSuccess;
 }
 
-template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks>
+template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks,
+          bool QF16 = false>
 cudaError_t launch_variant(const GatherArgs& a, cudaStream_t stream) {
-  cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB>();
+  cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB, QF16>();
   if (e != cudaSuccess) return e;
-  gather_attn_kernel<FMT, PAGED, STAGES, MINB>
+  gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16>
       <<<static_cast<unsigned>(gather_grid(a)), kThreads, Smem<FMT, STAGES>::kTotal, stream>>>(a);
   return cudaGetLastError();
+}
+
+// The query is IEEE half (FP16-activation contract); default ring and occupancy.
+template <int FMT>
+cudaError_t launch_f16q(const GatherArgs& a, cudaStream_t stream) {
+  return launch_variant<FMT, false, Fmt<FMT>::kStages, Fmt<FMT>::kMinBlocks, true>(a, stream);
 }
 
 // CTAs of the default kernel of this layout that one SM holds at once: the smaller of its

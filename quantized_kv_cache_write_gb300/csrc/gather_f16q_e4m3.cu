@@ -1,0 +1,9 @@
+// Gather-attention instantiation for the QKV_E4M3 layout with an IEEE-half query (the
+// FP16-activation contract); one translation unit per layout so the kernels compile in parallel.
+#include "gather_attn.cuh"
+
+namespace qkv {
+cudaError_t launch_gather_f16q_e4m3(const GatherArgs& a, cudaStream_t stream) {
+  return gather::launch_f16q<QKV_E4M3>(a, stream);
+}
+}  // namespace qkv

@@ -1,0 +1,9 @@
+// Gather-attention instantiation for the QKV_INT8_INLINE layout with an IEEE-half query (the
+// FP16-activation contract); one translation unit per layout so the kernels compile in parallel.
+#include "gather_attn.cuh"
+
+namespace qkv {
+cudaError_t launch_gather_f16q_int8_inline(const GatherArgs& a, cudaStream_t stream) {
+  return gather::launch_f16q<QKV_INT8_INLINE>(a, stream);
+}
+}  // namespace qkv

@@ -16,25 +16,26 @@ constexpr int kMaxGroup = 128;  // GQA group; above 16 the gather runs one CTA p
 constexpr int kInlineRecord = kHeadDim + 4;  // 256 code bytes + fp32 scale
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_write_int8(const void* k, const void* v, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
                               void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                               int64_t num_slots, uint32_t* dev_status, cudaStream_t stream);
-cudaError_t launch_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
                               void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out,
                                   cudaStream_t stream);
 cudaError_t launch_calib_histogram(const void* x, int64_t n, uint64_t* hist, cudaStream_t stream);
-cudaError_t launch_calib_stats(const uint64_t* hist, float scale, qkv_calib_summary* stats, cudaStream_t stream);
+cudaError_t launch_calib_stats(const uint64_t* hist, bool f16, float scale, qkv_calib_summary* stats,
+                               cudaStream_t stream);
 cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
                                 int num_q_heads, int num_splits, float v_scale_post, float* out,
                                 float* lse, cudaStream_t stream);
 
 // Arguments of one gather-attention launch (already validated on the host).
 struct GatherArgs {
-  const __nv_bfloat16* q;
+  const __nv_bfloat16* q;  // bf16, or IEEE half bits for the fp16-query launchers
   const uint8_t* k_cache;
   const uint8_t* v_cache;
   const float* k_scale_tok;
@@ -74,6 +75,10 @@ cudaError_t launch_gather_paged_bf16(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_paged_int8_side(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_paged_int8_inline(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_paged_e4m3(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_f16q_int8_side(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_f16q_int8_inline(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_f16q_e4m3(const GatherArgs& a, cudaStream_t stream);
+cudaError_t launch_gather_f16q_f16(const GatherArgs& a, cudaStream_t stream);
 cudaError_t gather_ctas_per_sm_bf16(int* n);
 cudaError_t gather_ctas_per_sm_int8_side(int* n);
 cudaError_t gather_ctas_per_sm_int8_inline(int* n);

@@ -1,6 +1,7 @@
 // Quantize-on-write kernels: int8 per-(token, head) absmax/127 (side or inline scale
 // layout) and FP8 E4M3 with calibrated per-layer scales, plus the amax/448 calibration
-// reduction.
+// reduction. New tokens are bf16, or IEEE half for the FP16-activation contract of
+// "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache" §Purpose (exact widening either way).
 //
 // Pages: "int8 per-(token,head) KV cache for the Qwen3.8-Flash-Next QSA path" §The finding
 // worth upstreaming (per-(token,head) scale, 260 B inline record vs side tensor);
@@ -22,7 +23,9 @@ struct HeadVec {
   float x[8];
 };
 
-__device__ __forceinline__ HeadVec load_head8(const __nv_bfloat16* src) {
+// Eight consecutive 16-bit activations (bf16, or IEEE half when F16), widened exactly to fp32.
+template <bool F16>
+__device__ __forceinline__ HeadVec load_head8(const uint16_t* src) {
   // Streaming read: the new tokens are consumed once.
   uint4 raw;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
@@ -32,8 +35,14 @@ __device__ __forceinline__ HeadVec load_head8(const __nv_bfloat16* src) {
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    h.x[2 * i] = bf16lo(w[i]);
-    h.x[2 * i + 1] = bf16hi(w[i]);
+    if (F16) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+      h.x[2 * i] = f.x;
+      h.x[2 * i + 1] = f.y;
+    } else {
+      h.x[2 * i] = bf16lo(w[i]);
+      h.x[2 * i + 1] = bf16hi(w[i]);
+    }
   }
   return h;
 }
@@ -61,9 +70,9 @@ __device__ __forceinline__ bool decode_item(int64_t item, int num_heads, const i
   return true;
 }
 
-template <bool kInline>
+template <bool kInline, bool F16>
 __global__ void __launch_bounds__(kWriteThreads)
-    write_int8_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    write_int8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                       int64_t num_tokens, int num_heads, int64_t token_stride,
                       const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
                       uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
@@ -75,8 +84,8 @@ __global__ void __launch_bounds__(kWriteThreads)
   int h, is_v;
   if (!decode_item(item, num_heads, slot_mapping, num_slots, dev_status, lane, t, h, is_v, slot)) return;
 
-  const __nv_bfloat16* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * kHeadDim + lane * 8;
-  const HeadVec hv = load_head8(src);
+  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * kHeadDim + lane * 8;
+  const HeadVec hv = load_head8<F16>(src);
   float a = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(hv.x[i]));
@@ -106,8 +115,9 @@ __global__ void __launch_bounds__(kWriteThreads)
   }
 }
 
+template <bool F16>
 __global__ void __launch_bounds__(kWriteThreads)
-    write_e4m3_kernel(const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    write_e4m3_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                       int64_t num_tokens, int num_heads, int64_t token_stride,
                       const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
                       uint8_t* __restrict__ v_cache, float k_scale, float v_scale, int64_t num_slots,
@@ -119,8 +129,8 @@ __global__ void __launch_bounds__(kWriteThreads)
   int h, is_v;
   if (!decode_item(item, num_heads, slot_mapping, num_slots, dev_status, lane, t, h, is_v, slot)) return;
 
-  const __nv_bfloat16* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * kHeadDim + lane * 8;
-  const HeadVec hv = load_head8(src);
+  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * kHeadDim + lane * 8;
+  const HeadVec hv = load_head8<F16>(src);
   const float s = is_v ? v_scale : k_scale;
   uint32_t word[2] = {0u, 0u};
 #pragma unroll
@@ -174,34 +184,33 @@ unsigned write_blocks(int64_t num_tokens, int num_heads) {
 
 }  // namespace
 
-cudaError_t launch_write_int8(const void* k, const void* v, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
                               void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                               int64_t num_slots, uint32_t* dev_status, cudaStream_t stream) {
   const unsigned blocks = write_blocks(num_tokens, num_heads);
-  auto kk = static_cast<const __nv_bfloat16*>(k);
-  auto vv = static_cast<const __nv_bfloat16*>(v);
+  auto kk = static_cast<const uint16_t*>(k);
+  auto vv = static_cast<const uint16_t*>(v);
   auto kc = static_cast<uint8_t*>(k_cache);
   auto vc = static_cast<uint8_t*>(v_cache);
-  if (inline_layout)
-    write_int8_kernel<true><<<blocks, kWriteThreads, 0, stream>>>(kk, vv, num_tokens, num_heads, token_stride,
-                                                                  slot_mapping, kc, vc, nullptr, nullptr,
-                                                                  num_slots, dev_status);
-  else
-    write_int8_kernel<false><<<blocks, kWriteThreads, 0, stream>>>(kk, vv, num_tokens, num_heads, token_stride,
-                                                                   slot_mapping, kc, vc, k_scale, v_scale,
-                                                                   num_slots, dev_status);
+  float* ks = inline_layout ? nullptr : k_scale;
+  float* vs = inline_layout ? nullptr : v_scale;
+  auto kern = inline_layout ? (f16 ? write_int8_kernel<true, true> : write_int8_kernel<true, false>)
+                            : (f16 ? write_int8_kernel<false, true> : write_int8_kernel<false, false>);
+  kern<<<blocks, kWriteThreads, 0, stream>>>(kk, vv, num_tokens, num_heads, token_stride, slot_mapping, kc, vc, ks,
+                                             vs, num_slots, dev_status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_write_e4m3(const void* k, const void* v, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
                               void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream) {
-  write_e4m3_kernel<<<write_blocks(num_tokens, num_heads), kWriteThreads, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), num_tokens, num_heads,
-      token_stride, slot_mapping, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale,
-      v_scale, num_slots, dev_status);
+  auto kern = f16 ? write_e4m3_kernel<true> : write_e4m3_kernel<false>;
+  kern<<<write_blocks(num_tokens, num_heads), kWriteThreads, 0, stream>>>(
+      static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), num_tokens, num_heads, token_stride,
+      slot_mapping, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale, v_scale, num_slots,
+      dev_status);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,12 @@ def bf16_dev(bits: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
 
 
+def act_dev(bits: np.ndarray, act_dtype: str = "bf16") -> torch.Tensor:
+    """16-bit activation bits on the device as bf16 or fp16."""
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.view(torch.float16 if act_dtype == "f16" else torch.bfloat16).cuda()
+
+
 def assert_close(got: np.ndarray, ref: np.ndarray, what: str, atol=ATOL, rtol=RTOL):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -43,14 +49,15 @@ class GpuPool:
         import quantized_kv_cache_write_gb300 as q
         self.fmt = fmt
         self.code = q.FORMATS[fmt]
+        self.act = wl.act_dtype
         S, H, D = wl.num_slots, wl.num_kv_heads, wl.head_dim
-        self.k_tok = bf16_dev(wl.k_tokens)
-        self.v_tok = bf16_dev(wl.v_tokens)
+        self.k_tok = act_dev(wl.k_tokens, wl.act_dtype)
+        self.v_tok = act_dev(wl.v_tokens, wl.act_dtype)
         self.slots = torch.from_numpy(wl.slot_mapping).cuda()
         self.k_scale_tok = self.v_scale_tok = None
         self.k_scale_layer = self.v_scale_layer = 1.0
-        if fmt == "bf16":
-            self.k_cache = torch.zeros((S, H, D), dtype=torch.bfloat16, device="cuda")
+        if fmt in ("bf16", "f16"):
+            self.k_cache = torch.zeros((S, H, D), dtype=self.k_tok.dtype, device="cuda")
             self.v_cache = torch.zeros_like(self.k_cache)
             take = self.slots >= 0
             self.k_cache[self.slots[take]] = self.k_tok[take]
@@ -68,11 +75,14 @@ class GpuPool:
             q.qkv_write_int8(self.k_tok, self.v_tok, self.slots, self.k_cache, self.v_cache,
                              layout=q.QKV_INT8_INLINE, dev_status=dev_status)
         elif fmt == "e4m3":
-            amax = torch.zeros(1, dtype=torch.int32, device="cuda")
-            sc = torch.zeros(2, dtype=torch.float32, device="cuda")
-            q.qkv_e4m3_calibrate(self.k_tok, amax, sc[0:1])
-            q.qkv_e4m3_calibrate(self.v_tok, amax, sc[1:2])
-            ks, vs = sc.cpu().numpy()
+            if wl.act_dtype == "f16":  # the calibration statistics give amax / 448 for half tensors
+                ks, vs = (np.float32(_calibrated_scale_f16(t)) for t in (self.k_tok, self.v_tok))
+            else:
+                amax = torch.zeros(1, dtype=torch.int32, device="cuda")
+                sc = torch.zeros(2, dtype=torch.float32, device="cuda")
+                q.qkv_e4m3_calibrate(self.k_tok, amax, sc[0:1])
+                q.qkv_e4m3_calibrate(self.v_tok, amax, sc[1:2])
+                ks, vs = sc.cpu().numpy()
             self.k_scale_layer, self.v_scale_layer = np.float32(ks), np.float32(vs)
             self.k_cache = torch.zeros((S, H, D), dtype=torch.uint8, device="cuda")
             self.v_cache = torch.zeros_like(self.k_cache)
@@ -85,7 +95,7 @@ class GpuPool:
                dev_status=None):
         """Run qsa_gather_attn (and the merge when split). Returns out, lse (and partials)."""
         import quantized_kv_cache_write_gb300 as q
-        qd = bf16_dev(wl.q) if q_dev is None else q_dev
+        qd = act_dev(wl.q, wl.act_dtype) if q_dev is None else q_dev
         idx = torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda() if idx_dev is None else idx_dev
         R, Hq, D = qd.shape
         kw = dict(num_kv_heads=wl.num_kv_heads, num_slots=wl.num_slots, k_scale_tok=self.k_scale_tok,
@@ -111,33 +121,44 @@ class GpuPool:
         return out.cpu().numpy(), lse.cpu().numpy(), o_part.cpu().numpy(), lse_part.cpu().numpy()
 
 
+def _calibrated_scale_f16(x: torch.Tensor) -> float:
+    import quantized_kv_cache_write_gb300 as q
+    hist = torch.zeros(q.CALIB_BINS, dtype=torch.int64, device="cuda")
+    rec = torch.zeros(8, dtype=torch.int64, device="cuda")
+    q.qkv_calib_histogram(x.contiguous(), hist)
+    q.qkv_calib_stats(hist, rec, 0.0, dtype=torch.float16)
+    return q.decode_calib_stats(rec)["scale"]
+
+
 class OraclePool:
     """The same slot pool written and dequantised by the CPU oracle (fp64)."""
 
     def __init__(self, wl, fmt: str):
         S = wl.num_slots
         self.fmt = fmt
+        self.act = dt = wl.act_dtype
         self.k_scale_layer = self.v_scale_layer = None
-        if fmt == "bf16":
+        if fmt in ("bf16", "f16"):
             kc, vc = oq.write_bf16(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S)
-            self.K, self.V = oatt.bf16_pool_fp64(kc), oatt.bf16_pool_fp64(vc)
+            widen = oatt.f16_pool_fp64 if fmt == "f16" else oatt.bf16_pool_fp64
+            self.K, self.V = widen(kc), widen(vc)
             self.Vpart = self.V
             self.bytes = (kc, vc)
         elif fmt == "int8_side":
-            kc, vc, ks, vs = oq.write_int8(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S, "side")
+            kc, vc, ks, vs = oq.write_int8(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S, "side", dtype=dt)
             self.K, self.V = oatt.int8_side_pool_fp64(kc, ks), oatt.int8_side_pool_fp64(vc, vs)
             self.Vpart = self.V
             self.bytes = (kc, vc, ks, vs)
         elif fmt == "int8_inline":
-            kr, vr = oq.write_int8(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S, "inline")
+            kr, vr = oq.write_int8(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S, "inline", dtype=dt)
             self.K, self.V = oatt.int8_inline_pool_fp64(kr), oatt.int8_inline_pool_fp64(vr)
             self.Vpart = self.V
             self.bytes = (kr, vr)
         elif fmt == "e4m3":
-            ks = oq.e4m3_calibrated_scale(wl.k_tokens)
-            vs = oq.e4m3_calibrated_scale(wl.v_tokens)
+            ks = oq.e4m3_calibrated_scale(wl.k_tokens, dtype=dt)
+            vs = oq.e4m3_calibrated_scale(wl.v_tokens, dtype=dt)
             self.k_scale_layer, self.v_scale_layer = ks, vs
-            kc, vc = oq.write_e4m3(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S, ks, vs)
+            kc, vc = oq.write_e4m3(wl.k_tokens, wl.v_tokens, wl.slot_mapping, S, ks, vs, dtype=dt)
             self.K, self.V = oatt.e4m3_pool_fp64(kc, ks), oatt.e4m3_pool_fp64(vc, vs)
             self.Vpart = oatt.e4m3_pool_fp64(vc, vs, apply_scale=False)  # split partials: no V scale
             self.bytes = (kc, vc)
@@ -145,7 +166,8 @@ class OraclePool:
             raise ValueError(fmt)
 
     def attend(self, wl, rows=None):
-        return oatt.gather_attention(wl.q, self.K, self.V, wl.topk, wl.softmax_scale, rows=rows)
+        return oatt.gather_attention(wl.q, self.K, self.V, wl.topk, wl.softmax_scale, rows=rows, q_dtype=self.act)
 
     def attend_splits(self, wl, P, rows=None):
-        return oatt.gather_attention_splits(wl.q, self.K, self.Vpart, wl.topk, wl.softmax_scale, P, rows=rows)
+        return oatt.gather_attention_splits(wl.q, self.K, self.Vpart, wl.topk, wl.softmax_scale, P, rows=rows,
+                                            q_dtype=self.act)

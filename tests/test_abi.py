@@ -216,3 +216,20 @@ def test_suggest_num_splits_host_validation(lib):
     assert L.qsa_suggest_num_splits(E.QKV_INT8_SIDE, 40, 15, 2, 2048, ctypes.byref(out)) == E.QKV_ERR_ARG
     assert L.qsa_suggest_num_splits(E.QKV_INT8_SIDE, 40, 258, 2, 2048, ctypes.byref(out)) == E.QKV_ERR_UNSUPPORTED
     assert L.qsa_suggest_num_splits(7, 40, 16, 1, 2048, ctypes.byref(out)) == E.QKV_ERR_ARG
+
+
+def test_fp16_entry_points_host_validation(lib):
+    E, L = lib, lib.lib
+    g16 = lambda fmt, **o: L.qsa_gather_attn_f16(FAKE, o.get("rows", 4), 16, 1, 256, fmt, FAKE, FAKE,
+                                                  o.get("ks"), o.get("vs"), 1.0, 1.0, 100, FAKE, 8, 0.0625, 1,
+                                                  FAKE, None, None, None, None, None)
+    assert g16(E.QKV_BF16) == E.QKV_ERR_ARG  # a bf16 pool needs a bf16 query
+    assert g16(E.QKV_F16, rows=0) == E.QKV_OK
+    assert g16(E.QKV_INT8_SIDE, rows=0, ks=FAKE, vs=FAKE) == E.QKV_OK
+    assert g16(E.QKV_INT8_SIDE) == E.QKV_ERR_ARG  # side scales still required
+    assert _gather(lib, fmt=E.QKV_F16, ks=None, vs=None, rows=0) == E.QKV_ERR_ARG  # fp16 pool, bf16 query
+    w8 = L.qkv_write_int8_f16(FAKE, FAKE, 3, 1, 64, 256, FAKE, E.QKV_INT8_SIDE, FAKE, FAKE, FAKE, FAKE, 10, None, None)
+    assert w8 == E.QKV_ERR_UNSUPPORTED
+    we = L.qkv_write_e4m3_f16(FAKE, FAKE, 3, 1, 256, 256, FAKE, FAKE, FAKE, 0.0, 1.0, 10, None, None)
+    assert we == E.QKV_ERR_SCALE
+    assert L.qkv_calib_stats_f16(FAKE, -2.0, FAKE, None) == E.QKV_ERR_SCALE
