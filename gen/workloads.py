@@ -270,14 +270,14 @@ def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: i
                  num_kv_heads: int = 1, pad_frac: float = 0.0, outlier_frac: float = 0.0,
                  outlier_factor: float = 16.0, num_tokens: Optional[int] = None,
                  num_splits: int = 1, softmax_scale: float = 1.0 / 16.0,
-                 zero_tokens: int = 0, act_dtype: str = "bf16") -> Workload:
+                 zero_tokens: int = 0, act_dtype: str = "bf16", head_dim: int = HEAD_DIM) -> Workload:
     """Generic small case for parity tests: ragged top-k, -1 padding, optional outliers.
 
     `zero_tokens` tokens (chosen after the outliers) get all-zero K and V vectors, the
     degenerate absmax = 0 case. act_dtype 'f16' rounds q, K and V to IEEE half instead of
-    bf16 (same draws).
+    bf16 (same draws). head_dim 128 draws 128-wide heads instead of 256.
     """
-    S, H, D = num_slots, num_kv_heads, HEAD_DIM
+    S, H, D = num_slots, num_kv_heads, head_dim
     T = S if num_tokens is None else num_tokens
     rng = np.random.default_rng(seed)
     k = _normals(rng, (T, H, D))
@@ -312,14 +312,14 @@ def small_random(seed: int, num_slots: int, rows: int, topk: int, num_q_heads: i
 
 def small_paged(seed: int, num_seqs: int = 3, max_blocks: int = 6, block_size: int = 16, rows: int = 5,
                 topk: int = 40, pad_frac: float = 0.1, unallocated_frac: float = 0.15,
-                num_q_heads: int = 16, num_kv_heads: int = 1) -> Workload:
+                num_q_heads: int = 16, num_kv_heads: int = 1, head_dim: int = HEAD_DIM) -> Workload:
     """A small paged pool: num_seqs x max_blocks blocks of block_size slots, each sequence's
     blocks a random permutation of the pool's blocks, some table entries unallocated (-1).
 
     Rows draw distinct positions of their sequence (some landing in unallocated blocks, which
     the library must flag) plus -1 padding. Slot ids are left to the oracle's translation.
     """
-    H, D, Hq = num_kv_heads, HEAD_DIM, num_q_heads
+    H, D, Hq = num_kv_heads, head_dim, num_q_heads
     rng = np.random.default_rng(seed)
     total_blocks = num_seqs * max_blocks
     S = total_blocks * block_size

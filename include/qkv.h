@@ -19,13 +19,13 @@
  *     trapped: the offending entry is skipped and a bit is OR-ed into the optional
  *     caller-provided device word `dev_status` (may be NULL).
  *   - head_dim must be 256 (256 B of int8 data per head, [INT8-PR §The finding worth
- *     upstreaming]); num_q_heads / num_kv_heads (the GQA group) must be 1..128 (groups above 16
+ *     upstreaming]) or 128 (the other common head size; all layouts and entry points); num_q_heads / num_kv_heads (the GQA group) must be 1..128 (groups above 16
  *     run as one CTA per 16 query heads, each gathering the row's slots).
  *   - Pool layouts, S = num_slots, H = num_kv_heads, D = head_dim:
  *       QKV_BF16        K, V: bf16 [S, H, D]
  *       QKV_INT8_SIDE   K, V: int8 [S, H, D]; k_scale, v_scale: fp32 [S, H] (side tensors)
  *       QKV_INT8_INLINE K, V: bytes [S, H, D + 4]: D int8 codes then the fp32 scale,
- *                       little-endian (the 260 B record of [INT8-PR])
+ *                       little-endian (the 260 B record of [INT8-PR]; 132 B for D = 128)
  *       QKV_E4M3        K, V: E4M3 bytes [S, H, D]; one fp32 K and one fp32 V scale per layer
  *       QKV_F16         K, V: IEEE half [S, H, D] (the unquantised cache of the FP16-activation
  *                       contract; gathered by qsa_gather_attn_f16 only)
@@ -45,7 +45,7 @@ typedef enum {
   QKV_OK = 0,
   QKV_ERR_ARG = 1,         /* null pointer, negative size, bad enum, unsupported shape mix */
   QKV_ERR_SCALE = 2,       /* a per-layer scale that is not finite or is <= 0 */
-  QKV_ERR_UNSUPPORTED = 3, /* head_dim != 256 or GQA group outside 1..128 */
+  QKV_ERR_UNSUPPORTED = 3, /* head_dim not 256 or 128, or GQA group outside 1..128 */
   QKV_ERR_ALIGN = 4,       /* a base pointer or stride breaks the required alignment */
   QKV_ERR_CUDA = 5         /* a kernel launch or attribute call failed */
 } qkv_status;
@@ -242,7 +242,7 @@ qkv_status qsa_gather_attn_f16(const void* q, int64_t rows, int num_q_heads, int
  *   Rows whose splits are all empty (lse_s = -inf) give o = 0, lse = -inf.
  *   o_part fp32 [rows, P, num_q_heads, head_dim], lse_part fp32 [rows, P, num_q_heads],
  *   out fp32 [rows, num_q_heads, head_dim], lse fp32 [rows, num_q_heads] or NULL.
- *   v_scale_post finite (1.0 for the non-E4M3 formats). head_dim must be 256.
+ *   v_scale_post finite (1.0 for the non-E4M3 formats). head_dim 256 or 128.
  */
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
                             int num_q_heads, int head_dim, int num_splits, float v_scale_post,

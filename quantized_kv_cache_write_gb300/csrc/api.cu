@@ -8,7 +8,6 @@
 
 namespace {
 
-using qkv::kHeadDim;
 using qkv::kMaxGroup;
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -20,7 +19,7 @@ qkv_status check_write_inputs(const void* k, const void* v, int64_t num_tokens, 
                               int head_dim, int64_t token_stride, const int64_t* slot_mapping,
                               const void* k_cache, const void* v_cache, int64_t num_slots) {
   if (num_tokens < 0 || num_slots < 0 || num_kv_heads < 1) return QKV_ERR_ARG;
-  if (head_dim != kHeadDim) return QKV_ERR_UNSUPPORTED;
+  if (!qkv::head_dim_ok(head_dim)) return QKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return QKV_OK;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache) return QKV_ERR_ARG;
   if (token_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return QKV_ERR_ARG;
@@ -64,7 +63,7 @@ qkv_status write_int8_impl(const void* k, const void* v, bool f16, int64_t num_t
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (!inl && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_write_int8(k, v, f16, num_tokens, num_kv_heads, token_stride, slot_mapping, inl,
+  return cuda_status(qkv::launch_write_int8(k, v, f16, head_dim, num_tokens, num_kv_heads, token_stride, slot_mapping, inl,
                                             k_cache, v_cache, k_scale, v_scale, num_slots, dev_status,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -80,7 +79,7 @@ qkv_status write_e4m3_impl(const void* k, const void* v, bool f16, int64_t num_t
   if (num_tokens == 0) return QKV_OK;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_write_e4m3(k, v, f16, num_tokens, num_kv_heads, token_stride, slot_mapping, k_cache,
+  return cuda_status(qkv::launch_write_e4m3(k, v, f16, head_dim, num_tokens, num_kv_heads, token_stride, slot_mapping, k_cache,
                                             v_cache, k_scale, v_scale, num_slots, dev_status,
                                             static_cast<cudaStream_t>(stream)));
 }
@@ -184,7 +183,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
     if (pg->num_seqs * pg->max_blocks > INT32_MAX) return QKV_ERR_ARG;
   }
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0) return QKV_ERR_ARG;
-  if (head_dim != kHeadDim || num_q_heads / num_kv_heads > kMaxGroup) return QKV_ERR_UNSUPPORTED;
+  if (!qkv::head_dim_ok(head_dim) || num_q_heads / num_kv_heads > kMaxGroup) return QKV_ERR_UNSUPPORTED;
   if (fmt != QKV_BF16 && fmt != QKV_INT8_SIDE && fmt != QKV_INT8_INLINE && fmt != QKV_E4M3 && fmt != QKV_F16)
     return QKV_ERR_ARG;
   if (!std::isfinite(softmax_scale)) return QKV_ERR_ARG;
@@ -231,6 +230,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   a.rows = rows;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
+  a.head_dim = head_dim;
   a.topk = topk;
   a.num_splits = num_splits;
   a.softmax_scale = softmax_scale;
@@ -364,14 +364,14 @@ qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t 
                             int head_dim, int num_splits, float v_scale_post, float* out, float* lse,
                             void* stream) {
   if (rows < 0 || num_q_heads < 1 || num_splits < 1) return QKV_ERR_ARG;
-  if (head_dim != kHeadDim) return QKV_ERR_UNSUPPORTED;
+  if (!qkv::head_dim_ok(head_dim)) return QKV_ERR_UNSUPPORTED;
   if (!std::isfinite(v_scale_post)) return QKV_ERR_ARG;
   if (rows == 0) return QKV_OK;
   if (!o_part || !lse_part || !out) return QKV_ERR_ARG;
   if (!aligned(o_part, 16) || !aligned(out, 16) || !aligned(lse_part, 4) || (lse && !aligned(lse, 4)))
     return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_splitk_merge(o_part, lse_part, rows, num_q_heads, num_splits, v_scale_post, out,
-                                              lse, static_cast<cudaStream_t>(stream)));
+  return cuda_status(qkv::launch_splitk_merge(o_part, lse_part, rows, num_q_heads, head_dim, num_splits, v_scale_post,
+                                              out, lse, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

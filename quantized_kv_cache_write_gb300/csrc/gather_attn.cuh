@@ -69,34 +69,32 @@ constexpr float kMaxFinite = 3.4028234663852886e38f;  // largest finite fp32
 constexpr float kTau = 8.0f;    // lazy-rescale threshold (log2 units): p <= 2^8
 constexpr int kPShift = 7;      // x < 2^15; a key 2^-21 below the running max still has a normal hi
 constexpr int kEuHeadroom = 2;  // int8: the V-scale bound 2^eu is raised 2^2 past the largest scale seen
-constexpr int kTmemCols = 128;  // per CTA: 4 warps x (their 32 lanes) x 128 fp32 columns
 
-// kRowBytes: bytes of one K (or V) row in shared memory (the inline layout keeps the 272 B
-// of 17 aligned 16 B chunks that cover any 260 B record starting on a 4 B boundary).
-// kKShift: extra offset of the odd K rows.
+// Per-layout traits. kKShift: extra offset of the odd K rows. Row sizes depend on the head
+// dim too: see Geom.
 template <int FMT>
 struct Fmt;
 template <>
 struct Fmt<QKV_INT8_SIDE> {
-  static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
+  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64;
   static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false, kNatural = true;
   static constexpr bool kWide = false, kF16 = false;
 };
 template <>
 struct Fmt<QKV_INT8_INLINE> {
-  static constexpr int kRowBytes = 272, kGlobalRow = kInlineRecord, kStages = 2, kMinBlocks = 2, kKShift = 16;
+  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 16;
   static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false, kNatural = false;
   static constexpr bool kWide = false, kF16 = false;
 };
 template <>
 struct Fmt<QKV_E4M3> {
-  static constexpr int kRowBytes = 256, kGlobalRow = 256, kStages = 2, kMinBlocks = 3, kKShift = 64;
+  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false, kNatural = true;
   static constexpr bool kWide = false, kF16 = false;
 };
 template <>
 struct Fmt<QKV_BF16> {
-  static constexpr int kRowBytes = 512, kGlobalRow = 512, kStages = 2, kMinBlocks = 1, kKShift = 16;
+  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true, kNatural = false;
   static constexpr bool kWide = true, kF16 = false;
 };
@@ -104,9 +102,23 @@ struct Fmt<QKV_BF16> {
 // multiplied as fp16 (q must be fp16 too)
 template <>
 struct Fmt<QKV_F16> {
-  static constexpr int kRowBytes = 512, kGlobalRow = 512, kStages = 2, kMinBlocks = 1, kKShift = 16;
+  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = false, kNatural = false;
   static constexpr bool kWide = true, kF16 = true;
+};
+
+// Head-dim dependent sizes (HD = 128 or 256).
+//   kRowBytes   one K (or V) row in shared memory; the inline layout keeps the HD + 16 bytes of
+//               aligned 16 B chunks that cover any (HD + 4)-byte record on a 4 B boundary
+//   kGlobalRow  bytes of one record in the pool
+//   kBlocks     64-dim blocks of q.K^T; kSweeps: 128-dim sweeps of p.V and of the final merge
+//   kTmemCols   fp32 accumulator columns per TMEM lane (16 heads x HD dims over 32 lanes)
+template <int FMT, int HD>
+struct Geom {
+  static_assert(HD == 128 || HD == 256, "head_dim 128 or 256");
+  static constexpr int kRowBytes = Fmt<FMT>::kInline ? HD + 16 : (Fmt<FMT>::kWide ? 2 * HD : HD);
+  static constexpr int kGlobalRow = Fmt<FMT>::kInline ? HD + 4 : (Fmt<FMT>::kWide ? 2 * HD : HD);
+  static constexpr int kBlocks = HD / 64, kSweeps = HD / 128, kTmemCols = HD / 2;
 };
 
 // V region i (rows i and i + 8) starts 16 B further along the bank cycle than a plain packing
@@ -121,15 +133,16 @@ __host__ __device__ constexpr int v_region_shift(int i) {
 template <int FMT>
 __host__ __device__ constexpr int merge_row() { return Fmt<FMT>::kNatural ? 136 : 164; }
 
-template <int FMT, int STAGES = Fmt<FMT>::kStages>
+template <int FMT, int HD = 256, int STAGES = Fmt<FMT>::kStages>
 struct Smem {
   using F = Fmt<FMT>;
-  static constexpr size_t kQ = 0;  // [16 k-steps][16 heads][16] 16-bit, fragment order
-  static constexpr size_t kQBytes = 16 * 16 * 16 * 2;
+  using G = Geom<FMT, HD>;
+  static constexpr size_t kQ = 0;  // [HD / 16 k-steps][16 heads][16] 16-bit, fragment order
+  static constexpr size_t kQBytes = (HD / 16) * 16 * 16 * 2;
   static constexpr size_t kFac = kQ + kQBytes;  // [16] floats: logit factor per head
   // one stage: K rows, V rows, side scales (K then V), inline record offsets
-  static constexpr size_t kKArea = 2 * 8 * size_t(F::kRowBytes) + F::kKShift;
-  static constexpr size_t kVRegion = 2 * size_t(F::kRowBytes);
+  static constexpr size_t kKArea = 2 * 8 * size_t(G::kRowBytes) + F::kKShift;
+  static constexpr size_t kVRegion = 2 * size_t(G::kRowBytes);
   static constexpr size_t kVArea = 8 * kVRegion + v_region_shift<FMT>(7);
   static constexpr size_t kStageK = 0;
   static constexpr size_t kStageV = kKArea;
@@ -140,17 +153,19 @@ struct Smem {
   static constexpr size_t kStageBytes = ((kStageMask + (STAGES > 2 ? 4 : 0)) + 15) / 16 * 16;
   static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][STAGES] stages
   static constexpr size_t kWarpRing = size_t(STAGES) * kStageBytes;
-  static constexpr size_t kTmem = kRing + kWarps * kWarpRing;  // TMEM base address
+  // final merge buffer [kWarps][16][merge_row] floats, reusing the rings (which it may outgrow
+  // for small rows)
+  static constexpr size_t kMergeBytes = size_t(kWarps) * 16 * merge_row<FMT>() * 4;
+  static constexpr size_t kRingArea = kWarps * kWarpRing > kMergeBytes ? kWarps * kWarpRing : kMergeBytes;
+  static constexpr size_t kTmem = kRing + kRingArea;  // TMEM base address
   static constexpr size_t kM = kTmem + 16;                         // [kWarps][16] floats
   static constexpr size_t kL = kM + kWarps * 16 * 4;                 // [kWarps][16] floats
   static constexpr size_t kPost = kL + kWarps * 16 * 4;             // [kWarps] floats
   static constexpr size_t kTotal = kPost + kWarps * 4;
-  // final merge buffer [kWarps][16][merge_row] floats, reusing the rings
-  static_assert(size_t(kWarps) * 16 * merge_row<FMT>() * 4 <= kWarps * kWarpRing, "merge buffer must fit in the rings");
   static_assert(kRing % 16 == 0 && kKArea % 16 == 0 && kVArea % 16 == 0, "alignment");
   // the CTAs that fit an SM (228 KB of shared memory, 1 KB reserved each) never ask for more
   // than its 512 TMEM columns, so an allocation never has to wait for another CTA
-  static_assert((233472 / (kTotal + 1024)) * kTmemCols <= 512, "TMEM budget");
+  static_assert((233472 / (kTotal + 1024)) * G::kTmemCols <= 512, "TMEM budget");
 };
 
 // Key row (0..15 within a tile) feeding column n of N-tile nt of q.K^T -- and so the key whose
@@ -174,18 +189,18 @@ __device__ __forceinline__ int key_of(int nt, int n) {
 // V: row r in region r mod 8, each region 2 rows plus 16 (r mod 8) B of rotation (bf16: see
 // v_region_shift): 8 consecutive rows start on 8 distinct 16 B banks, as the transposed
 // matrix loads and the 16 B fragment reads want.
-template <int FMT>
+template <int FMT, int HD>
 __device__ __forceinline__ uint32_t k_row_off(int r) {
-  constexpr int RB = Fmt<FMT>::kRowBytes;
+  constexpr int RB = Geom<FMT, HD>::kRowBytes;
   const int b = Fmt<FMT>::kInt8 ? 1 : 0;
   const int region = (r >> b) & 1;
   const int idx = ((r >> (b + 1)) << b) | (r & ((1 << b) - 1));  // r without bit b
   return RB * idx + region * (8 * RB + Fmt<FMT>::kKShift);
 }
-template <int FMT>
+template <int FMT, int HD>
 __device__ __forceinline__ uint32_t v_row_off(int r) {
-  constexpr int RB = Fmt<FMT>::kRowBytes;
-  return Smem<FMT>::kStageV + (r & 7) * (2 * RB) + v_region_shift<FMT>(r & 7) + RB * (r >> 3);
+  constexpr int RB = Geom<FMT, HD>::kRowBytes;
+  return Smem<FMT, HD>::kStageV + (r & 7) * (2 * RB) + v_region_shift<FMT>(r & 7) + RB * (r >> 3);
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
@@ -203,10 +218,11 @@ __device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
 // QF16: q is IEEE half instead of bf16 (the FP16-activation contract); it only changes how
 // the query is staged.
 template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks,
-          bool QF16 = false>
+          bool QF16 = false, int HD = 256>
 __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const GatherArgs a) {
   using F = Fmt<FMT>;
-  using L = Smem<FMT, STAGES>;
+  using GM = Geom<FMT, HD>;
+  using L = Smem<FMT, HD, STAGES>;
   static_assert(STAGES >= 2, "the ring needs a stage in flight while one is computed");
   static_assert(!(F::kBf16 && QF16) && !(F::kF16 && !QF16), "a 16-bit pool takes a query of its own type");
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -234,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   const uint32_t sQ = smem_u32(smem + L::kQ);
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kTmem);
   if (warp == 0) {
-    tmem_alloc(smem_u32(sTmem), kTmemCols);
+    tmem_alloc(smem_u32(sTmem), GM::kTmemCols);
     tmem_relinquish_alloc_permit();
   }
 
@@ -300,14 +316,14 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   // lane l takes key l / 8 + 4 t (t = 0..3) and chunks l % 8 + 8 u of it, so only the record
   // base changes per key and every chunk of a key is an immediate offset from it. (More
   // keys per instruction split a request over more lines and were measured slower.)
-  constexpr int kRowChunks = F::kRowBytes / 16;
+  constexpr int kRowChunks = GM::kRowBytes / 16;
   constexpr int kKpi = 4;                              // keys per copy instruction
   constexpr int kHs = F::kInline ? 1 : kRowChunks / 8;  // lines per key
   const int key_sub = lane >> 3, chunk_sub = lane & 7;
   const uint8_t* kb_l = a.k_cache + 16 * chunk_sub;
   const uint8_t* vb_l = a.v_cache + 16 * chunk_sub;
-  const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT>(key_sub) + 16 * chunk_sub;
-  const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT>(key_sub) - L::kStageV + 16 * chunk_sub;
+  const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT, HD>(key_sub) + 16 * chunk_sub;
+  const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT, HD>(key_sub) - L::kStageV + 16 * chunk_sub;
 
   // Copy one 16-key tile into ring stage i % STAGES; returns the tile's valid-key mask (a
   // two-stage ring carries it one tile ahead in a register, a deeper one in the stage).
@@ -327,9 +343,9 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
         // bf16 zero-fill it, as a stale NaN code times p = 0 would still give NaN.
         const int nb = (F::kInt8 || rec >= 0) ? 16 : 0;
         rec = max(rec, 0);
-        const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(rec)) * F::kGlobalRow;
+        const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(rec)) * GM::kGlobalRow;
         // offsets of key l / 8 + 4 t relative to key l / 8 (the row layouts are additive)
-        const uint32_t tk = k_row_off<FMT>(kKpi * t), tv = v_row_off<FMT>(kKpi * t);
+        const uint32_t tk = k_row_off<FMT, HD>(kKpi * t), tv = v_row_off<FMT, HD>(kKpi * t);
 #pragma unroll
         for (int u = 0; u < kHs; ++u) {
           cp_async16(sbase + dk_l + tk + 128 * u, kb_l + off + 128 * u, nb);
@@ -338,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       }
     } else {
       // 16 B copies: consecutive lanes take consecutive chunks of a row (whole lines)
-      constexpr int kChunks = F::kInline ? 17 : F::kRowBytes / 16;
+      constexpr int kChunks = GM::kRowBytes / 16;  // inline: HD / 16 + 1
       constexpr int kTotalCopies = kKeys * kChunks;
       constexpr int kIters = (kTotalCopies + 31) / 32;
 #pragma unroll
@@ -352,10 +368,10 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
         slot = valid ? slot : 0;
         const int64_t rec = static_cast<int64_t>(slot) * H + h;
         if (act) {
-          const uint32_t dK = sbase + k_row_off<FMT>(key) + jj * 16;
-          const uint32_t dV = sbase + v_row_off<FMT>(key) + jj * 16;
+          const uint32_t dK = sbase + k_row_off<FMT, HD>(key) + jj * 16;
+          const uint32_t dV = sbase + v_row_off<FMT, HD>(key) + jj * 16;
           if (F::kInline) {
-            const int64_t off = rec * F::kGlobalRow;
+            const int64_t off = rec * GM::kGlobalRow;
             const int64_t al = off & ~int64_t(15);
             const int delta = static_cast<int>(off - al);
             // the 17th chunk copies only the record's own bytes (never past the pool's end)
@@ -411,22 +427,22 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     }
   }
 
-  // ---------------- stage the query once: 8 threads per head, 32 head dims each
+  // ---------------- stage the query once: 8 threads per head, HD / 8 head dims each
   {
+    constexpr int kW = HD / 16;  // 32-bit words (two head dims each) per thread
     const int qh = tid >> 3, part = tid & 7;
     const bool live = qh < Gc;
-    uint32_t w[16];
+    uint32_t w[kW];
     if (live) {
-      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + hq0 + qh) * kHeadDim +
-                                                      32 * part);
+      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + hq0 + qh) * HD + (HD / 8) * part);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kW / 4; ++i) {
         const uint4 x = __ldg(p + i);
         w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
+      for (int i = 0; i < kW; ++i) w[i] = 0u;
     }
     int sg = 0;
     if (!F::kBf16) {
@@ -437,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       if (QF16) {
         __half2 mh = __floats2half2_rn(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kW; ++i) {
           const uint32_t a16 = w[i] & 0x7FFF7FFFu;
           mh = __hmax2(mh, *reinterpret_cast<const __half2*>(&a16));
         }
@@ -445,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       } else {
         __nv_bfloat162 mh = __floats2bfloat162_rn(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < kW; ++i) {
           const uint32_t a16 = w[i] & 0x7FFF7FFFu;
           mh = __hmax2(mh, *reinterpret_cast<const __nv_bfloat162*>(&a16));
         }
@@ -461,11 +477,11 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     // two head dims per 32-bit store: the pair that shares a B-fragment register of a code
     // word (int8: d, d + 2; E4M3 and bf16: d, d + 1) sits in adjacent k-indices
 #pragma unroll
-    for (int g4 = 0; g4 < 8; ++g4) {
+    for (int g4 = 0; g4 < kW / 2; ++g4) {
 #pragma unroll
       for (int up = 0; up < 2; ++up) {
         const int i0 = 4 * g4 + (F::kInt8 ? up : 2 * up), i1 = i0 + (F::kInt8 ? 2 : 1);
-        const int d = 32 * part + i0;
+        const int d = (HD / 8) * part + i0;
         const int blk = d >> 6, cc = (d >> 4) & 3, ks = (d >> 2) & 3;
         const uint32_t b0 = (i0 & 1) ? (w[i0 >> 1] >> 16) : (w[i0 >> 1] & 0xFFFFu);
         const uint32_t b1 = (i1 & 1) ? (w[i1 >> 1] >> 16) : (w[i1 >> 1] & 0xFFFFu);
@@ -506,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
 #pragma unroll
     for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) tmem_st32(tacc + 32 * q, z);
+    for (int q = 0; q < GM::kTmemCols / 32; ++q) tmem_st32(tacc + 32 * q, z);
   }
 
   // ---------------- online-softmax state (per warp)
@@ -550,11 +566,11 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const int key = key_of<FMT>(nt, hn);
-      rowK[nt] = sbase + k_row_off<FMT>(key);
+      rowK[nt] = sbase + k_row_off<FMT, HD>(key);
       if (F::kInline) delta_k[nt] = lds_u8(sbase + L::kStageMeta + key);
     }
 #pragma unroll
-    for (int blk = 0; blk < 4; ++blk) {
+    for (int blk = 0; blk < GM::kBlocks; ++blk) {
       uint32_t kw[2][8];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -622,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
           vb = lds32(sbase + L::kStageKs + (kKeys + lane) * 4);
         } else {
           const int dl = lds_u8(sbase + L::kStageMeta + lane);
-          vb = lds32(sbase + v_row_off<FMT>(lane) + dl + kHeadDim);
+          vb = lds32(sbase + v_row_off<FMT, HD>(lane) + dl + HD);
         }
       }
       vmx_bits = __reduce_max_sync(0xffffffffu, vb & 0x7FFFFFFFu);
@@ -642,8 +658,8 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
           vs = __uint_as_float(lds32(sbase + L::kStageKs + (kKeys + kt) * 4));
         } else if (F::kInline) {
           const int dl = lds_u8(sbase + L::kStageMeta + kt);
-          ksc = __uint_as_float(lds32(sbase + k_row_off<FMT>(kt) + dl + kHeadDim));
-          vs = __uint_as_float(lds32(sbase + v_row_off<FMT>(kt) + dl + kHeadDim));
+          ksc = __uint_as_float(lds32(sbase + k_row_off<FMT, HD>(kt) + dl + HD));
+          vs = __uint_as_float(lds32(sbase + v_row_off<FMT, HD>(kt) + dl + HD));
         }
         // (padding keys already carry a zero V scale: their scale copies zero-fill)
         vsc[nt][e] = vs;
@@ -759,13 +775,13 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       int dv[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int ri = 0; ri < 4; ++ri) {
-        rowV[ri] = sbase + v_row_off<FMT>(rows[ri]);
+        rowV[ri] = sbase + v_row_off<FMT, HD>(rows[ri]);
         if (F::kInline) dv[ri] = lds_u8(sbase + L::kStageMeta + rows[ri]);
       }
       // natural layouts: lane l addresses key row l % 16 of the 16 B column block l / 16 (+ 2 m)
-      const uint32_t vmat = sbase + v_row_off<FMT>(lane & 15) + 16 * (lane >> 4);
+      const uint32_t vmat = sbase + v_row_off<FMT, HD>(lane & 15) + 16 * (lane >> 4);
 #pragma unroll
-      for (int sw = 0; sw < 2; ++sw) {
+      for (int sw = 0; sw < GM::kSweeps; ++sw) {
         // accumulator quarters 2 sw (N-tiles 16 sw + 0..7) and 2 sw + 1 (16 sw + 8..15)
         float ob[2][32];
         // the previous sweep's stores have read these registers (and the previous tile's
@@ -926,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     lse_h = (lsum > 0.f) ? (M + log2f(lsum)) * kLn2 : -INFINITY;
   }
 #pragma unroll 1
-  for (int sw = 0; sw < 2; ++sw) {
+  for (int sw = 0; sw < GM::kSweeps; ++sw) {
     {
       float ob[2][32];
       tmem_ld32(tacc + 64 * sw, ob[0]);
@@ -981,8 +997,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
           }
         }
         const int64_t qhead = hq0 + hh;
-        float* dst = (P == 1) ? a.out + (r * Hq + qhead) * kHeadDim
-                              : a.o_part + ((r * P + split) * Hq + qhead) * kHeadDim;
+        float* dst = (P == 1) ? a.out + (r * Hq + qhead) * HD : a.o_part + ((r * P + split) * Hq + qhead) * HD;
         dst += 128 * sw + (F::kNatural ? 4 * part : 16 * part);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -1017,12 +1032,12 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       if (hh < Gc) {
         // thread (hh, part) merges head hh's float4 columns part + 8 i: 8 threads of a head
         // read one contiguous 128 B line per load
-        int col4[8];
+        int col4[HD / 32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) col4[i] = part + 8 * i;
+        for (int i = 0; i < HD / 32; ++i) col4[i] = part + 8 * i;
         const int64_t qhead = hq0 + hh;
-        merge_head<8, 2>(a.o_part + (r * P * Hq + qhead) * kHeadDim, a.lse_part + r * P * Hq + qhead, Hq, P,
-                      F::kE4m3 ? a.v_scale_layer : 1.f, col4, a.out + (r * Hq + qhead) * kHeadDim,
+        merge_head<HD / 32, 2>(a.o_part + (r * P * Hq + qhead) * HD, a.lse_part + r * P * Hq + qhead, Hq, P, HD,
+                               F::kE4m3 ? a.v_scale_layer : 1.f, col4, a.out + (r * Hq + qhead) * HD,
                       (a.lse != nullptr && part == 0) ? a.lse + r * Hq + qhead : nullptr);
       }
       if (tid == 0) a.counters[unit] = 0u;  // every split has arrived: ready for the next call
@@ -1032,7 +1047,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
-  if (warp == 0) tmem_dealloc(*sTmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(*sTmem, GM::kTmemCols);
 }
 
 // CTAs of one launch: (row, KV head, 16-head chunk, split).
@@ -1042,7 +1057,7 @@ inline int64_t gather_grid(const GatherArgs& a) {
 }
 
 // Opt the kernel into its dynamic shared memory, once per device.
-template <int FMT, bool PAGED, int STAGES, int MINB, bool QF16 = false>
+template <int FMT, bool PAGED, int STAGES, int MINB, bool QF16 = false, int HD = 256>
 cudaError_t prepare_variant() {
   static bool attr_done[64] = {};
   int dev = 0;
@@ -1050,13 +1065,13 @@ cudaError_t prepare_variant() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16>,
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(Smem<FMT, STAGES>::kTotal));
+                             static_cast<int>(Smem<FMT, HD, STAGES>::kTotal));
     if (e != cudaSuccess) return e;
     // all of the unified L1 / shared array as shared memory: the copies bypass L1 anyway, and
     // the occupancy query then sees the CTAs per SM that a launch gets
-    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16>,
+    e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>,
                              cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     attr_done[dev] = true;
@@ -1065,19 +1080,27 @@ cudaError_t prepare_variant() {
 }
 
 template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks,
-          bool QF16 = false>
+          bool QF16 = false, int HD = 256>
 cudaError_t launch_variant(const GatherArgs& a, cudaStream_t stream) {
-  cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB, QF16>();
+  cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB, QF16, HD>();
   if (e != cudaSuccess) return e;
-  gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16>
-      <<<static_cast<unsigned>(gather_grid(a)), kThreads, Smem<FMT, STAGES>::kTotal, stream>>>(a);
+  gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>
+      <<<static_cast<unsigned>(gather_grid(a)), kThreads, Smem<FMT, HD, STAGES>::kTotal, stream>>>(a);
   return cudaGetLastError();
 }
 
-// The query is IEEE half (FP16-activation contract); default ring and occupancy.
+// The default ring and occupancy of the layout, for the launch's head dim (256 or 128).
+template <int FMT, bool PAGED, bool QF16>
+cudaError_t launch_hd(const GatherArgs& a, cudaStream_t stream) {
+  constexpr int S = Fmt<FMT>::kStages, B = Fmt<FMT>::kMinBlocks;
+  if (a.head_dim == 128) return launch_variant<FMT, PAGED, S, B, QF16, 128>(a, stream);
+  return launch_variant<FMT, PAGED, S, B, QF16, 256>(a, stream);
+}
+
+// The query is IEEE half (FP16-activation contract).
 template <int FMT>
 cudaError_t launch_f16q(const GatherArgs& a, cudaStream_t stream) {
-  return launch_variant<FMT, false, Fmt<FMT>::kStages, Fmt<FMT>::kMinBlocks, true>(a, stream);
+  return launch_hd<FMT, false, true>(a, stream);
 }
 
 // CTAs of the default kernel of this layout that one SM holds at once: the smaller of its
@@ -1093,7 +1116,7 @@ cudaError_t resident_ctas_per_sm(int* n) {
   if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess) return e;
-  const size_t per_cta = Smem<FMT, S>::kTotal + fa.sharedSizeBytes + static_cast<size_t>(reserved);
+  const size_t per_cta = Smem<FMT, 256, S>::kTotal + fa.sharedSizeBytes + static_cast<size_t>(reserved);
   const int by_smem = static_cast<int>(static_cast<size_t>(smem_sm) / per_cta);
   const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
   const int by_regs = regs_warp > 0 ? regs_sm / (regs_warp * kWarps) : by_smem;
@@ -1103,7 +1126,7 @@ cudaError_t resident_ctas_per_sm(int* n) {
 
 template <int FMT, bool PAGED = false>
 cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
-  return launch_variant<FMT, PAGED>(a, stream);
+  return launch_hd<FMT, PAGED, false>(a, stream);
 }
 
 }  // namespace gather

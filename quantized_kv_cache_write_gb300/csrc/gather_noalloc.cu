@@ -5,7 +5,7 @@
 // device memory itself -- for example a plugin running inside a host engine that hands it
 // pre-allocated tensors and forbids allocation during serving, because cudaMalloc can
 // synchronise the whole device and fragments a memory pool the host manages. Such a caller
-// cannot provide the [rows, P, Hq, 256] partial buffers that qsa_gather_attn needs for
+// cannot provide the [rows, P, Hq, head_dim] partial buffers that qsa_gather_attn needs for
 // num_splits > 1; this entry point supplies them from the static array below.
 //
 // The array costs every GPU that loads libqkv.so kQkvNoallocScratchBytes of device memory
@@ -56,19 +56,19 @@ extern "C" qkv_status qsa_gather_attn_splitk_noalloc(
     return qsa_gather_attn(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok,
                            v_scale_tok, k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, 1,
                            out, lse, nullptr, nullptr, dev_status, stream);
-  if (rows < 0 || num_q_heads < 1 || num_splits < 1 || head_dim != qkv::kHeadDim) return QKV_ERR_ARG;
+  if (rows < 0 || num_q_heads < 1 || num_splits < 1 || !qkv::head_dim_ok(head_dim)) return QKV_ERR_ARG;
   if (rows == 0) return QKV_OK;
   if (static_cast<uint64_t>(rows) > kScratchBytes || static_cast<uint64_t>(num_splits) > kScratchBytes)
     return QKV_ERR_ARG;
   if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return QKV_ERR_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3) != 0) return QKV_ERR_ALIGN;
 
-  // Partials layout inside the scratch: o_part [rows, P, Hq, 256] fp32, then lse_part
+  // Partials layout inside the scratch: o_part [rows, P, Hq, head_dim] fp32, then lse_part
   // [rows, P, Hq] fp32 starting on a 256 B boundary. Sizes beyond the array are refused.
   const uint64_t parts = static_cast<uint64_t>(rows) * static_cast<uint64_t>(num_splits) *
                          static_cast<uint64_t>(num_q_heads);
   if (parts > kScratchBytes) return QKV_ERR_ARG;
-  const uint64_t o_bytes = parts * qkv::kHeadDim * sizeof(float);
+  const uint64_t o_bytes = parts * static_cast<uint64_t>(head_dim) * sizeof(float);
   const uint64_t lse_off = (o_bytes + 255) & ~uint64_t(255);
   if (lse_off + parts * sizeof(float) > kScratchBytes) return QKV_ERR_ARG;
 

@@ -11,16 +11,17 @@
 
 namespace qkv {
 
-constexpr int kHeadDim = 256;
+constexpr int kHeadDim = 256;       // the pages' head dim (256 B of int8 per head)
+constexpr int kHeadDimSmall = 128;  // the other head dim the kernels take
+__host__ __device__ constexpr bool head_dim_ok(int d) { return d == kHeadDim || d == kHeadDimSmall; }
 constexpr int kMaxGroup = 128;  // GQA group; above 16 the gather runs one CTA per 16 query heads
-constexpr int kInlineRecord = kHeadDim + 4;  // 256 code bytes + fp32 scale
 
 // ------------------------------------------------------------------ launchers
-cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
                               void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                               int64_t num_slots, uint32_t* dev_status, cudaStream_t stream);
-cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
                               void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream);
@@ -30,7 +31,7 @@ cudaError_t launch_calib_histogram(const void* x, int64_t n, uint64_t* hist, cud
 cudaError_t launch_calib_stats(const uint64_t* hist, bool f16, float scale, qkv_calib_summary* stats,
                                cudaStream_t stream);
 cudaError_t launch_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
-                                int num_q_heads, int num_splits, float v_scale_post, float* out,
+                                int num_q_heads, int head_dim, int num_splits, float v_scale_post, float* out,
                                 float* lse, cudaStream_t stream);
 
 // Arguments of one gather-attention launch (already validated on the host).
@@ -47,6 +48,7 @@ struct GatherArgs {
   int64_t rows;
   int num_q_heads;
   int num_kv_heads;
+  int head_dim;  // 256 or 128
   int topk;
   int num_splits;
   float softmax_scale;
@@ -251,14 +253,15 @@ __device__ __forceinline__ void f2scale(float* v, uint64_t s) {
 // Split-K merge of one (row, query head) over the NV float4 column groups col4[0..NV):
 //   lse = log sum_s exp(lse_s),  o = v_scale_post * sum_s exp(lse_s - lse) o_s,
 // with empty splits (lse_s = -inf) skipped and an all-empty row giving o = 0, lse = -inf.
-// o_head = o_part at (row, split 0, head): splits are Hq * kHeadDim floats apart; lp = lse_part
+// o_head = o_part at (row, split 0, head): splits are Hq * head_dim floats apart; lp = lse_part
 // at (row, split 0, head): splits are Hq floats apart. Partials are read through L2
 // (ld.global.cg) because in the fused gather other CTAs of the same launch wrote them. The
 // loads of U splits are issued together (U * NV 16 B loads in flight per thread); the sums
 // still run over s = 0, 1, ... in order, so a column's result does not depend on which thread
 // or kernel merges it, nor on U.
 template <int NV, int U>
-__device__ __forceinline__ void merge_head(const float* o_head, const float* lp, int Hq, int P, float v_scale_post,
+__device__ __forceinline__ void merge_head(const float* o_head, const float* lp, int Hq, int P, int head_dim,
+                                           float v_scale_post,
                                            const int (&col4)[NV], float* out_head, float* lse_out) {
   float m = -INFINITY;
 #pragma unroll 4
@@ -274,7 +277,7 @@ __device__ __forceinline__ void merge_head(const float* o_head, const float* lp,
 #pragma unroll
   for (int i = 0; i < 4 * NV; ++i) acc[i] = 0.f;
   float wsum = 0.f;
-  const int64_t sstride = static_cast<int64_t>(Hq) * kHeadDim;
+  const int64_t sstride = static_cast<int64_t>(Hq) * head_dim;
   for (int s0 = 0; s0 < P; s0 += U) {
     float4 x[U][NV];
     float ls[U];

@@ -8,9 +8,9 @@
 // "Qwen3.8 Flash Next NVFP4 QSA FP8 E4M3 KV Scales" §Calibration (stored = e4m3fn(x/scale),
 // scale = max envelope / 448).
 //
-// One warp owns one (token, head, tensor): 32 lanes x 8 bf16 = the 256-wide head vector,
-// read as one coalesced 512 B line; the absmax is a 5-step shuffle reduction; the codes
-// leave as one coalesced 256 B line. Division is IEEE (__fdiv_rn) and rounding is
+// One warp owns one (token, head, tensor): 32 lanes x 8 values = a 256-wide head vector, read
+// as one coalesced line (head_dim 128: lanes 16..31 idle); the absmax is a 5-step shuffle
+// reduction; the codes leave as one coalesced line. Division is IEEE (__fdiv_rn) and rounding is
 // round-to-nearest-even so the stored bytes equal a plain fp32 reference bit for bit.
 #include "qkv_internal.cuh"
 
@@ -72,7 +72,7 @@ __device__ __forceinline__ bool decode_item(int64_t item, int num_heads, const i
 
 template <bool kInline, bool F16>
 __global__ void __launch_bounds__(kWriteThreads)
-    write_int8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+    write_int8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
                       int64_t num_tokens, int num_heads, int64_t token_stride,
                       const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
                       uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(kWriteThreads)
   int h, is_v;
   if (!decode_item(item, num_heads, slot_mapping, num_slots, dev_status, lane, t, h, is_v, slot)) return;
 
-  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * kHeadDim + lane * 8;
-  const HeadVec hv = load_head8<F16>(src);
+  const bool act = 8 * lane < head_dim;  // lane owns head dims 8 lane .. 8 lane + 7
+  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * head_dim + lane * 8;
+  const HeadVec hv = act ? load_head8<F16>(src) : HeadVec{};
   float a = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(hv.x[i]));
@@ -104,20 +105,22 @@ __global__ void __launch_bounds__(kWriteThreads)
   const int64_t rec = slot * num_heads + h;
   uint8_t* cache = is_v ? v_cache : k_cache;
   if (kInline) {
-    uint8_t* base = cache + rec * kInlineRecord;
+    uint8_t* base = cache + rec * (head_dim + 4);  // head_dim codes, then the fp32 scale
     uint32_t* dst = reinterpret_cast<uint32_t*>(base + lane * 8);  // records are 4 B aligned
-    dst[0] = word[0];
-    dst[1] = word[1];
-    if (lane == 0) *reinterpret_cast<float*>(base + kHeadDim) = scale;
+    if (act) {
+      dst[0] = word[0];
+      dst[1] = word[1];
+    }
+    if (lane == 0) *reinterpret_cast<float*>(base + head_dim) = scale;
   } else {
-    *reinterpret_cast<uint2*>(cache + rec * kHeadDim + lane * 8) = make_uint2(word[0], word[1]);
+    if (act) *reinterpret_cast<uint2*>(cache + rec * head_dim + lane * 8) = make_uint2(word[0], word[1]);
     if (lane == 0) (is_v ? v_scale : k_scale)[rec] = scale;
   }
 }
 
 template <bool F16>
 __global__ void __launch_bounds__(kWriteThreads)
-    write_e4m3_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+    write_e4m3_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
                       int64_t num_tokens, int num_heads, int64_t token_stride,
                       const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
                       uint8_t* __restrict__ v_cache, float k_scale, float v_scale, int64_t num_slots,
@@ -129,7 +132,8 @@ __global__ void __launch_bounds__(kWriteThreads)
   int h, is_v;
   if (!decode_item(item, num_heads, slot_mapping, num_slots, dev_status, lane, t, h, is_v, slot)) return;
 
-  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * kHeadDim + lane * 8;
+  if (8 * lane >= head_dim) return;  // head_dim 128: lanes 16..31 own no dims (no shuffles follow)
+  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * head_dim + lane * 8;
   const HeadVec hv = load_head8<F16>(src);
   const float s = is_v ? v_scale : k_scale;
   uint32_t word[2] = {0u, 0u};
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kWriteThreads)
     word[i >> 2] |= (p & 0xFFFFu) << (8 * (i & 3));
   }
   uint8_t* cache = is_v ? v_cache : k_cache;
-  *reinterpret_cast<uint2*>(cache + (slot * num_heads + h) * kHeadDim + lane * 8) = make_uint2(word[0], word[1]);
+  *reinterpret_cast<uint2*>(cache + (slot * num_heads + h) * head_dim + lane * 8) = make_uint2(word[0], word[1]);
 }
 
 // max |x| over n bf16 values, as fp32 bits (non-negative floats order like their bits).
@@ -184,7 +188,7 @@ unsigned write_blocks(int64_t num_tokens, int num_heads) {
 
 }  // namespace
 
-cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
                               void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                               int64_t num_slots, uint32_t* dev_status, cudaStream_t stream) {
@@ -197,18 +201,18 @@ cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int64_t nu
   float* vs = inline_layout ? nullptr : v_scale;
   auto kern = inline_layout ? (f16 ? write_int8_kernel<true, true> : write_int8_kernel<true, false>)
                             : (f16 ? write_int8_kernel<false, true> : write_int8_kernel<false, false>);
-  kern<<<blocks, kWriteThreads, 0, stream>>>(kk, vv, num_tokens, num_heads, token_stride, slot_mapping, kc, vc, ks,
-                                             vs, num_slots, dev_status);
+  kern<<<blocks, kWriteThreads, 0, stream>>>(kk, vv, head_dim, num_tokens, num_heads, token_stride, slot_mapping, kc,
+                                             vc, ks, vs, num_slots, dev_status);
   return cudaGetLastError();
 }
 
-cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int64_t num_tokens, int num_heads,
+cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
                               int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
                               void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream) {
   auto kern = f16 ? write_e4m3_kernel<true> : write_e4m3_kernel<false>;
   kern<<<write_blocks(num_tokens, num_heads), kWriteThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), num_tokens, num_heads, token_stride,
+      static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), head_dim, num_tokens, num_heads, token_stride,
       slot_mapping, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale, v_scale, num_slots,
       dev_status);
   return cudaGetLastError();

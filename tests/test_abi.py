@@ -59,7 +59,8 @@ def _gather(lib, **over):
 
 def test_gather_host_validation(lib):
     E = lib
-    assert _gather(lib, d=128) == E.QKV_ERR_UNSUPPORTED
+    assert _gather(lib, d=64) == E.QKV_ERR_UNSUPPORTED
+    assert _gather(lib, d=128, rows=0) == E.QKV_OK  # 128-wide heads are supported
     assert _gather(lib, hq=258, hkv=2) == E.QKV_ERR_UNSUPPORTED  # group 129
     assert _gather(lib, hq=256, hkv=2, rows=0) == E.QKV_OK  # group 128 is supported
     assert _gather(lib, hq=15, hkv=2) == E.QKV_ERR_ARG
@@ -108,7 +109,7 @@ def test_write_host_validation(lib):
 
 def test_merge_and_calibrate_host_validation(lib):
     E, L = lib, lib.lib
-    assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 128, 4, 1.0, FAKE, None, None) == E.QKV_ERR_UNSUPPORTED
+    assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 192, 4, 1.0, FAKE, None, None) == E.QKV_ERR_UNSUPPORTED
     assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 256, 0, 1.0, FAKE, None, None) == E.QKV_ERR_ARG
     assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 256, 4, float("inf"), FAKE, None, None) == E.QKV_ERR_ARG
     assert L.qsa_splitk_merge(FAKE + 4, FAKE, 2, 16, 256, 4, 1.0, FAKE, None, None) == E.QKV_ERR_ALIGN
@@ -162,7 +163,7 @@ def test_paged_gather_host_validation(lib):
     assert _gather_paged(lib, bt=None) == E.QKV_ERR_ARG
     assert _gather_paged(lib, rs=None) == E.QKV_ERR_ARG
     assert _gather_paged(lib, rs=FAKE + 2) == E.QKV_ERR_ALIGN
-    assert _gather_paged(lib, d=128) == E.QKV_ERR_UNSUPPORTED  # the common checks still apply
+    assert _gather_paged(lib, d=96) == E.QKV_ERR_UNSUPPORTED  # the common checks still apply
     assert _gather_paged(lib, rows=0) == E.QKV_OK
 
 
@@ -186,7 +187,7 @@ def test_fused_gather_host_validation(lib):
     assert _gather_fused(lib, lp=None) == E.QKV_ERR_ARG
     assert _gather_fused(lib, out=FAKE + 4) == E.QKV_ERR_ALIGN
     assert _gather_fused(lib, P=0) == E.QKV_ERR_ARG
-    assert _gather_fused(lib, d=128) == E.QKV_ERR_UNSUPPORTED
+    assert _gather_fused(lib, d=512) == E.QKV_ERR_UNSUPPORTED
     assert _gather_fused(lib, fmt=E.QKV_E4M3, ks=None, vs=None, ksl=0.0) == E.QKV_ERR_SCALE
     assert _gather_fused(lib, rows=0) == E.QKV_OK
     # unsplit: workspace and counters are neither needed nor allowed to be required
