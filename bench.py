@@ -44,7 +44,8 @@ KERNEL_SOURCES = ["gather_attn.cuh", "qkv_internal.cuh", "gather_int8_side.cu"]
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    # 2000 steps keep the timed region ~0.6 s long, so the 50 ms clock sampler sees it under load
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--splits", type=int, default=1, help="K-splits of each row (1 = unsplit)")
@@ -82,8 +83,8 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def load_traffic():
-    """ncu dram bytes per gather launch, if taken on the current kernel source; else None."""
+def load_profile():
+    """The committed ncu figures of the gather kernel, if taken on the current kernel source."""
     try:
         kv = {}
         with open(TRAFFIC_FILE) as f:
@@ -93,8 +94,17 @@ def load_traffic():
                     kv[k.strip()] = v.strip()
         if kv.get("kernel_source_sha256_16") != kernel_source_hash():
             return None
-        return float(kv["dram_bytes_per_launch"])
+        return kv
     except Exception:
+        return None
+
+
+def load_traffic():
+    """ncu dram bytes per gather launch, if taken on the current kernel source; else None."""
+    kv = load_profile()
+    try:
+        return float(kv["dram_bytes_per_launch"]) if kv else None
+    except (KeyError, ValueError):
         return None
 
 
@@ -331,6 +341,8 @@ def main():
         "rows_per_s": round(rows_per_s, 1),
         "frac_of_hbm_peak_total": round(value / (world * peak), 4),
         "unique_gathered_GBps": round(world * uniq_slots * SLOT_BYTES["int8_side"] / (ms * 1e-3) / 1e9, 2),
+        "frac_of_hbm_peak_unique": round(uniq_slots * SLOT_BYTES["int8_side"] / (ms * 1e-3) / 1e9 / peak, 4),
+        "unique_slots": uniq_slots,
         "write_ms": round(sum(write_ms) / len(write_ms), 5),
         "gather_ms": round(g_ms, 5),
         "gpu_launches": launches_per_step * args.steps,
@@ -338,7 +350,10 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": load_traffic(),
                      "kernel": "gather_attn_kernel<QKV_INT8_SIDE>",
-                     "algorithmic_bytes_per_launch": gathered, "peak_source": peak_src},
+                     "algorithmic_bytes_per_launch": gathered, "peak_source": peak_src,
+                     "ncu": ({k: float(v) for k, v in prof.items() if k not in ("kernel_source_sha256_16",)}
+                             if (prof := load_profile()) else None),
+                     "ncu_source": "profiles/gather_int8_side_page1_full.md (same kernel source hash)"},
         "wall_s_timed_region": round(t_wall, 3),
         "pages_context": {"gb10_side_ms": 9.6, "gb10_inline_ms": 60.2,
                           "note": "one GB10 (sm_121), Triton path; context only"},
