@@ -206,7 +206,9 @@ def run_reference(args):
     from gen import page1_shape
     wl = page1_shape(1)
     K, V = oracle_setup(wl)
-    n = args.cpu_sample_rows or 64
+    # rows per step: the whole --steps K --warmup W run stays near a minute of CPU time
+    # (the oracle takes ~2 ms per row of 1024 keys x 16 heads on one core)
+    n = args.cpu_sample_rows or max(1, min(64, int(60.0 / (max(1, args.steps) + max(1, args.warmup)) / 0.002)))
     rows = list(range(n))
     time_oracle(wl, K, V, rows, max(1, args.warmup))
     times = time_oracle(wl, K, V, rows, max(1, args.steps))
