@@ -712,12 +712,15 @@ def measure_workloads(q, flush, stream, reps, peak):
     out = torch.empty((wl.rows, wl.num_q_heads, D), dtype=torch.float32, device="cuda")
     g = _time_events(lambda: q.qsa_gather_attn(qd, q.QKV_INT8_SIDE, kc, vc, idx, wl.softmax_scale, out=out,
                                                k_scale_tok=ks, v_scale_tok=vs), flush, stream, reps)
+    lens = torch.from_numpy(np.minimum(np.arange(wl.rows), wl.topk.shape[1]).astype(np.int32)).cuda()
+    gv = _time_events(lambda: q.qsa_gather_attn_varlen(qd, q.QKV_INT8_SIDE, kc, vc, idx, lens, wl.softmax_scale,
+                                                       out=out, k_scale_tok=ks, v_scale_tok=vs), flush, stream, reps)
     visits = int((wl.topk >= 0).sum())
     res["chunked_prefill"] = {
         "shape": "8192 new tokens into a 524288-slot pool; 8192 rows, row i attends min(1024, i) earlier tokens",
         "write_int8_ms": round(w8, 5), "write_e4m3_ms": round(we, 5),
         "write_int8_GBps": round(8192 * (1024 + 520) / (w8 * 1e-3) / 1e9, 2),
-        "gather_int8_side_ms": round(g, 5), "slot_visits": visits,
+        "gather_int8_side_ms": round(g, 5), "gather_varlen_ms": round(gv, 5), "slot_visits": visits,
         "gather_GBps": round(visits * SLOT_BYTES["int8_side"] / (g * 1e-3) / 1e9, 2),
         "note": "the 8192 written slots (4.3 MB) stay in L2: gathered GB/s is bounded by L2, not HBM "
                 f"(measured HBM peak {peak} GB/s)"}

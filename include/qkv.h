@@ -221,6 +221,28 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
                            float* o_part, float* lse_part, uint32_t* dev_status, void* stream);
 
 /*
+ * qsa_gather_attn_varlen -- qsa_gather_attn for rows of different lengths: row r's valid
+ * entries are topk_idx[r, 0 .. topk_len[r]); the entries past that length are never read (they
+ * may hold anything). A batch that mixes long and short rows (the pages route such mixed
+ * catch-up / decode batches across kernels, [E4M3-PR §Implementation scope]) then costs only
+ * its valid entries. Inside the length, -1 is still padding.
+ *   topk_len  int32 [rows], each in [0, topk]; a value outside is flagged with
+ *             QKV_DEV_BAD_INDEX and clamped. NULL is QKV_ERR_ARG (use qsa_gather_attn).
+ *   The split partition stays over the full width topk (split s covers columns
+ *   [s c, (s + 1) c), c = ceil(topk / P)), so a short row's trailing splits are empty
+ *   (o = 0, lse = -inf). Everything else as qsa_gather_attn; the result equals qsa_gather_attn
+ *   on topk_idx with the entries past each row's length set to -1.
+ */
+qkv_status qsa_gather_attn_varlen(const void* q, int64_t rows, int num_q_heads, int num_kv_heads,
+                                  int head_dim, qkv_format fmt, const void* k_cache,
+                                  const void* v_cache, const float* k_scale_tok,
+                                  const float* v_scale_tok, float k_scale_layer,
+                                  float v_scale_layer, int64_t num_slots, const int32_t* topk_idx,
+                                  int topk, const int32_t* topk_len, float softmax_scale,
+                                  int num_splits, float* out, float* lse, float* o_part,
+                                  float* lse_part, uint32_t* dev_status, void* stream);
+
+/*
  * qsa_gather_attn_f16 -- qsa_gather_attn with an IEEE-half query, for the FP16-activation
  * contract [E4M3-PR §Purpose]. q fp16 [rows, num_q_heads, head_dim]; fmt one of
  * QKV_INT8_SIDE, QKV_INT8_INLINE, QKV_E4M3 or QKV_F16 (a half pool); QKV_BF16 is

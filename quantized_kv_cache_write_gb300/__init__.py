@@ -47,6 +47,8 @@ _SIGS = {
     "qsa_suggest_num_splits": [_i32, _i64, _i32, _i32, _i32, ctypes.POINTER(ctypes.c_int)],
     "qsa_gather_attn_splitk_noalloc": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p,
                                        _i32, _f32, _i32, _p, _p, _p, _p],
+    "qsa_gather_attn_varlen": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _p,
+                               _f32, _i32, _p, _p, _p, _p, _p, _p],
     "qsa_gather_attn_f16": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32, _f32,
                             _i32, _p, _p, _p, _p, _p, _p],
     "qsa_gather_attn_splitk_fused": [_p, _i64, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _f32, _f32, _i64, _p, _i32,
@@ -198,6 +200,26 @@ def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: floa
                             _ptr(topk_idx), topk, float(softmax_scale), num_splits, _ptr(out), _ptr(lse),
                             _ptr(o_part), _ptr(lse_part), _ptr(dev_status), _stream(stream))
     _check(name, st)
+
+
+def qsa_gather_attn_varlen(q, fmt: int, k_cache, v_cache, topk_idx, topk_len, softmax_scale: float, *,
+                           num_kv_heads: int = 1, num_slots: Optional[int] = None, k_scale_tok=None,
+                           v_scale_tok=None, k_scale_layer: float = 1.0, v_scale_layer: float = 1.0,
+                           num_splits: int = 1, out=None, lse=None, o_part=None, lse_part=None, dev_status=None,
+                           stream=None):
+    """Gather for rows of different lengths: row r uses topk_idx[r, :topk_len[r]] (int32 [R])."""
+    _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
+    R, Hq, D = q.shape
+    if topk_len is None or topk_len.numel() != R or topk_len.dtype != torch.int32:
+        raise ValueError(f"topk_len must be int32 [{R}]")
+    S = k_cache.shape[0] if num_slots is None else num_slots
+    topk = topk_idx.shape[1]
+    st = lib.qsa_gather_attn_varlen(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
+                                    _ptr(k_scale_tok), _ptr(v_scale_tok), float(k_scale_layer), float(v_scale_layer),
+                                    S, _ptr(topk_idx), topk, _ptr(topk_len), float(softmax_scale), num_splits,
+                                    _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), _ptr(dev_status),
+                                    _stream(stream))
+    _check("qsa_gather_attn_varlen", st)
 
 
 def qsa_gather_attn_paged(q, fmt: int, k_cache, v_cache, block_table, row_seq, topk_pos, block_size: int,

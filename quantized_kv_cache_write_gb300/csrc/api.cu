@@ -172,7 +172,8 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
                        const float* v_scale_tok, float k_scale_layer, float v_scale_layer, int64_t num_slots,
                        const int32_t* topk_idx, int topk, float softmax_scale, int num_splits, float* out,
                        float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream,
-                       const Paging* pg, uint32_t* counters = nullptr, bool q_f16 = false) {
+                       const Paging* pg, uint32_t* counters = nullptr, bool q_f16 = false,
+                       const int32_t* topk_len = nullptr) {
   if (rows < 0 || topk < 0 || num_splits < 1 || num_slots < 0) return QKV_ERR_ARG;
   // a 16-bit pool is multiplied in its own type, so it needs a query of that type
   if ((fmt == QKV_F16 && !q_f16) || (fmt == QKV_BF16 && q_f16)) return QKV_ERR_ARG;
@@ -208,6 +209,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   if (!q || !k_cache || !v_cache || (topk > 0 && !topk_idx)) return QKV_ERR_ARG;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (topk_idx && !aligned(topk_idx, 4)) return QKV_ERR_ALIGN;
+  if (topk_len && !aligned(topk_len, 4)) return QKV_ERR_ALIGN;
   if (side && (!aligned(k_scale_tok, 4) || !aligned(v_scale_tok, 4))) return QKV_ERR_ALIGN;
   if ((out && !aligned(out, 16)) || (o_part && !aligned(o_part, 16))) return QKV_ERR_ALIGN;
   if ((lse && !aligned(lse, 4)) || (lse_part && !aligned(lse_part, 4))) return QKV_ERR_ALIGN;
@@ -227,6 +229,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   a.v_scale_layer = v_scale_layer;
   a.num_slots = num_slots;
   a.topk_idx = topk_idx;
+  a.topk_len = topk_len;
   a.rows = rows;
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
@@ -285,6 +288,18 @@ qkv_status qsa_gather_attn(const void* q, int64_t rows, int num_q_heads, int num
   return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
                      k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, num_splits, out, lse,
                      o_part, lse_part, dev_status, stream, nullptr);
+}
+
+qkv_status qsa_gather_attn_varlen(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,
+                                  qkv_format fmt, const void* k_cache, const void* v_cache,
+                                  const float* k_scale_tok, const float* v_scale_tok, float k_scale_layer,
+                                  float v_scale_layer, int64_t num_slots, const int32_t* topk_idx, int topk,
+                                  const int32_t* topk_len, float softmax_scale, int num_splits, float* out,
+                                  float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream) {
+  if (rows > 0 && topk_len == nullptr) return QKV_ERR_ARG;
+  return gather_impl(q, rows, num_q_heads, num_kv_heads, head_dim, fmt, k_cache, v_cache, k_scale_tok, v_scale_tok,
+                     k_scale_layer, v_scale_layer, num_slots, topk_idx, topk, softmax_scale, num_splits, out, lse,
+                     o_part, lse_part, dev_status, stream, nullptr, nullptr, false, topk_len);
 }
 
 qkv_status qsa_gather_attn_f16(const void* q, int64_t rows, int num_q_heads, int num_kv_heads, int head_dim,

@@ -242,9 +242,18 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   const int64_t r = rh / H;
   const int hq0 = h * G + kHeadsPerCta * qc;            // first query head of this CTA
   const int Gc = min(kHeadsPerCta, G - kHeadsPerCta * qc);  // query heads of this CTA (1..16)
+  // the split partition is over the full width topk; a row with a valid length (varlen) ends
+  // there, and its columns past it are never read
+  int len = a.topk;
+  if (a.topk_len != nullptr) {
+    const int l = __ldg(a.topk_len + r);
+    if ((l < 0 || l > a.topk) && tid == 0 && split == 0 && qc == 0 && a.dev_status != nullptr)
+      atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+    len = min(max(l, 0), a.topk);
+  }
   const int per_split = (a.topk + P - 1) / P;
-  const int col0 = min(a.topk, split * per_split);
-  const int col1 = min(a.topk, col0 + per_split);
+  const int col0 = min(len, split * per_split);
+  const int col1 = min(len, split * per_split + per_split);
   float* sFac = reinterpret_cast<float*>(smem + L::kFac);
   uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
   const uint32_t sQ = smem_u32(smem + L::kQ);
@@ -339,9 +348,11 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
 #pragma unroll
       for (int t = 0; t < kKeys / kKpi; ++t) {
         int rec = __shfl_sync(0xffffffffu, rec_l, key_sub + kKpi * t);
-        // int8 padding reads record 0 (finite codes; its p is 0): no zero-fill needed. E4M3 and
-        // bf16 zero-fill it, as a stale NaN code times p = 0 would still give NaN.
-        const int nb = (F::kInt8 || rec >= 0) ? 16 : 0;
+        // padding copies nothing and zero-fills its row (a zero source size reads no memory):
+        // a stale E4M3 or bf16 NaN times p = 0 would still give NaN, and redirecting padding to
+        // a real record made every padded row of a batch hammer the same L2 lines (2x slower on
+        // causal chunked-prefill rows, whose padding sits at the end)
+        const int nb = rec >= 0 ? 16 : 0;
         rec = max(rec, 0);
         const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(rec)) * GM::kGlobalRow;
         // offsets of key l / 8 + 4 t relative to key l / 8 (the row layouts are additive)

@@ -45,6 +45,7 @@ struct GatherArgs {
   float v_scale_layer;
   int64_t num_slots;
   const int32_t* topk_idx;
+  const int32_t* topk_len = nullptr;  // varlen: valid entries per row [rows], or null (all topk)
   int64_t rows;
   int num_q_heads;
   int num_kv_heads;

@@ -234,3 +234,13 @@ def test_fp16_entry_points_host_validation(lib):
     we = L.qkv_write_e4m3_f16(FAKE, FAKE, 3, 1, 256, 256, FAKE, FAKE, FAKE, 0.0, 1.0, 10, None, None)
     assert we == E.QKV_ERR_SCALE
     assert L.qkv_calib_stats_f16(FAKE, -2.0, FAKE, None) == E.QKV_ERR_SCALE
+
+
+def test_varlen_host_validation(lib):
+    E, L = lib, lib.lib
+    vl = lambda **o: L.qsa_gather_attn_varlen(FAKE, o.get("rows", 4), 16, 1, 256, E.QKV_INT8_SIDE, FAKE, FAKE, FAKE,
+                                              FAKE, 1.0, 1.0, 100, FAKE, 8, o.get("lens", FAKE), 0.0625, 1, FAKE,
+                                              None, None, None, None, None)
+    assert vl(lens=None) == E.QKV_ERR_ARG
+    assert vl(lens=FAKE + 2) == E.QKV_ERR_ALIGN
+    assert vl(rows=0) == E.QKV_OK
