@@ -403,8 +403,23 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     return mask;
   };
 
-  // Start the first tiles' index loads and copies before staging the query, so their
-  // latencies overlap the query's.
+  // The query's global loads go out first, then the first tiles' index loads and copies: the
+  // copies wait for their indices, and the query's latency overlaps both.
+  constexpr int kW = HD / 16;  // query: 32-bit words (two head dims each) per thread
+  const int qh = tid >> 3, part = tid & 7;
+  const bool live = qh < Gc;
+  uint32_t w[kW];
+  if (live) {
+    const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + hq0 + qh) * HD + (HD / 8) * part);
+#pragma unroll
+    for (int i = 0; i < kW / 4; ++i) {
+      const uint4 x = __ldg(p + i);
+      w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < kW; ++i) w[i] = 0u;
+  }
   // index pipeline: nidx = tile i + 1's entry (slot id, or position when paged); paged also
   // carries nblk = its block id and ppos = tile i + 2's position
   // The prologue issues tiles 0 .. STAGES - 2 (one commit group each) and loads tile
@@ -438,23 +453,9 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     }
   }
 
-  // ---------------- stage the query once: 8 threads per head, HD / 8 head dims each
+  // ---------------- stage the query once: 8 threads per head, HD / 8 head dims each (its
+  // global loads were issued before the first tile's copies, see above)
   {
-    constexpr int kW = HD / 16;  // 32-bit words (two head dims each) per thread
-    const int qh = tid >> 3, part = tid & 7;
-    const bool live = qh < Gc;
-    uint32_t w[kW];
-    if (live) {
-      const uint4* p = reinterpret_cast<const uint4*>(a.q + (r * Hq + hq0 + qh) * HD + (HD / 8) * part);
-#pragma unroll
-      for (int i = 0; i < kW / 4; ++i) {
-        const uint4 x = __ldg(p + i);
-        w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < kW; ++i) w[i] = 0u;
-    }
     int sg = 0;
     if (!F::kBf16) {
       // fp16 operands: a power of two puts the head's largest |q| in [2^14, 2^15)
@@ -930,7 +931,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   __syncthreads();
   // combine weights, once per CTA: thread (hh, part) owns head hh and a quarter of each half's
   // head dims; warp w's partial enters with exp2(m_w - M) 2^(its pre-scale) / l
-  const int hh = tid >> 3, part = tid & 7;
+  const int hh = qh;  // = tid >> 3; part = tid & 7 as in the query staging
   float wo[kWarps];
   float lse_h = -INFINITY;
   if (hh < Gc) {
