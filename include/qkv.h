@@ -35,6 +35,7 @@
 #ifndef QKV_H
 #define QKV_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -382,6 +383,60 @@ qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, i
                                  const int32_t* topk_pos, int topk, float softmax_scale,
                                  int num_splits, float* out, float* lse, float* o_part,
                                  float* lse_part, uint32_t* dev_status, void* stream);
+
+/*
+ * qsa_gather_attn_ex -- one entry point for every combination of the gather's options: the
+ * plain call's arguments plus, each optional, per-row lengths (varlen), a paged pool (block
+ * table), the fused split-K merge (arrival counters) and an IEEE-half query. The operations
+ * are those of qsa_gather_attn, qsa_gather_attn_varlen, qsa_gather_attn_paged,
+ * qsa_gather_attn_splitk_fused and qsa_gather_attn_f16 [INT8-PR §The finding worth
+ * upstreaming; HOIST-PR §Changes; E4M3-PR §Implementation scope, §Purpose], and the same
+ * arguments mean the same things, with the same errors.
+ *   size        sizeof(qsa_gather_desc), for the layout check (else QKV_ERR_ARG).
+ *   q_fp16      0: bf16 query; 1: IEEE-half query (formats as for qsa_gather_attn_f16).
+ *   topk_len    NULL, or int32 [rows] valid entries per row (qsa_gather_attn_varlen).
+ *   block_table NULL, or a paged pool (qsa_gather_attn_paged: num_seqs, max_blocks,
+ *               block_size, row_seq); topk_idx then holds positions. Paged pools take a bf16
+ *               query (q_fp16 = 1 with a block table is QKV_ERR_ARG).
+ *   counters    NULL, or the fused merge's arrival counters (qsa_gather_attn_splitk_fused);
+ *               with num_splits > 1, out (and optionally lse) then receive the merged result
+ *               and o_part / lse_part are the workspace.
+ */
+typedef struct {
+  size_t size;
+  const void* q;
+  int q_fp16;
+  int64_t rows;
+  int num_q_heads;
+  int num_kv_heads;
+  int head_dim;
+  qkv_format fmt;
+  const void* k_cache;
+  const void* v_cache;
+  const float* k_scale_tok;
+  const float* v_scale_tok;
+  float k_scale_layer;
+  float v_scale_layer;
+  int64_t num_slots;
+  const int32_t* topk_idx;
+  int topk;
+  float softmax_scale;
+  int num_splits;
+  float* out;
+  float* lse;
+  float* o_part;
+  float* lse_part;
+  uint32_t* dev_status;
+  const int32_t* topk_len;
+  const int32_t* block_table;
+  int64_t num_seqs;
+  int max_blocks;
+  int block_size;
+  const int32_t* row_seq;
+  uint32_t* counters;
+} qsa_gather_desc;
+
+qkv_status qsa_gather_attn_ex(const qsa_gather_desc* desc, void* stream);
 
 /* Static, human-readable name of a status code. Never NULL. */
 const char* qkv_status_str(qkv_status s);

@@ -64,6 +64,21 @@ lib.qkv_status_str.argtypes = [ctypes.c_int]
 lib.qkv_status_str.restype = ctypes.c_char_p
 
 
+class GatherDesc(ctypes.Structure):
+    """qsa_gather_desc of include/qkv.h, field for field."""
+    _fields_ = [("size", ctypes.c_size_t), ("q", _p), ("q_fp16", _i32), ("rows", _i64), ("num_q_heads", _i32),
+                ("num_kv_heads", _i32), ("head_dim", _i32), ("fmt", _i32), ("k_cache", _p), ("v_cache", _p),
+                ("k_scale_tok", _p), ("v_scale_tok", _p), ("k_scale_layer", _f32), ("v_scale_layer", _f32),
+                ("num_slots", _i64), ("topk_idx", _p), ("topk", _i32), ("softmax_scale", _f32),
+                ("num_splits", _i32), ("out", _p), ("lse", _p), ("o_part", _p), ("lse_part", _p),
+                ("dev_status", _p), ("topk_len", _p), ("block_table", _p), ("num_seqs", _i64),
+                ("max_blocks", _i32), ("block_size", _i32), ("row_seq", _p), ("counters", _p)]
+
+
+lib.qsa_gather_attn_ex.argtypes = [ctypes.POINTER(GatherDesc), _p]
+lib.qsa_gather_attn_ex.restype = ctypes.c_int
+
+
 class QKVError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
@@ -220,6 +235,46 @@ def qsa_gather_attn_varlen(q, fmt: int, k_cache, v_cache, topk_idx, topk_len, so
                                     _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), _ptr(dev_status),
                                     _stream(stream))
     _check("qsa_gather_attn_varlen", st)
+
+
+def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: float, *, num_kv_heads: int = 1,
+                       num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
+                       k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, num_splits: int = 1, out=None,
+                       lse=None, o_part=None, lse_part=None, dev_status=None, topk_len=None, block_table=None,
+                       row_seq=None, block_size: int = 0, counters=None, stream=None):
+    """Any combination of the gather's options in one call (see qsa_gather_attn_ex in qkv.h).
+
+    q bf16 or fp16 [R, Hq, D]; topk_len int32 [R] (varlen); block_table int32 [num_seqs,
+    max_blocks] with row_seq int32 [R] and block_size (paged: topk_idx holds positions);
+    counters [R, Hkv, ceil(G / 16)] (fused split-K merge into out / lse).
+    """
+    _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
+    R, Hq, D = q.shape
+    if topk_len is not None and (topk_len.numel() != R or topk_len.dtype != torch.int32):
+        raise ValueError(f"topk_len must be int32 [{R}]")
+    if block_table is not None and (block_table.dim() != 2 or row_seq is None or row_seq.numel() != R):
+        raise ValueError(f"block_table must be [num_seqs, max_blocks] with row_seq [{R}]")
+    if counters is not None and counters.numel() != R * num_kv_heads * ((Hq // num_kv_heads + 15) // 16):
+        raise ValueError("counters must hold rows x num_kv_heads x ceil(G / 16) entries")
+    d = GatherDesc()
+    d.size = ctypes.sizeof(GatherDesc)
+    d.q, d.q_fp16, d.rows, d.num_q_heads, d.num_kv_heads, d.head_dim = _ptr(q), int(q.dtype == torch.float16), R, Hq, \
+        num_kv_heads, D
+    d.fmt, d.k_cache, d.v_cache = fmt, _ptr(k_cache), _ptr(v_cache)
+    d.k_scale_tok, d.v_scale_tok = _ptr(k_scale_tok), _ptr(v_scale_tok)
+    d.k_scale_layer, d.v_scale_layer = float(k_scale_layer), float(v_scale_layer)
+    d.num_slots = k_cache.shape[0] if num_slots is None else num_slots
+    d.topk_idx, d.topk, d.softmax_scale, d.num_splits = _ptr(topk_idx), topk_idx.shape[1], float(softmax_scale), \
+        num_splits
+    d.out, d.lse, d.o_part, d.lse_part, d.dev_status = _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), \
+        _ptr(dev_status)
+    d.topk_len, d.counters = _ptr(topk_len), _ptr(counters)
+    if block_table is not None:
+        d.block_table, d.num_seqs, d.max_blocks, d.block_size = _ptr(block_table), block_table.shape[0], \
+            block_table.shape[1], int(block_size)
+        d.row_seq = _ptr(row_seq)
+    st = lib.qsa_gather_attn_ex(ctypes.byref(d), _stream(stream))
+    _check("qsa_gather_attn_ex", st)
 
 
 def qsa_gather_attn_paged(q, fmt: int, k_cache, v_cache, block_table, row_seq, topk_pos, block_size: int,

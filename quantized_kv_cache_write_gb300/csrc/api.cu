@@ -375,6 +375,19 @@ qkv_status qsa_suggest_num_splits(qkv_format fmt, int64_t rows, int num_q_heads,
   return QKV_OK;
 }
 
+qkv_status qsa_gather_attn_ex(const qsa_gather_desc* d, void* stream) {
+  if (d == nullptr || d->size != sizeof(qsa_gather_desc)) return QKV_ERR_ARG;
+  if (d->q_fp16 != 0 && d->q_fp16 != 1) return QKV_ERR_ARG;
+  const bool paged = d->block_table != nullptr;
+  if (!paged && d->row_seq != nullptr) return QKV_ERR_ARG;
+  const Paging pg{d->block_table, d->row_seq, d->num_seqs, d->max_blocks, d->block_size};
+  uint32_t* counters = d->num_splits > 1 ? d->counters : nullptr;  // an unsplit call merges nothing
+  return gather_impl(d->q, d->rows, d->num_q_heads, d->num_kv_heads, d->head_dim, d->fmt, d->k_cache, d->v_cache,
+                     d->k_scale_tok, d->v_scale_tok, d->k_scale_layer, d->v_scale_layer, d->num_slots, d->topk_idx,
+                     d->topk, d->softmax_scale, d->num_splits, d->out, d->lse, d->o_part, d->lse_part, d->dev_status,
+                     stream, paged ? &pg : nullptr, counters, d->q_fp16 != 0, d->topk_len);
+}
+
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows, int num_q_heads,
                             int head_dim, int num_splits, float v_scale_post, float* out, float* lse,
                             void* stream) {

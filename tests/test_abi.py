@@ -244,3 +244,45 @@ def test_varlen_host_validation(lib):
     assert vl(lens=None) == E.QKV_ERR_ARG
     assert vl(lens=FAKE + 2) == E.QKV_ERR_ALIGN
     assert vl(rows=0) == E.QKV_OK
+
+
+def test_gather_desc_layout_matches_the_header(lib, tmp_path):
+    """The binding's ctypes mirror of qsa_gather_desc has the C compiler's field offsets."""
+    import ctypes
+    import shutil
+    import subprocess
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [f[0] for f in lib.GatherDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "qkv.h"\nint main(void) {\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(qsa_gather_desc, {n}));\n' for n in names)
+                   + '  printf("%zu\\n", sizeof(qsa_gather_desc));\n  return 0;\n}\n')
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [getattr(lib.GatherDesc, n).offset for n in names] + [ctypes.sizeof(lib.GatherDesc)]
+    assert got == want
+
+
+def test_gather_ex_host_validation(lib):
+    import ctypes
+    E, L = lib, lib.lib
+    d = lib.GatherDesc()
+    d.size = ctypes.sizeof(d)
+    d.q, d.rows, d.num_q_heads, d.num_kv_heads, d.head_dim, d.fmt = FAKE, 4, 16, 1, 256, E.QKV_INT8_SIDE
+    d.k_cache = d.v_cache = d.k_scale_tok = d.v_scale_tok = d.topk_idx = d.out = FAKE
+    d.num_slots, d.topk, d.softmax_scale, d.num_splits = 100, 8, 0.0625, 1
+    d.rows = 0
+    assert L.qsa_gather_attn_ex(ctypes.byref(d), None) == E.QKV_OK
+    d.size = 8
+    assert L.qsa_gather_attn_ex(ctypes.byref(d), None) == E.QKV_ERR_ARG  # layout check
+    d.size = ctypes.sizeof(d)
+    d.q_fp16 = 2
+    assert L.qsa_gather_attn_ex(ctypes.byref(d), None) == E.QKV_ERR_ARG
+    d.q_fp16, d.rows, d.row_seq = 0, 4, FAKE  # row_seq without a block table
+    assert L.qsa_gather_attn_ex(ctypes.byref(d), None) == E.QKV_ERR_ARG
+    d.row_seq, d.block_table, d.num_seqs, d.max_blocks, d.block_size, d.q_fp16 = FAKE, FAKE, 2, 8, 16, 1
+    assert L.qsa_gather_attn_ex(ctypes.byref(d), None) == E.QKV_ERR_ARG  # paged pools take a bf16 query
+    assert L.qsa_gather_attn_ex(None, None) == E.QKV_ERR_ARG
