@@ -76,10 +76,15 @@ def load_peak():
 
 
 def kernel_source_hash() -> str:
+    """sha256[:16] of the gather kernel's code: its sources with comments and blank lines
+    removed, so that an edit of the comments alone keeps the recorded profile valid."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "quantized_kv_cache_write_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "quantized_kv_cache_write_gb300", "csrc", name)) as f:
+            for line in f:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

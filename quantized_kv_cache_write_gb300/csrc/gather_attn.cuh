@@ -21,10 +21,16 @@
 // (Bulk copies on the TMA engine, one 256 B row each, were measured slower on this access
 // pattern: 6.4 vs 4.8 TB/s of gathered rows with the math removed.)
 //
-// Accumulators: each warp's 16 x 256 fp32 p.V accumulator lives in tensor memory (TMEM,
-// 32 lanes x 128 columns per warp) and streams through registers a quarter at a time around
-// the MMAs. Registers are what bound this kernel's occupancy; holding the accumulator in
-// TMEM leaves room for three CTAs (12 warps) per SM instead of two.
+// Accumulators: each warp's 16 x HD fp32 p.V accumulator lives in tensor memory (TMEM,
+// 32 lanes x HD / 2 columns per warp) and streams through registers 128 head dims at a time
+// around the MMAs. Registers are what bound this kernel's occupancy; holding the accumulator
+// in TMEM leaves room for three CTAs (12 warps) per SM instead of two.
+//
+// Variants (template parameters): the layout; PAGED (positions through a block table); the
+// ring depth and CTAs per SM; QF16 (an IEEE-half query, for the FP16-activation contract of
+// the calibrated E4M3 page, and the unquantised fp16 pool); HD (head dim 256 or 128). Run-time
+// options: per-row lengths (varlen: columns past a row's length are never read) and the fused
+// split-K merge (arrival counters).
 //
 // Per 16-key tile and warp:
 //   q.K^T  mma.sync m16n8k16, M = the GQA group (16 query heads, padded), N = 8 keys, K = 16
@@ -41,8 +47,8 @@
 //          the m16k16 A layout) as an fp16 hi + lo pair (bf16 pair for the bf16 layout): with
 //          outlier tokens a row can be a near-even mix of two large V rows of opposite sign,
 //          and single-fp16 p would lose ~1e-3 of the result to cancellation. int8 p also
-//          carries the slot's V scale and a power of two keeping it a normal fp16. 32 N-tiles:
-//          N-tile 16 s + t, column n covers head dim 128 s + 16 n + t; two MMAs (hi, lo) each.
+//          carries the slot's V scale and a power of two keeping it a normal fp16. HD / 8
+//          N-tiles of 8 head dims, two MMAs (hi, lo) each.
 // The E4M3 V scale and the power-of-two pre-scale are applied once at the end; split partials
 // are written normalised, without the E4M3 V scale.
 #pragma once
