@@ -604,6 +604,26 @@ def _time_events(fn, flush, stream, reps):
     return sum(ms) / len(ms)
 
 
+def _time_graph(fn, flush, stream, reps):
+    """Mean device time in ms of one replay of a CUDA graph captured from fn() (L2 flushed
+    before every replay). fn runs eagerly first, on the capture's side stream too."""
+    import torch
+    fn()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    ms = _time_events(g.replay, flush, stream, reps)
+    del g
+    return ms
+
+
 def measure_workloads(q, flush, stream, reps, peak):
     """The pages' other workload shapes, gather path only (context; the metric is the page-1 shape).
 
@@ -638,32 +658,55 @@ def measure_workloads(q, flush, stream, reps, peak):
         def unsplit():
             q.qsa_gather_attn(qd, code, kc, vc, idx, wl.softmax_scale, out=out, **kw)
 
+        # the split count qsa_suggest_num_splits picks (one wave of resident CTAs), fused
+        Pa = q.qsa_suggest_num_splits(code, R, Hq, wl.num_kv_heads, wl.topk.shape[1])
+        o_pa = torch.empty((R, Pa, Hq, D), dtype=torch.float32, device="cuda")
+        l_pa = torch.empty((R, Pa, Hq), dtype=torch.float32, device="cuda")
+        cnt_a = torch.zeros((R, wl.num_kv_heads), dtype=torch.int32, device="cuda")
+
+        def fused_suggested():
+            q.qsa_gather_attn_splitk_fused(qd, code, kc, vc, idx, wl.softmax_scale, num_splits=Pa, out=out,
+                                           o_part=o_pa, lse_part=l_pa, counters=cnt_a, **kw)
+
         t = {"split_plus_merge_ms": _time_events(two, flush, stream, reps),
              "fused_ms": _time_events(fused, flush, stream, reps),
              "unsplit_ms": _time_events(unsplit, flush, stream, reps)}
-        return t, (qd, idx, out)
+        return t, (qd, idx, out), {"fused": fused, "fused_suggested": fused_suggested, "suggested_splits": Pa}
 
     # calibrated E4M3 split-K: 12 layers, each its own 131072-slot pool
-    per_layer = []
+    per_layer, fns = [], []
     for layer in range(E4M3_SPLITK_LAYERS):
         wl = e4m3_splitk_layer(layer)
         kc, vc, kw, vpost = _device_pool(q, wl, "e4m3")
-        t, _ = split_variants(wl, "e4m3", kc, vc, kw, vpost)
+        t, _, f = split_variants(wl, "e4m3", kc, vc, kw, vpost)
         per_layer.append(t)
+        fns.append(f)  # keeps this layer's pool and buffers alive for the graph below
         del kc, vc
     tot = {k: sum(t[k] for t in per_layer) for k in per_layer[0]}
     bytes_layer = 64 * 2051 * SLOT_BYTES["e4m3"]
+    # all 12 layers' fused launches as one CUDA graph, replayed after one L2 flush: a decode
+    # step's attention over the layers without a host launch or an event between layers
+    graph = {}
+    for name in ("fused", "fused_suggested"):
+        graph[name + "_ms"] = _time_graph(lambda name=name: [f[name]() for f in fns], flush, stream, reps)
     res["e4m3_splitk_12_layers"] = {
         "shape": "12 layers x (64 rows, top-k 2051, 8 splits) over 131072-slot E4M3 pools, 16 query heads",
         "sum_ms": {k: round(v, 5) for k, v in tot.items()},
         "per_layer_ms": {k: [round(t[k], 5) for t in per_layer] for k in per_layer[0]},
         "fused_gathered_GBps": round(E4M3_SPLITK_LAYERS * bytes_layer / (tot["fused_ms"] * 1e-3) / 1e9, 2),
-        "note": "each layer timed alone after an L2 flush"}
+        "note": "each layer timed alone after an L2 flush",
+        "graph_12_layers_ms": {k: round(v, 5) for k, v in graph.items()},
+        "graph_suggested_splits": fns[0]["suggested_splits"],
+        "graph_fused_gathered_GBps": round(E4M3_SPLITK_LAYERS * bytes_layer / (graph["fused_ms"] * 1e-3) / 1e9, 2),
+        "graph_fused_suggested_gathered_GBps": round(
+            E4M3_SPLITK_LAYERS * bytes_layer / (graph["fused_suggested_ms"] * 1e-3) / 1e9, 2),
+        "graph_note": "one CUDA graph of the 12 layers' fused launches, L2 flushed once before each replay"}
+    del fns
 
     # long-context decode: 8 x 131072 tokens, 40 rows x top-k 2048, 16 splits; also the paged kernel
     wl = long_context_decode(3)
     kc, vc, kw, vpost = _device_pool(q, wl, "int8_side")
-    t, (qd, idx, out) = split_variants(wl, "int8_side", kc, vc, kw, vpost)
+    t, (qd, idx, out), _ = split_variants(wl, "int8_side", kc, vc, kw, vpost)
     table = torch.from_numpy(np.ascontiguousarray(wl.block_table, dtype=np.int32)).cuda()
     rs = torch.from_numpy(np.ascontiguousarray(wl.row_seq, dtype=np.int32)).cuda()
     pos = torch.from_numpy(np.ascontiguousarray(wl.topk_pos, dtype=np.int32)).cuda()

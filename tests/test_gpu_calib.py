@@ -97,3 +97,65 @@ def test_calibrated_scale_agrees_with_qkv_e4m3_calibrate():
     _, st = _gpu_stats([wl.k_tokens.ravel()])
     assert np.float32(st["scale"]) == sc.cpu().numpy()[0]
     assert st["saturated"] == 0
+
+
+def _crafted_histogram(seed, dtype):
+    """A sparse histogram with counts on bins at row (32), warp-range (1024) and finite /
+    non-finite edges, and the magnitudes it counts, each with a random sign."""
+    rng = np.random.default_rng(seed)
+    fnf = 0x7F80 if dtype == "bf16" else 0x7C00  # first non-finite magnitude
+    edges = np.array([0, 1, 31, 32, 33, 1023, 1024, 1025, 2047, 2048, 16383, 16384, fnf - 1, fnf, fnf + 1, 32767])
+    bins = np.unique(np.concatenate([edges[rng.random(edges.size) < 0.7], rng.integers(0, 32768, 40)]))
+    counts = rng.integers(1, 2000, bins.size)
+    hist = np.zeros(32768, dtype=np.int64)
+    hist[bins] = counts
+    bits = np.repeat(bins.astype(np.uint16), counts)
+    bits |= (rng.integers(0, 2, bits.size).astype(np.uint16) << np.uint16(15))
+    return hist, bits
+
+
+def _bin_f32(b, dtype):
+    if dtype == "bf16":
+        return np.array([b << 16], dtype=np.uint32).view(np.float32)[0]
+    return np.float32(np.array([b], dtype=np.uint16).view(np.float16)[0])
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("seed", range(6))
+def test_stats_of_crafted_histograms(dtype, seed):
+    """The stats pass alone, fed histograms built on the host: ranks and class edges that fall
+    on row and warp-range boundaries, scales that put a bin exactly on 2^-9 or 2^-6 or next
+    to 464, and scales that put every element in one class."""
+    import quantized_kv_cache_write_gb300 as q
+    hist, bits = _crafted_histogram(100 + seed, dtype)
+    fnf = 0x7F80 if dtype == "bf16" else 0x7C00
+    finite = np.nonzero(hist[1:fnf])[0] + 1
+    rng = np.random.default_rng(seed)
+    b = int(rng.choice(finite))
+    v = _bin_f32(b, dtype)
+    scales = [0.0, 1.0, float(v * np.float32(512.0)), float(v * np.float32(64.0)), float(v / np.float32(464.0)),
+              1e-30, 1e30]
+    hd = torch.from_numpy(hist).cuda()
+    buf = torch.full((8,), -1, dtype=torch.int64, device="cuda")
+    for scale in scales:
+        if not (np.isfinite(scale) and scale >= 0.0):
+            continue
+        q.qkv_calib_stats(hd, buf, scale, dtype=torch.float16 if dtype == "f16" else torch.bfloat16)
+        torch.cuda.synchronize()
+        _compare(q.decode_calib_stats(buf), calibration_stats(bits, None if scale == 0.0 else scale, dtype=dtype))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_stats_of_only_non_finite_values(dtype):
+    import quantized_kv_cache_write_gb300 as q
+    fnf = 0x7F80 if dtype == "bf16" else 0x7C00
+    hist = np.zeros(32768, dtype=np.int64)
+    hist[[fnf, fnf + 5, 32767]] = [3, 2, 1]
+    bits = np.repeat(np.array([fnf, fnf + 5, 32767], dtype=np.uint16), [3, 2, 1])
+    buf = torch.full((8,), -1, dtype=torch.int64, device="cuda")
+    for scale in (0.0, 2.0):
+        q.qkv_calib_stats(torch.from_numpy(hist).cuda(), buf, scale,
+                          dtype=torch.float16 if dtype == "f16" else torch.bfloat16)
+        got = q.decode_calib_stats(buf)
+        _compare(got, calibration_stats(bits, None if scale == 0.0 else scale, dtype=dtype))
+        assert got["count"] == 0 and got["nonfinite"] == 6 and got["p99_9"] == 0.0
