@@ -789,6 +789,33 @@ def measure_workloads(q, flush, stream, reps, peak):
         "histogram_GBps": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9, 2),
         "histogram_frac_of_hbm_peak": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9 / peak, 4)}
     del x
+
+    # pool fill: the page-1 pool's 262144 new tokens written in one call (HBM-bound at this size;
+    # per token 1024 B of bf16 K and V read, 2 x 260 B (int8 + scale) or 2 x 256 B (E4M3) written)
+    from gen import page1_shape
+    wl = page1_shape(1, with_step=False)
+    k_tok, v_tok = bf(wl.k_tokens), bf(wl.v_tokens)
+    slots = torch.from_numpy(wl.slot_mapping).cuda()
+    T, S = wl.k_tokens.shape[0], wl.num_slots
+    kc = torch.zeros((S, 1, HEAD_DIM), dtype=torch.int8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks = torch.zeros((S, 1), dtype=torch.float32, device="cuda")
+    vs = torch.zeros_like(ks)
+    w8 = _time_events(lambda: q.qkv_write_int8(k_tok, v_tok, slots, kc, vc, ks, vs), flush, stream, reps)
+    del kc, vc, ks, vs
+    ec = torch.zeros((S, 1, HEAD_DIM), dtype=torch.uint8, device="cuda")
+    evc = torch.zeros_like(ec)
+    we = _time_events(lambda: q.qkv_write_e4m3(k_tok, v_tok, slots, ec, evc, 0.01, 0.01), flush, stream, reps)
+    b8, be = T * (1024 + 520), T * (1024 + 512)
+    res["pool_fill"] = {
+        "shape": f"{T} bf16 tokens (1 KV head x 256, K and V) written into a {S}-slot pool in one call",
+        "write_int8_side_ms": round(w8, 5), "write_e4m3_ms": round(we, 5),
+        "write_int8_side_GBps": round(b8 / (w8 * 1e-3) / 1e9, 2),
+        "write_e4m3_GBps": round(be / (we * 1e-3) / 1e9, 2),
+        "write_int8_side_frac_of_hbm_peak": round(b8 / (w8 * 1e-3) / 1e9 / peak, 4),
+        "write_e4m3_frac_of_hbm_peak": round(be / (we * 1e-3) / 1e9 / peak, 4)}
+    del ec, evc, k_tok, v_tok
+    torch.cuda.empty_cache()
     return res
 
 

@@ -110,12 +110,18 @@ _ACT16 = (torch.bfloat16, torch.float16)
 
 
 def _tokens(k: torch.Tensor, v: torch.Tensor):
-    """[T, Hkv, D] views sharing one token stride; heads and dims contiguous."""
+    """[T, Hkv, D] views sharing one token stride; heads and dims contiguous. (The stride of a
+    dimension of size 1 is never used, so it may be anything.)"""
     if k.dim() != 3 or k.shape != v.shape or k.dtype not in _ACT16 or v.dtype != k.dtype:
         raise ValueError("k and v must be bf16 (or both fp16) [num_tokens, num_kv_heads, head_dim] of equal shape")
-    if k.stride(2) != 1 or k.stride(1) != k.shape[2] or v.stride()[1:] != k.stride()[1:] or k.stride(0) != v.stride(0):
+    T, H, D = k.shape
+
+    def heads_contiguous(t):
+        return (D == 1 or t.stride(2) == 1) and (H == 1 or t.stride(1) == D)
+
+    if not (heads_contiguous(k) and heads_contiguous(v)) or (T > 1 and k.stride(0) != v.stride(0)):
         raise ValueError("k and v need contiguous heads and one shared token stride")
-    return k.shape[0], k.shape[1], k.shape[2], k.stride(0)
+    return T, H, D, (k.stride(0) if T > 1 else H * D)
 
 
 def qkv_write_int8(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None, *,

@@ -8,10 +8,11 @@
 // "Qwen3.8 Flash Next NVFP4 QSA FP8 E4M3 KV Scales" §Calibration (stored = e4m3fn(x/scale),
 // scale = max envelope / 448).
 //
-// One warp owns one (token, head, tensor): 32 lanes x 8 values = a 256-wide head vector, read
-// as one coalesced line (head_dim 128: lanes 16..31 idle); the absmax is a 5-step shuffle
-// reduction; the codes leave as one coalesced line. Division is IEEE (__fdiv_rn) and rounding is
-// round-to-nearest-even so the stored bytes equal a plain fp32 reference bit for bit.
+// One warp owns one (token, head) row of K or V, or both rows when the write is large: 32 lanes
+// x 8 values = a 256-wide head vector, read as one coalesced line (head_dim 128: lanes 16..31
+// idle); the absmax is a 5-step shuffle reduction; the codes leave as one coalesced line.
+// Division is IEEE (__fdiv_rn) and rounding is round-to-nearest-even, so the stored bytes
+// equal a plain fp32 reference bit for bit.
 #include "qkv_internal.cuh"
 
 namespace qkv {
@@ -23,14 +24,18 @@ struct HeadVec {
   float x[8];
 };
 
-// Eight consecutive 16-bit activations (bf16, or IEEE half when F16), widened exactly to fp32.
-template <bool F16>
-__device__ __forceinline__ HeadVec load_head8(const uint16_t* src) {
-  // Streaming read: the new tokens are consumed once.
+// Eight consecutive 16-bit activations (bf16, or IEEE half when F16), loaded raw (streaming:
+// the new tokens are consumed once) and widened exactly to fp32.
+__device__ __forceinline__ uint4 load_raw8(const uint16_t* src) {
   uint4 raw;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(raw.x), "=r"(raw.y), "=r"(raw.z), "=r"(raw.w)
                : "l"(src));
+  return raw;
+}
+
+template <bool F16>
+__device__ __forceinline__ HeadVec widen8(const uint4& raw) {
   HeadVec h;
   const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -53,46 +58,71 @@ __device__ __forceinline__ float warp_max(float a) {
   return a;
 }
 
-// Decode the warp's work item: (token, head, is_v). Returns false when the token is skipped.
-__device__ __forceinline__ bool decode_item(int64_t item, int num_heads, const int64_t* slot_mapping,
-                                            int64_t num_slots, uint32_t* dev_status, int lane,
-                                            int64_t& t, int& h, int& is_v, int64_t& slot) {
-  is_v = static_cast<int>(item & 1);
-  const int64_t th = item >> 1;
-  t = th / num_heads;
-  h = static_cast<int>(th - t * num_heads);
-  slot = slot_mapping[t];
+// Large writes pair a token head's K and V rows in one warp (two row loads in flight per
+// lane, one slot load for both); small ones give each row its own warp, twice the warps to
+// spread a latency-bound launch over. Measured on one GB300 (int8 side / E4M3): 262144 tokens
+// 143 -> 120 / 113 -> 91 us paired; 2048 tokens 8-9 / 7 us either way.
+constexpr int64_t kPairedMinUnits = 16384;  // (token, head) units from which rows are paired
+
+// The (token t, head h) of a unit. 32-bit division whenever the index fits, which it does at
+// any realistic size (64-bit division is several times longer).
+__device__ __forceinline__ void decode_unit(int64_t unit, int num_heads, int64_t& t, int& h) {
+  if (unit <= 0xFFFFFFFFll) {
+    const uint32_t t32 = static_cast<uint32_t>(unit) / static_cast<uint32_t>(num_heads);
+    t = t32;
+    h = static_cast<int>(static_cast<uint32_t>(unit) - t32 * static_cast<uint32_t>(num_heads));
+  } else {
+    t = unit / num_heads;
+    h = static_cast<int>(unit - t * num_heads);
+  }
+}
+
+// Whether a token's slot is written: false when it is skipped (-1) or out of range (flagged by
+// lane 0 of the warp that `flags`, one per token).
+__device__ __forceinline__ bool slot_ok(int64_t slot, int64_t num_slots, uint32_t* dev_status, int lane, bool flags) {
   if (slot == -1) return false;
   if (slot < -1 || slot >= num_slots) {
-    if (lane == 0 && is_v == 0 && h == 0 && dev_status != nullptr) atomicOr(dev_status, QKV_DEV_BAD_SLOT);
+    if (lane == 0 && flags && dev_status != nullptr) atomicOr(dev_status, QKV_DEV_BAD_SLOT);
     return false;
   }
   return true;
 }
 
-template <bool kInline, bool F16>
-__global__ void __launch_bounds__(kWriteThreads)
-    write_int8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
-                      int64_t num_tokens, int num_heads, int64_t token_stride,
-                      const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
-                      uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
-                      float* __restrict__ v_scale, int64_t num_slots, uint32_t* dev_status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * kWriteThreads + threadIdx.x) >> 5;
-  if (item >= num_tokens * num_heads * 2) return;
-  int64_t t, slot;
-  int h, is_v;
-  if (!decode_item(item, num_heads, slot_mapping, num_slots, dev_status, lane, t, h, is_v, slot)) return;
+// The warp's rows: one row (K or V: kv) of a (token, head) unit, or both rows of a unit when
+// paired. Every row and the slot are loaded before any is used, so the loads are in flight
+// together (a skipped token's rows are still in bounds: t < num_tokens). Returns false for a
+// warp past the end, a skipped token or a bad slot; the result is warp-uniform.
+template <bool kPaired>
+__device__ __forceinline__ bool warp_rows(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
+                                          int64_t num_tokens, int num_heads, int64_t token_stride,
+                                          const int64_t* __restrict__ slot_mapping, int64_t num_slots,
+                                          uint32_t* dev_status, int lane, bool act, uint4 (&raw)[2], int& kv,
+                                          int64_t& rec) {
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * kWriteThreads + threadIdx.x) >> 5;
+  const int64_t unit = kPaired ? wid : wid >> 1;
+  if (unit >= num_tokens * num_heads) return false;
+  kv = kPaired ? 0 : static_cast<int>(wid & 1);
+  int64_t t;
+  int h;
+  decode_unit(unit, num_heads, t, h);
+  const int64_t off = t * token_stride + static_cast<int64_t>(h) * head_dim + lane * 8;
+  raw[0] = act ? load_raw8((kv ? v : k) + off) : make_uint4(0, 0, 0, 0);
+  if (kPaired) raw[1] = act ? load_raw8(v + off) : make_uint4(0, 0, 0, 0);
+  const int64_t slot = slot_mapping[t];
+  if (!slot_ok(slot, num_slots, dev_status, lane, kv == 0 && h == 0)) return false;
+  rec = slot * num_heads + h;
+  return true;
+}
 
-  const bool act = 8 * lane < head_dim;  // lane owns head dims 8 lane .. 8 lane + 7
-  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * head_dim + lane * 8;
-  const HeadVec hv = act ? load_head8<F16>(src) : HeadVec{};
+// int8 codes and scale of one head row into record `rec` of `cache` (and `scale_out`, side layout).
+template <bool kInline>
+__device__ __forceinline__ void store_int8_row(const HeadVec& hv, int lane, bool act, int head_dim, int64_t rec,
+                                               uint8_t* __restrict__ cache, float* __restrict__ scale_out) {
   float a = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(hv.x[i]));
   a = warp_max(a);
   const float scale = __fdiv_rn(a, 127.0f);
-
   uint32_t word[2] = {0u, 0u};
   if (scale > 0.f) {
 #pragma unroll
@@ -102,8 +132,6 @@ __global__ void __launch_bounds__(kWriteThreads)
       word[i >> 2] |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * (i & 3));
     }
   }
-  const int64_t rec = slot * num_heads + h;
-  uint8_t* cache = is_v ? v_cache : k_cache;
   if (kInline) {
     uint8_t* base = cache + rec * (head_dim + 4);  // head_dim codes, then the fp32 scale
     uint32_t* dst = reinterpret_cast<uint32_t*>(base + lane * 8);  // records are 4 B aligned
@@ -114,28 +142,13 @@ __global__ void __launch_bounds__(kWriteThreads)
     if (lane == 0) *reinterpret_cast<float*>(base + head_dim) = scale;
   } else {
     if (act) *reinterpret_cast<uint2*>(cache + rec * head_dim + lane * 8) = make_uint2(word[0], word[1]);
-    if (lane == 0) (is_v ? v_scale : k_scale)[rec] = scale;
+    if (lane == 0) scale_out[rec] = scale;
   }
 }
 
-template <bool F16>
-__global__ void __launch_bounds__(kWriteThreads)
-    write_e4m3_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
-                      int64_t num_tokens, int num_heads, int64_t token_stride,
-                      const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
-                      uint8_t* __restrict__ v_cache, float k_scale, float v_scale, int64_t num_slots,
-                      uint32_t* dev_status) {
-  const int lane = threadIdx.x & 31;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * kWriteThreads + threadIdx.x) >> 5;
-  if (item >= num_tokens * num_heads * 2) return;
-  int64_t t, slot;
-  int h, is_v;
-  if (!decode_item(item, num_heads, slot_mapping, num_slots, dev_status, lane, t, h, is_v, slot)) return;
-
-  if (8 * lane >= head_dim) return;  // head_dim 128: lanes 16..31 own no dims (no shuffles follow)
-  const uint16_t* src = (is_v ? v : k) + t * token_stride + static_cast<int64_t>(h) * head_dim + lane * 8;
-  const HeadVec hv = load_head8<F16>(src);
-  const float s = is_v ? v_scale : k_scale;
+// E4M3 codes of one head row (lanes that own dims only) into record `rec` of `cache`.
+__device__ __forceinline__ void store_e4m3_row(const HeadVec& hv, int lane, int head_dim, int64_t rec, float s,
+                                               uint8_t* __restrict__ cache) {
   uint32_t word[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
@@ -144,8 +157,47 @@ __global__ void __launch_bounds__(kWriteThreads)
     const uint32_t p = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
     word[i >> 2] |= (p & 0xFFFFu) << (8 * (i & 3));
   }
-  uint8_t* cache = is_v ? v_cache : k_cache;
-  *reinterpret_cast<uint2*>(cache + (slot * num_heads + h) * head_dim + lane * 8) = make_uint2(word[0], word[1]);
+  *reinterpret_cast<uint2*>(cache + rec * head_dim + lane * 8) = make_uint2(word[0], word[1]);
+}
+
+template <bool kInline, bool F16, bool kPaired>
+__global__ void __launch_bounds__(kWriteThreads)
+    write_int8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
+                      int64_t num_tokens, int num_heads, int64_t token_stride,
+                      const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
+                      uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
+                      float* __restrict__ v_scale, int64_t num_slots, uint32_t* dev_status) {
+  const int lane = threadIdx.x & 31;
+  const bool act = 8 * lane < head_dim;  // lane owns head dims 8 lane .. 8 lane + 7 (128: lanes 0..15)
+  uint4 raw[2];
+  int kv;
+  int64_t rec;
+  if (!warp_rows<kPaired>(k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, num_slots, dev_status,
+                          lane, act, raw, kv, rec))
+    return;
+  store_int8_row<kInline>(widen8<F16>(raw[0]), lane, act, head_dim, rec, kv ? v_cache : k_cache,
+                          kv ? v_scale : k_scale);
+  if (kPaired) store_int8_row<kInline>(widen8<F16>(raw[1]), lane, act, head_dim, rec, v_cache, v_scale);
+}
+
+template <bool F16, bool kPaired>
+__global__ void __launch_bounds__(kWriteThreads)
+    write_e4m3_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
+                      int64_t num_tokens, int num_heads, int64_t token_stride,
+                      const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
+                      uint8_t* __restrict__ v_cache, float k_scale, float v_scale, int64_t num_slots,
+                      uint32_t* dev_status) {
+  const int lane = threadIdx.x & 31;
+  const bool act = 8 * lane < head_dim;  // head_dim 128: lanes 16..31 own no dims (no shuffles follow)
+  uint4 raw[2];
+  int kv;
+  int64_t rec;
+  if (!warp_rows<kPaired>(k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, num_slots, dev_status,
+                          lane, act, raw, kv, rec) ||
+      !act)
+    return;
+  store_e4m3_row(widen8<F16>(raw[0]), lane, head_dim, rec, kv ? v_scale : k_scale, kv ? v_cache : k_cache);
+  if (kPaired) store_e4m3_row(widen8<F16>(raw[1]), lane, head_dim, rec, v_scale, v_cache);
 }
 
 // max |x| over n bf16 values, as fp32 bits (non-negative floats order like their bits).
@@ -181,8 +233,10 @@ __global__ void e4m3_scale_kernel(const uint32_t* __restrict__ amax_bits, float*
   scale_out[0] = __fdiv_rn(__uint_as_float(amax_bits[0]), 448.0f);
 }
 
+bool write_paired(int64_t num_tokens, int num_heads) { return num_tokens * num_heads >= kPairedMinUnits; }
+
 unsigned write_blocks(int64_t num_tokens, int num_heads) {
-  const int64_t warps = num_tokens * num_heads * 2;
+  const int64_t warps = num_tokens * num_heads * (write_paired(num_tokens, num_heads) ? 1 : 2);
   return static_cast<unsigned>((warps * 32 + kWriteThreads - 1) / kWriteThreads);
 }
 
@@ -199,8 +253,12 @@ cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int head_d
   auto vc = static_cast<uint8_t*>(v_cache);
   float* ks = inline_layout ? nullptr : k_scale;
   float* vs = inline_layout ? nullptr : v_scale;
-  auto kern = inline_layout ? (f16 ? write_int8_kernel<true, true> : write_int8_kernel<true, false>)
-                            : (f16 ? write_int8_kernel<false, true> : write_int8_kernel<false, false>);
+  const bool pr = write_paired(num_tokens, num_heads);
+  auto kern = inline_layout
+                  ? (f16 ? (pr ? write_int8_kernel<true, true, true> : write_int8_kernel<true, true, false>)
+                         : (pr ? write_int8_kernel<true, false, true> : write_int8_kernel<true, false, false>))
+                  : (f16 ? (pr ? write_int8_kernel<false, true, true> : write_int8_kernel<false, true, false>)
+                         : (pr ? write_int8_kernel<false, false, true> : write_int8_kernel<false, false, false>));
   kern<<<blocks, kWriteThreads, 0, stream>>>(kk, vv, head_dim, num_tokens, num_heads, token_stride, slot_mapping, kc,
                                              vc, ks, vs, num_slots, dev_status);
   return cudaGetLastError();
@@ -210,7 +268,9 @@ cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int head_d
                               int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
                               void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream) {
-  auto kern = f16 ? write_e4m3_kernel<true> : write_e4m3_kernel<false>;
+  const bool pr = write_paired(num_tokens, num_heads);
+  auto kern = f16 ? (pr ? write_e4m3_kernel<true, true> : write_e4m3_kernel<true, false>)
+                  : (pr ? write_e4m3_kernel<false, true> : write_e4m3_kernel<false, false>);
   kern<<<write_blocks(num_tokens, num_heads), kWriteThreads, 0, stream>>>(
       static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), head_dim, num_tokens, num_heads, token_stride,
       slot_mapping, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale, v_scale, num_slots,

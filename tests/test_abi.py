@@ -143,6 +143,22 @@ def test_binding_rejects_buffers_that_disagree_with_q(lib):
                                            out=torch.zeros((2, 16, 256)))
 
 
+def test_token_views_ignore_the_strides_of_unit_dimensions(lib):
+    """A dimension of size 1 is never stepped over, so its stride (0 for a broadcast view) does
+    not matter; real mismatches are still refused."""
+    import torch
+    base = torch.zeros((5, 256), dtype=torch.bfloat16)
+    k = base.as_strided((5, 1, 256), (256, 0, 1))
+    assert lib._tokens(k, k) == (5, 1, 256, 256)
+    one = base.as_strided((1, 1, 256), (0, 0, 1))
+    assert lib._tokens(one, one) == (1, 1, 256, 256)
+    two = torch.zeros((5, 2, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        lib._tokens(two.transpose(0, 1).contiguous().transpose(0, 1), two)  # heads not contiguous
+    with pytest.raises(ValueError):
+        lib._tokens(torch.zeros((5, 1, 512), dtype=torch.bfloat16)[:, :, :256], k)  # token strides differ
+
+
 def _gather_paged(lib, **over):
     a = dict(q=FAKE, rows=4, hq=16, hkv=1, d=256, fmt=lib.QKV_INT8_SIDE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE,
              ksl=1.0, vsl=1.0, S=100, bt=FAKE, nseq=2, mb=8, bs=16, rs=FAKE, pos=FAKE, topk=8, sm=0.0625, P=1,
