@@ -19,6 +19,8 @@
 // HBM-bound: 2 bytes read per element.
 // stats: one CTA of 32 warps, each reading a 1024-bin range in coalesced rows; the class
 // edges and the rank bins are then located by a few warps at once.
+#include <atomic>
+
 #include "qkv_internal.cuh"
 
 namespace qkv {
@@ -261,32 +263,34 @@ __global__ void __launch_bounds__(kStatsWarps * 32) calib_stats_kernel(const uns
   }
 }
 
+// Per-device caches below are atomic: host threads may race on a device's first call, and
+// both then store the same value.
 int sm_count_cached() {
-  static int count[64] = {};
+  static std::atomic<int> count[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (count[dev] == 0) {
-    int c = 0;
+  int c = count[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    count[dev] = c;
+    count[dev].store(c, std::memory_order_relaxed);
   }
-  return count[dev];
+  return c;
 }
 
 }  // namespace
 
 cudaError_t launch_calib_histogram(const void* x, int64_t n, uint64_t* hist, cudaStream_t stream) {
   if (n == 0) return cudaSuccess;
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   constexpr int smem = kBins * sizeof(uint32_t);
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(calib_hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   const int sms = sm_count_cached();
   if (sms <= 0) return cudaErrorInvalidDevice;

@@ -53,6 +53,7 @@
 // are written normalised, without the E4M3 V scale.
 #pragma once
 
+#include <atomic>
 #include "qkv_internal.cuh"
 
 namespace qkv {
@@ -1074,15 +1075,16 @@ inline int64_t gather_grid(const GatherArgs& a) {
   return a.rows * a.num_kv_heads * chunks * a.num_splits;
 }
 
-// Opt the kernel into its dynamic shared memory, once per device.
+// Opt the kernel into its dynamic shared memory, once per device. Host threads may race here on
+// a device's first call: both set the same attributes (idempotent), and the flags are atomic.
 template <int FMT, bool PAGED, int STAGES, int MINB, bool QF16 = false, int HD = 256>
 cudaError_t prepare_variant() {
-  static bool attr_done[64] = {};
+  static std::atomic<bool> attr_done[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
+  if (!attr_done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(Smem<FMT, HD, STAGES>::kTotal));
@@ -1092,7 +1094,7 @@ cudaError_t prepare_variant() {
     e = cudaFuncSetAttribute(gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>,
                              cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_done[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }
