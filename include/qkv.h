@@ -74,7 +74,8 @@ typedef enum {
  *
  *   k, v          bf16 [num_tokens, num_kv_heads, head_dim]; token t starts at element
  *                 t * token_stride (token_stride >= num_kv_heads*head_dim, a multiple of 8);
- *                 base pointers 16-byte aligned.
+ *                 base pointers 16-byte aligned. Every token's rows are read, a skipped
+ *                 token's too (its slot is loaded alongside them, not before).
  *   slot_mapping  int64 [num_tokens]. Slots must be distinct (duplicates race).
  *   layout        QKV_INT8_SIDE: k_cache/v_cache int8 [S,H,D] (16 B-aligned) and
  *                 k_scale/v_scale fp32 [S,H];
