@@ -72,6 +72,7 @@ typedef enum {
  *     c_d = clamp(rint(x_d / scale), -127, 127) with ties to even; amax == 0 stores scale 0
  *     and zero codes. Codes and scale go to slot slot_mapping[t]; -1 skips the token.
  *
+ *   num_tokens * num_kv_heads at most 2^32 (one launch), else QKV_ERR_ARG.
  *   k, v          bf16 [num_tokens, num_kv_heads, head_dim]; token t starts at element
  *                 t * token_stride (token_stride >= num_kv_heads*head_dim, a multiple of 8);
  *                 base pointers 16-byte aligned. Every token's rows are read, a skipped

@@ -21,6 +21,8 @@ qkv_status check_write_inputs(const void* k, const void* v, int64_t num_tokens, 
   if (num_tokens < 0 || num_slots < 0 || num_kv_heads < 1) return QKV_ERR_ARG;
   if (!qkv::head_dim_ok(head_dim)) return QKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return QKV_OK;
+  // one warp per head row: 2 T H warps of 32 threads must fit a grid of 2^31 - 1 blocks of 256
+  if (num_tokens > (int64_t(1) << 32) / num_kv_heads) return QKV_ERR_ARG;
   if (!k || !v || !slot_mapping || !k_cache || !v_cache) return QKV_ERR_ARG;
   if (token_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return QKV_ERR_ARG;
   if (token_stride % 8 != 0 || !aligned(k, 16) || !aligned(v, 16)) return QKV_ERR_ALIGN;

@@ -104,6 +104,7 @@ def test_write_host_validation(lib):
     assert w8(layout=E.QKV_INT8_INLINE) == E.QKV_ERR_ARG  # inline must not get scale pointers
     assert w8(ks=None) == E.QKV_ERR_ARG
     assert w8(T=-1) == E.QKV_ERR_ARG
+    assert w8(T=(1 << 32) + 1) == E.QKV_ERR_ARG  # more head rows than one launch's grid holds
     assert w8(T=0) == E.QKV_OK
 
 
