@@ -268,6 +268,7 @@ qkv_status qsa_gather_attn_f16(const void* q, int64_t rows, int num_q_heads, int
  *   o_part fp32 [rows, P, num_q_heads, head_dim], lse_part fp32 [rows, P, num_q_heads],
  *   out fp32 [rows, num_q_heads, head_dim], lse fp32 [rows, num_q_heads] or NULL.
  *   v_scale_post finite (1.0 for the non-E4M3 formats). head_dim 256 or 128.
+ *   rows * num_q_heads at most 2^32 (one launch), else QKV_ERR_ARG.
  */
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows,
                             int num_q_heads, int head_dim, int num_splits, float v_scale_post,

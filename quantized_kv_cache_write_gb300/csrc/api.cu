@@ -397,6 +397,7 @@ qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t 
   if (!qkv::head_dim_ok(head_dim)) return QKV_ERR_UNSUPPORTED;
   if (!std::isfinite(v_scale_post)) return QKV_ERR_ARG;
   if (rows == 0) return QKV_OK;
+  if (rows > (int64_t(1) << 32) / num_q_heads) return QKV_ERR_ARG;  // one warp per (row, head): one grid
   if (!o_part || !lse_part || !out) return QKV_ERR_ARG;
   if (!aligned(o_part, 16) || !aligned(out, 16) || !aligned(lse_part, 4) || (lse && !aligned(lse, 4)))
     return QKV_ERR_ALIGN;

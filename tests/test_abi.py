@@ -111,6 +111,7 @@ def test_write_host_validation(lib):
 def test_merge_and_calibrate_host_validation(lib):
     E, L = lib, lib.lib
     assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 192, 4, 1.0, FAKE, None, None) == E.QKV_ERR_UNSUPPORTED
+    assert L.qsa_splitk_merge(FAKE, FAKE, 1 << 29, 16, 256, 4, 1.0, FAKE, None, None) == E.QKV_ERR_ARG
     assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 256, 0, 1.0, FAKE, None, None) == E.QKV_ERR_ARG
     assert L.qsa_splitk_merge(FAKE, FAKE, 2, 16, 256, 4, float("inf"), FAKE, None, None) == E.QKV_ERR_ARG
     assert L.qsa_splitk_merge(FAKE + 4, FAKE, 2, 16, 256, 4, 1.0, FAKE, None, None) == E.QKV_ERR_ALIGN
