@@ -123,6 +123,58 @@ qkv_status qkv_write_e4m3_f16(const void* k, const void* v, int64_t num_tokens, 
                               int64_t num_slots, uint32_t* dev_status, void* stream);
 
 /*
+ * qkv_write_ex -- the writes with every option through one descriptor: the format (int8 side,
+ * int8 inline or E4M3), bf16 or IEEE-half tokens, and the slot addressing: slot ids
+ * (slot_mapping, as qkv_write_int8 / qkv_write_e4m3) or a paged pool, where token t sits at
+ * logical position token_pos[t] of sequence token_seq[t] and its slot is
+ *     block_table[seq, pos / block_size] * block_size + pos % block_size
+ * (the addressing qsa_gather_attn_paged reads; [E4M3-PR §Implementation scope]: the KV cache
+ * is paged storage). Arithmetic and stored bytes are those of qkv_write_int8 / qkv_write_e4m3.
+ *   size           sizeof(qkv_write_desc), for the layout check (else QKV_ERR_ARG).
+ *   fmt            QKV_INT8_SIDE (k_scale, v_scale fp32 [S, H]), QKV_INT8_INLINE (scale
+ *                  pointers NULL) or QKV_E4M3 (k_scale_layer, v_scale_layer finite and > 0,
+ *                  else QKV_ERR_SCALE; scale pointers NULL); anything else QKV_ERR_ARG.
+ *   act_fp16       0: k, v bf16; 1: IEEE half.
+ *   slot_mapping   int64 [num_tokens] slot ids, -1 = skip; NULL selects paged addressing, and
+ *                  then token_seq, token_pos (int32 [num_tokens]) and block_table (int32
+ *                  [num_seqs, max_blocks], < 0 = unallocated) are required (4 B-aligned),
+ *                  with block_size >= 1, max_blocks >= 1, num_seqs >= 1 and
+ *                  max_blocks * block_size < 2^31. Giving both addressings is QKV_ERR_ARG.
+ *                  A position of -1 skips the token. A position outside [-1, max_blocks *
+ *                  block_size), a sequence outside [0, num_seqs), an unallocated block or a
+ *                  slot outside [0, S) set QKV_DEV_BAD_SLOT and skip the token.
+ *   the rest       as for qkv_write_int8 / qkv_write_e4m3.
+ */
+typedef struct {
+  size_t size;
+  qkv_format fmt;
+  int act_fp16;
+  const void* k;
+  const void* v;
+  int64_t num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int64_t token_stride;
+  const int64_t* slot_mapping;
+  const int32_t* token_seq;
+  const int32_t* token_pos;
+  const int32_t* block_table;
+  int64_t num_seqs;
+  int max_blocks;
+  int block_size;
+  void* k_cache;
+  void* v_cache;
+  float* k_scale;
+  float* v_scale;
+  float k_scale_layer;
+  float v_scale_layer;
+  int64_t num_slots;
+  uint32_t* dev_status;
+} qkv_write_desc;
+
+qkv_status qkv_write_ex(const qkv_write_desc* desc, void* stream);
+
+/*
  * qkv_e4m3_calibrate -- per-tensor calibrated E4M3 scale = (max |x|) / 448 over n bf16
  * values, computed on the device.                             [SCALES §Calibration]
  *   x          bf16 [n], 16 B-aligned.

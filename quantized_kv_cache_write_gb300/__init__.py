@@ -79,6 +79,20 @@ lib.qsa_gather_attn_ex.argtypes = [ctypes.POINTER(GatherDesc), _p]
 lib.qsa_gather_attn_ex.restype = ctypes.c_int
 
 
+class WriteDesc(ctypes.Structure):
+    """qkv_write_desc of include/qkv.h, field for field."""
+    _fields_ = [("size", ctypes.c_size_t), ("fmt", _i32), ("act_fp16", _i32), ("k", _p), ("v", _p),
+                ("num_tokens", _i64), ("num_kv_heads", _i32), ("head_dim", _i32), ("token_stride", _i64),
+                ("slot_mapping", _p), ("token_seq", _p), ("token_pos", _p), ("block_table", _p),
+                ("num_seqs", _i64), ("max_blocks", _i32), ("block_size", _i32), ("k_cache", _p), ("v_cache", _p),
+                ("k_scale", _p), ("v_scale", _p), ("k_scale_layer", _f32), ("v_scale_layer", _f32),
+                ("num_slots", _i64), ("dev_status", _p)]
+
+
+lib.qkv_write_ex.argtypes = [ctypes.POINTER(WriteDesc), _p]
+lib.qkv_write_ex.restype = ctypes.c_int
+
+
 class QKVError(RuntimeError):
     def __init__(self, fn: str, status: int):
         self.status = status
@@ -143,6 +157,33 @@ def qkv_write_e4m3(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale
     st = getattr(lib, name)(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                             float(k_scale), float(v_scale), k_cache.shape[0], _ptr(dev_status), _stream(stream))
     _check(name, st)
+
+
+def qkv_write_ex(k, v, fmt: int, k_cache, v_cache, *, slot_mapping=None, token_seq=None, token_pos=None,
+                 block_table=None, block_size: int = 1, k_scale=None, v_scale=None, k_scale_layer: float = 1.0,
+                 v_scale_layer: float = 1.0, dev_status=None, stream=None):
+    """Any write through one descriptor (see qkv_write_ex in qkv.h): int8 side / inline or E4M3,
+    bf16 or fp16 tokens, slot ids (slot_mapping) or a paged pool (token_seq, token_pos int32
+    [T]; block_table int32 [num_seqs, max_blocks]; block_size)."""
+    T, H, D, stride = _tokens(k, v)
+    d = WriteDesc()
+    d.size = ctypes.sizeof(WriteDesc)
+    d.fmt, d.act_fp16 = int(fmt), int(k.dtype == torch.float16)
+    d.k, d.v, d.num_tokens, d.num_kv_heads, d.head_dim, d.token_stride = _ptr(k), _ptr(v), T, H, D, stride
+    d.slot_mapping, d.token_seq, d.token_pos = _ptr(slot_mapping), _ptr(token_seq), _ptr(token_pos)
+    d.block_table = _ptr(block_table)
+    if block_table is not None:
+        if block_table.dim() != 2:
+            raise ValueError("block_table must be [num_seqs, max_blocks]")
+        d.num_seqs, d.max_blocks, d.block_size = block_table.shape[0], block_table.shape[1], int(block_size)
+    for name, t in (("token_seq", token_seq), ("token_pos", token_pos)):
+        if t is not None and t.numel() != T:
+            raise ValueError(f"{name} must hold one entry per token ({T})")
+    d.k_cache, d.v_cache, d.k_scale, d.v_scale = _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale)
+    d.k_scale_layer, d.v_scale_layer = float(k_scale_layer), float(v_scale_layer)
+    d.num_slots, d.dev_status = k_cache.shape[0], _ptr(dev_status)
+    st = lib.qkv_write_ex(ctypes.byref(d), _stream(stream))
+    _check("qkv_write_ex", st)
 
 
 def qkv_e4m3_calibrate(x, amax_bits, scale_out, *, stream=None):

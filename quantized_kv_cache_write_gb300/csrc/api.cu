@@ -17,16 +17,25 @@ qkv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QKV_OK : QKV_E
 // Shared checks of the two write calls' token inputs.
 qkv_status check_write_inputs(const void* k, const void* v, int64_t num_tokens, int num_kv_heads,
                               int head_dim, int64_t token_stride, const int64_t* slot_mapping,
-                              const void* k_cache, const void* v_cache, int64_t num_slots) {
+                              const void* k_cache, const void* v_cache, int64_t num_slots,
+                              const qkv::WritePaging* pg = nullptr) {
   if (num_tokens < 0 || num_slots < 0 || num_kv_heads < 1) return QKV_ERR_ARG;
   if (!qkv::head_dim_ok(head_dim)) return QKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return QKV_OK;
   // one warp per head row: 2 T H warps of 32 threads must fit a grid of 2^31 - 1 blocks of 256
   if (num_tokens > (int64_t(1) << 32) / num_kv_heads) return QKV_ERR_ARG;
-  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return QKV_ERR_ARG;
+  if (!k || !v || !k_cache || !v_cache) return QKV_ERR_ARG;
+  if (pg == nullptr ? !slot_mapping : (!pg->token_seq || !pg->token_pos || !pg->block_table)) return QKV_ERR_ARG;
   if (token_stride < static_cast<int64_t>(num_kv_heads) * head_dim) return QKV_ERR_ARG;
   if (token_stride % 8 != 0 || !aligned(k, 16) || !aligned(v, 16)) return QKV_ERR_ALIGN;
-  if (!aligned(slot_mapping, 8)) return QKV_ERR_ALIGN;
+  if (pg == nullptr) {
+    if (!aligned(slot_mapping, 8)) return QKV_ERR_ALIGN;
+  } else {
+    if (pg->block_size < 1 || pg->max_blocks < 1 || pg->num_seqs < 1) return QKV_ERR_ARG;
+    if (static_cast<int64_t>(pg->max_blocks) * pg->block_size > INT32_MAX) return QKV_ERR_ARG;
+    if (!aligned(pg->token_seq, 4) || !aligned(pg->token_pos, 4) || !aligned(pg->block_table, 4))
+      return QKV_ERR_ALIGN;
+  }
   return QKV_OK;
 }
 
@@ -53,9 +62,9 @@ namespace {
 qkv_status write_int8_impl(const void* k, const void* v, bool f16, int64_t num_tokens, int num_kv_heads,
                            int head_dim, int64_t token_stride, const int64_t* slot_mapping, qkv_format layout,
                            void* k_cache, void* v_cache, float* k_scale, float* v_scale, int64_t num_slots,
-                           uint32_t* dev_status, void* stream) {
+                           uint32_t* dev_status, void* stream, const qkv::WritePaging* pg = nullptr) {
   qkv_status st = check_write_inputs(k, v, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping,
-                                     k_cache, v_cache, num_slots);
+                                     k_cache, v_cache, num_slots, pg);
   if (st != QKV_OK) return st;
   if (layout != QKV_INT8_SIDE && layout != QKV_INT8_INLINE) return QKV_ERR_ARG;
   const bool inl = layout == QKV_INT8_INLINE;
@@ -65,24 +74,24 @@ qkv_status write_int8_impl(const void* k, const void* v, bool f16, int64_t num_t
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (!inl && (!aligned(k_scale, 4) || !aligned(v_scale, 4))) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_write_int8(k, v, f16, head_dim, num_tokens, num_kv_heads, token_stride, slot_mapping, inl,
-                                            k_cache, v_cache, k_scale, v_scale, num_slots, dev_status,
+  return cuda_status(qkv::launch_write_int8(k, v, f16, head_dim, num_tokens, num_kv_heads, token_stride, slot_mapping, pg,
+                                            inl, k_cache, v_cache, k_scale, v_scale, num_slots, dev_status,
                                             static_cast<cudaStream_t>(stream)));
 }
 
 qkv_status write_e4m3_impl(const void* k, const void* v, bool f16, int64_t num_tokens, int num_kv_heads,
                            int head_dim, int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
                            void* v_cache, float k_scale, float v_scale, int64_t num_slots, uint32_t* dev_status,
-                           void* stream) {
+                           void* stream, const qkv::WritePaging* pg = nullptr) {
   qkv_status st = check_write_inputs(k, v, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping,
-                                     k_cache, v_cache, num_slots);
+                                     k_cache, v_cache, num_slots, pg);
   if (st != QKV_OK) return st;
   if (!finite_positive(k_scale) || !finite_positive(v_scale)) return QKV_ERR_SCALE;
   if (num_tokens == 0) return QKV_OK;
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16)) return QKV_ERR_ALIGN;
   if (dev_status && !aligned(dev_status, 4)) return QKV_ERR_ALIGN;
-  return cuda_status(qkv::launch_write_e4m3(k, v, f16, head_dim, num_tokens, num_kv_heads, token_stride, slot_mapping, k_cache,
-                                            v_cache, k_scale, v_scale, num_slots, dev_status,
+  return cuda_status(qkv::launch_write_e4m3(k, v, f16, head_dim, num_tokens, num_kv_heads, token_stride, slot_mapping, pg,
+                                            k_cache, v_cache, k_scale, v_scale, num_slots, dev_status,
                                             static_cast<cudaStream_t>(stream)));
 }
 
@@ -119,6 +128,27 @@ qkv_status qkv_write_e4m3_f16(const void* k, const void* v, int64_t num_tokens, 
                               void* stream) {
   return write_e4m3_impl(k, v, true, num_tokens, num_kv_heads, head_dim, token_stride, slot_mapping, k_cache,
                          v_cache, k_scale, v_scale, num_slots, dev_status, stream);
+}
+
+qkv_status qkv_write_ex(const qkv_write_desc* d, void* stream) {
+  if (d == nullptr || d->size != sizeof(qkv_write_desc)) return QKV_ERR_ARG;
+  const bool paged = d->slot_mapping == nullptr;
+  if (!paged && (d->token_seq || d->token_pos || d->block_table)) return QKV_ERR_ARG;  // one addressing only
+  const qkv::WritePaging pg{d->token_seq, d->token_pos, d->block_table, d->num_seqs, d->max_blocks, d->block_size};
+  const qkv::WritePaging* pp = paged ? &pg : nullptr;
+  if (d->act_fp16 != 0 && d->act_fp16 != 1) return QKV_ERR_ARG;
+  const bool f16 = d->act_fp16 == 1;
+  if (d->fmt == QKV_INT8_SIDE || d->fmt == QKV_INT8_INLINE)
+    return write_int8_impl(d->k, d->v, f16, d->num_tokens, d->num_kv_heads, d->head_dim, d->token_stride,
+                           d->slot_mapping, d->fmt, d->k_cache, d->v_cache, d->k_scale, d->v_scale, d->num_slots,
+                           d->dev_status, stream, pp);
+  if (d->fmt == QKV_E4M3) {
+    if (d->k_scale || d->v_scale) return QKV_ERR_ARG;  // per-token scale tensors belong to the int8 side layout
+    return write_e4m3_impl(d->k, d->v, f16, d->num_tokens, d->num_kv_heads, d->head_dim, d->token_stride,
+                           d->slot_mapping, d->k_cache, d->v_cache, d->k_scale_layer, d->v_scale_layer,
+                           d->num_slots, d->dev_status, stream, pp);
+  }
+  return QKV_ERR_ARG;
 }
 
 qkv_status qkv_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out, void* stream) {

@@ -16,14 +16,27 @@ constexpr int kHeadDimSmall = 128;  // the other head dim the kernels take
 __host__ __device__ constexpr bool head_dim_ok(int d) { return d == kHeadDim || d == kHeadDimSmall; }
 constexpr int kMaxGroup = 128;  // GQA group; above 16 the gather runs one CTA per 16 query heads
 
+// Paged addressing of the writes: token t sits at logical position token_pos[t] of sequence
+// token_seq[t], and its slot is block_table[seq, pos / block_size] * block_size + pos %
+// block_size (the gather's paged addressing, for the tokens being written).
+struct WritePaging {
+  const int32_t* token_seq;
+  const int32_t* token_pos;
+  const int32_t* block_table;
+  int64_t num_seqs;
+  int max_blocks;
+  int block_size;
+};
+
 // ------------------------------------------------------------------ launchers
+// paging == nullptr: slot ids in slot_mapping; else slot_mapping is unused
 cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
-                              int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
-                              void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                              int64_t token_stride, const int64_t* slot_mapping, const WritePaging* paging,
+                              bool inline_layout, void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                               int64_t num_slots, uint32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
-                              int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
-                              void* v_cache, float k_scale, float v_scale, int64_t num_slots,
+                              int64_t token_stride, const int64_t* slot_mapping, const WritePaging* paging,
+                              void* k_cache, void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream);
 cudaError_t launch_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits, float* scale_out,
                                   cudaStream_t stream);

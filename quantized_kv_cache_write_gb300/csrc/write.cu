@@ -88,16 +88,31 @@ __device__ __forceinline__ bool slot_ok(int64_t slot, int64_t num_slots, uint32_
   return true;
 }
 
+// The slot of token t in a paged pool: -1 when its position is -1 (skipped); -2 (flagged, then
+// skipped) for a position outside [-1, max_blocks * block_size), a sequence outside
+// [0, num_seqs) or an unallocated block (id < 0); a slot past the pool is flagged by the caller.
+__device__ __forceinline__ int64_t paged_slot(const WritePaging& pg, int64_t t, int64_t num_slots) {
+  const int seq = __ldg(pg.token_seq + t), pos = __ldg(pg.token_pos + t);  // both loads in flight
+  if (pos == -1) return -1;
+  if (pos < -1 || static_cast<int64_t>(pos) >= static_cast<int64_t>(pg.max_blocks) * pg.block_size || seq < 0 ||
+      seq >= pg.num_seqs)
+    return -2;
+  const int b = pos / pg.block_size;
+  const int blk = __ldg(pg.block_table + static_cast<int64_t>(seq) * pg.max_blocks + b);
+  if (blk < 0) return -2;
+  return static_cast<int64_t>(blk) * pg.block_size + (pos - b * pg.block_size);
+}
+
 // The warp's rows: one row (K or V: kv) of a (token, head) unit, or both rows of a unit when
 // paired. Every row and the slot are loaded before any is used, so the loads are in flight
 // together (a skipped token's rows are still in bounds: t < num_tokens). Returns false for a
 // warp past the end, a skipped token or a bad slot; the result is warp-uniform.
-template <bool kPaired>
+template <bool kPaired, bool kPaged>
 __device__ __forceinline__ bool warp_rows(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
                                           int64_t num_tokens, int num_heads, int64_t token_stride,
-                                          const int64_t* __restrict__ slot_mapping, int64_t num_slots,
-                                          uint32_t* dev_status, int lane, bool act, uint4 (&raw)[2], int& kv,
-                                          int64_t& rec) {
+                                          const int64_t* __restrict__ slot_mapping, const WritePaging& pg,
+                                          int64_t num_slots, uint32_t* dev_status, int lane, bool act,
+                                          uint4 (&raw)[2], int& kv, int64_t& rec) {
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * kWriteThreads + threadIdx.x) >> 5;
   const int64_t unit = kPaired ? wid : wid >> 1;
   if (unit >= num_tokens * num_heads) return false;
@@ -108,7 +123,7 @@ __device__ __forceinline__ bool warp_rows(const uint16_t* __restrict__ k, const 
   const int64_t off = t * token_stride + static_cast<int64_t>(h) * head_dim + lane * 8;
   raw[0] = act ? load_raw8((kv ? v : k) + off) : make_uint4(0, 0, 0, 0);
   if (kPaired) raw[1] = act ? load_raw8(v + off) : make_uint4(0, 0, 0, 0);
-  const int64_t slot = slot_mapping[t];
+  const int64_t slot = kPaged ? paged_slot(pg, t, num_slots) : slot_mapping[t];
   if (!slot_ok(slot, num_slots, dev_status, lane, kv == 0 && h == 0)) return false;
   rec = slot * num_heads + h;
   return true;
@@ -160,11 +175,11 @@ __device__ __forceinline__ void store_e4m3_row(const HeadVec& hv, int lane, int 
   *reinterpret_cast<uint2*>(cache + rec * head_dim + lane * 8) = make_uint2(word[0], word[1]);
 }
 
-template <bool kInline, bool F16, bool kPaired>
+template <bool kInline, bool F16, bool kPaired, bool kPaged>
 __global__ void __launch_bounds__(kWriteThreads)
     write_int8_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
                       int64_t num_tokens, int num_heads, int64_t token_stride,
-                      const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
+                      const int64_t* __restrict__ slot_mapping, const WritePaging pg, uint8_t* __restrict__ k_cache,
                       uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
                       float* __restrict__ v_scale, int64_t num_slots, uint32_t* dev_status) {
   const int lane = threadIdx.x & 31;
@@ -172,19 +187,19 @@ __global__ void __launch_bounds__(kWriteThreads)
   uint4 raw[2];
   int kv;
   int64_t rec;
-  if (!warp_rows<kPaired>(k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, num_slots, dev_status,
-                          lane, act, raw, kv, rec))
+  if (!warp_rows<kPaired, kPaged>(k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, pg, num_slots,
+                                  dev_status, lane, act, raw, kv, rec))
     return;
   store_int8_row<kInline>(widen8<F16>(raw[0]), lane, act, head_dim, rec, kv ? v_cache : k_cache,
                           kv ? v_scale : k_scale);
   if (kPaired) store_int8_row<kInline>(widen8<F16>(raw[1]), lane, act, head_dim, rec, v_cache, v_scale);
 }
 
-template <bool F16, bool kPaired>
+template <bool F16, bool kPaired, bool kPaged>
 __global__ void __launch_bounds__(kWriteThreads)
     write_e4m3_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int head_dim,
                       int64_t num_tokens, int num_heads, int64_t token_stride,
-                      const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_cache,
+                      const int64_t* __restrict__ slot_mapping, const WritePaging pg, uint8_t* __restrict__ k_cache,
                       uint8_t* __restrict__ v_cache, float k_scale, float v_scale, int64_t num_slots,
                       uint32_t* dev_status) {
   const int lane = threadIdx.x & 31;
@@ -192,8 +207,8 @@ __global__ void __launch_bounds__(kWriteThreads)
   uint4 raw[2];
   int kv;
   int64_t rec;
-  if (!warp_rows<kPaired>(k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, num_slots, dev_status,
-                          lane, act, raw, kv, rec) ||
+  if (!warp_rows<kPaired, kPaged>(k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, pg, num_slots,
+                                  dev_status, lane, act, raw, kv, rec) ||
       !act)
     return;
   store_e4m3_row(widen8<F16>(raw[0]), lane, head_dim, rec, kv ? v_scale : k_scale, kv ? v_cache : k_cache);
@@ -240,41 +255,70 @@ unsigned write_blocks(int64_t num_tokens, int num_heads) {
   return static_cast<unsigned>((warps * 32 + kWriteThreads - 1) / kWriteThreads);
 }
 
+template <bool kInline, bool F16, bool kPaired, bool kPaged>
+void launch_int8(unsigned blocks, const uint16_t* k, const uint16_t* v, int head_dim, int64_t num_tokens,
+                 int num_heads, int64_t token_stride, const int64_t* slot_mapping, const WritePaging& pg,
+                 uint8_t* kc, uint8_t* vc, float* ks, float* vs, int64_t num_slots, uint32_t* dev_status,
+                 cudaStream_t stream) {
+  write_int8_kernel<kInline, F16, kPaired, kPaged><<<blocks, kWriteThreads, 0, stream>>>(
+      k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, pg, kc, vc, ks, vs, num_slots, dev_status);
+}
+
+template <bool kInline, bool F16>
+void launch_int8(bool paired, bool paged, unsigned blocks, const uint16_t* k, const uint16_t* v, int head_dim,
+                 int64_t num_tokens, int num_heads, int64_t token_stride, const int64_t* slot_mapping,
+                 const WritePaging& pg, uint8_t* kc, uint8_t* vc, float* ks, float* vs, int64_t num_slots,
+                 uint32_t* dev_status, cudaStream_t stream) {
+  auto kern = paired ? (paged ? launch_int8<kInline, F16, true, true> : launch_int8<kInline, F16, true, false>)
+                     : (paged ? launch_int8<kInline, F16, false, true> : launch_int8<kInline, F16, false, false>);
+  kern(blocks, k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, pg, kc, vc, ks, vs, num_slots,
+       dev_status, stream);
+}
+
+template <bool F16, bool kPaired, bool kPaged>
+void launch_e4m3(unsigned blocks, const uint16_t* k, const uint16_t* v, int head_dim, int64_t num_tokens,
+                 int num_heads, int64_t token_stride, const int64_t* slot_mapping, const WritePaging& pg,
+                 uint8_t* kc, uint8_t* vc, float ks, float vs, int64_t num_slots, uint32_t* dev_status,
+                 cudaStream_t stream) {
+  write_e4m3_kernel<F16, kPaired, kPaged><<<blocks, kWriteThreads, 0, stream>>>(
+      k, v, head_dim, num_tokens, num_heads, token_stride, slot_mapping, pg, kc, vc, ks, vs, num_slots, dev_status);
+}
+
 }  // namespace
 
 cudaError_t launch_write_int8(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
-                              int64_t token_stride, const int64_t* slot_mapping, bool inline_layout,
-                              void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                              int64_t token_stride, const int64_t* slot_mapping, const WritePaging* paging,
+                              bool inline_layout, void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                               int64_t num_slots, uint32_t* dev_status, cudaStream_t stream) {
   const unsigned blocks = write_blocks(num_tokens, num_heads);
+  const bool pr = write_paired(num_tokens, num_heads), pgd = paging != nullptr;
+  const WritePaging pg = pgd ? *paging : WritePaging{nullptr, nullptr, nullptr, 0, 0, 1};
   auto kk = static_cast<const uint16_t*>(k);
   auto vv = static_cast<const uint16_t*>(v);
   auto kc = static_cast<uint8_t*>(k_cache);
   auto vc = static_cast<uint8_t*>(v_cache);
   float* ks = inline_layout ? nullptr : k_scale;
   float* vs = inline_layout ? nullptr : v_scale;
-  const bool pr = write_paired(num_tokens, num_heads);
-  auto kern = inline_layout
-                  ? (f16 ? (pr ? write_int8_kernel<true, true, true> : write_int8_kernel<true, true, false>)
-                         : (pr ? write_int8_kernel<true, false, true> : write_int8_kernel<true, false, false>))
-                  : (f16 ? (pr ? write_int8_kernel<false, true, true> : write_int8_kernel<false, true, false>)
-                         : (pr ? write_int8_kernel<false, false, true> : write_int8_kernel<false, false, false>));
-  kern<<<blocks, kWriteThreads, 0, stream>>>(kk, vv, head_dim, num_tokens, num_heads, token_stride, slot_mapping, kc,
-                                             vc, ks, vs, num_slots, dev_status);
+  auto kern = inline_layout ? (f16 ? launch_int8<true, true> : launch_int8<true, false>)
+                            : (f16 ? launch_int8<false, true> : launch_int8<false, false>);
+  kern(pr, pgd, blocks, kk, vv, head_dim, num_tokens, num_heads, token_stride, slot_mapping, pg, kc, vc, ks, vs,
+       num_slots, dev_status, stream);
   return cudaGetLastError();
 }
 
 cudaError_t launch_write_e4m3(const void* k, const void* v, bool f16, int head_dim, int64_t num_tokens, int num_heads,
-                              int64_t token_stride, const int64_t* slot_mapping, void* k_cache,
-                              void* v_cache, float k_scale, float v_scale, int64_t num_slots,
+                              int64_t token_stride, const int64_t* slot_mapping, const WritePaging* paging,
+                              void* k_cache, void* v_cache, float k_scale, float v_scale, int64_t num_slots,
                               uint32_t* dev_status, cudaStream_t stream) {
-  const bool pr = write_paired(num_tokens, num_heads);
-  auto kern = f16 ? (pr ? write_e4m3_kernel<true, true> : write_e4m3_kernel<true, false>)
-                  : (pr ? write_e4m3_kernel<false, true> : write_e4m3_kernel<false, false>);
-  kern<<<write_blocks(num_tokens, num_heads), kWriteThreads, 0, stream>>>(
-      static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), head_dim, num_tokens, num_heads, token_stride,
-      slot_mapping, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale, v_scale, num_slots,
-      dev_status);
+  const bool pr = write_paired(num_tokens, num_heads), pgd = paging != nullptr;
+  const WritePaging pg = pgd ? *paging : WritePaging{nullptr, nullptr, nullptr, 0, 0, 1};
+  auto kern = f16 ? (pr ? (pgd ? launch_e4m3<true, true, true> : launch_e4m3<true, true, false>)
+                        : (pgd ? launch_e4m3<true, false, true> : launch_e4m3<true, false, false>))
+                  : (pr ? (pgd ? launch_e4m3<false, true, true> : launch_e4m3<false, true, false>)
+                        : (pgd ? launch_e4m3<false, false, true> : launch_e4m3<false, false, false>));
+  kern(write_blocks(num_tokens, num_heads), static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), head_dim,
+       num_tokens, num_heads, token_stride, slot_mapping, pg, static_cast<uint8_t*>(k_cache),
+       static_cast<uint8_t*>(v_cache), k_scale, v_scale, num_slots, dev_status, stream);
   return cudaGetLastError();
 }
 

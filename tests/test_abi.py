@@ -304,3 +304,62 @@ def test_gather_ex_host_validation(lib):
     d.row_seq, d.block_table, d.num_seqs, d.max_blocks, d.block_size, d.q_fp16 = FAKE, FAKE, 2, 8, 16, 1
     assert L.qsa_gather_attn_ex(ctypes.byref(d), None) == E.QKV_ERR_ARG  # paged pools take a bf16 query
     assert L.qsa_gather_attn_ex(None, None) == E.QKV_ERR_ARG
+
+
+def test_write_desc_layout_matches_the_header(lib, tmp_path):
+    """The binding's ctypes mirror of qkv_write_desc has the C compiler's field offsets."""
+    import ctypes
+    import shutil
+    import subprocess
+    cc = shutil.which("cc") or shutil.which("gcc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [f[0] for f in lib.WriteDesc._fields_]
+    src = tmp_path / "wlayout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "qkv.h"\nint main(void) {\n'
+                   + "".join(f'  printf("%zu\\n", offsetof(qkv_write_desc, {n}));\n' for n in names)
+                   + '  printf("%zu\\n", sizeof(qkv_write_desc));\n  return 0;\n}\n')
+    exe = tmp_path / "wlayout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [getattr(lib.WriteDesc, n).offset for n in names] + [ctypes.sizeof(lib.WriteDesc)]
+    assert got == want
+
+
+def test_write_ex_host_validation(lib):
+    """Refusals before any launch: descriptor size, one addressing at a time, paged geometry,
+    format-specific scales."""
+    import ctypes
+    E = lib
+
+    def call(**over):
+        d = lib.WriteDesc()
+        d.size = ctypes.sizeof(lib.WriteDesc)
+        d.fmt, d.act_fp16 = E.QKV_INT8_SIDE, 0
+        d.k = d.v = FAKE
+        d.num_tokens, d.num_kv_heads, d.head_dim, d.token_stride = 3, 1, 256, 256
+        d.slot_mapping = FAKE
+        d.k_cache = d.v_cache = FAKE
+        d.k_scale = d.v_scale = FAKE
+        d.k_scale_layer = d.v_scale_layer = 1.0
+        d.num_slots = 10
+        for k, v in over.items():
+            setattr(d, k, v)
+        return lib.lib.qkv_write_ex(ctypes.byref(d), None)
+
+    assert lib.lib.qkv_write_ex(None, None) == E.QKV_ERR_ARG
+    assert call(size=8) == E.QKV_ERR_ARG
+    assert call(fmt=E.QKV_BF16) == E.QKV_ERR_ARG
+    assert call(act_fp16=2) == E.QKV_ERR_ARG
+    assert call(token_seq=FAKE) == E.QKV_ERR_ARG  # slot ids and a paged pool at once
+    paged = dict(slot_mapping=None, token_seq=FAKE, token_pos=FAKE, block_table=FAKE, num_seqs=2, max_blocks=4,
+                 block_size=16)
+    assert call(**{**paged, "block_table": None}) == E.QKV_ERR_ARG
+    assert call(**{**paged, "block_size": 0}) == E.QKV_ERR_ARG
+    assert call(**{**paged, "max_blocks": 1 << 20, "block_size": 1 << 12}) == E.QKV_ERR_ARG  # positions past 2^31
+    assert call(**{**paged, "token_pos": FAKE + 2}) == E.QKV_ERR_ALIGN
+    assert call(fmt=E.QKV_E4M3) == E.QKV_ERR_ARG  # E4M3 takes no per-token scale tensors
+    assert call(fmt=E.QKV_E4M3, k_scale=None, v_scale=None, k_scale_layer=0.0) == E.QKV_ERR_SCALE
+    assert call(fmt=E.QKV_INT8_INLINE) == E.QKV_ERR_ARG  # inline records hold their scales
+    assert call(num_tokens=0) == E.QKV_OK
+    assert call(**{**paged, "num_tokens": 0}) == E.QKV_OK
