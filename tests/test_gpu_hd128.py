@@ -30,8 +30,10 @@ def _wl(seed, act="bf16", **kw):
 
 @pytest.mark.parametrize("act", ["bf16", "f16"])
 @pytest.mark.parametrize("fmt", ["int8_side", "int8_inline", "e4m3"])
-def test_writes_are_bit_exact(fmt, act):
-    wl = _wl(101, act, zero_tokens=2)
+@pytest.mark.parametrize("large", [False, True])
+def test_writes_are_bit_exact(fmt, act, large):
+    """large: 18000 tokens, past the size where each warp writes a token's K and V rows."""
+    wl = _wl(101, act, zero_tokens=2, **(dict(num_slots=20000, num_tokens=18000) if large else {}))
     gp, op = GpuPool(wl, fmt), OraclePool(wl, fmt)
     got = (gp.k_cache, gp.v_cache, gp.k_scale_tok, gp.v_scale_tok) if fmt == "int8_side" else (gp.k_cache, gp.v_cache)
     for g, r in zip(got, op.bytes):
