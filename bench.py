@@ -827,11 +827,17 @@ def measure_workloads(q, flush, stream, reps, peak):
     rec = torch.zeros(8, dtype=torch.int64, device="cuda")
     h_ms = _time_events(lambda: q.qkv_calib_histogram(x, hist), flush, stream, reps)
     s_ms = _time_events(lambda: q.qkv_calib_stats(hist, rec), flush, stream, reps)
+    amax = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sc = torch.zeros(1, dtype=torch.float32, device="cuda")
+    a_ms = _time_events(lambda: q.qkv_e4m3_calibrate(x, amax, sc), flush, stream, reps)
     res["calibration"] = {
         "shape": f"one layer's K: {x.numel()} bf16 values (131072 slots x 256)",
         "histogram_ms": round(h_ms, 5), "stats_ms": round(s_ms, 5),
         "histogram_GBps": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9, 2),
-        "histogram_frac_of_hbm_peak": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9 / peak, 4)}
+        "histogram_frac_of_hbm_peak": round(x.numel() * 2 / (h_ms * 1e-3) / 1e9 / peak, 4),
+        "e4m3_calibrate_ms": round(a_ms, 5),
+        "e4m3_calibrate_GBps": round(x.numel() * 2 / (a_ms * 1e-3) / 1e9, 2),
+        "e4m3_calibrate_frac_of_hbm_peak": round(x.numel() * 2 / (a_ms * 1e-3) / 1e9 / peak, 4)}
     del x
 
     # pool fill: the page-1 pool's 262144 new tokens written in one call (HBM-bound at this size;

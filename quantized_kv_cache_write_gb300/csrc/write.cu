@@ -13,6 +13,8 @@
 // idle); the absmax is a 5-step shuffle reduction; the codes leave as one coalesced line.
 // Division is IEEE (__fdiv_rn) and rounding is round-to-nearest-even, so the stored bytes
 // equal a plain fp32 reference bit for bit.
+#include <atomic>
+
 #include "qkv_internal.cuh"
 
 namespace qkv {
@@ -215,24 +217,32 @@ __global__ void __launch_bounds__(kWriteThreads)
   if (kPaired) store_e4m3_row(widen8<F16>(raw[1]), lane, head_dim, rec, v_scale, v_cache);
 }
 
-// max |x| over n bf16 values, as fp32 bits (non-negative floats order like their bits).
+// max |x| over n bf16 values, as fp32 bits (non-negative floats order like their bits). A
+// grid-stride loop with four 16 B loads in flight per thread.
+__device__ __forceinline__ uint32_t absmax8(uint32_t m, const uint4& r) {
+  const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) m = max(m, max((w[j] & 0x7FFFu) << 16, w[j] & 0x7FFF0000u));
+  return m;
+}
+
 __global__ void __launch_bounds__(256)
     absmax_bf16_kernel(const uint16_t* __restrict__ x, int64_t n, uint32_t* __restrict__ amax_bits) {
   uint32_t m = 0;
   const int64_t nvec = n / 8;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const uint4* xv = reinterpret_cast<const uint4*>(x);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-    const uint4 r = __ldg(xv + i);
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < nvec; i += 4 * stride) {
+    uint4 r[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      m = max(m, (w[j] & 0x7FFFu) << 16);
-      m = max(m, w[j] & 0x7FFF0000u);
-    }
+    for (int u = 0; u < 4; ++u) r[u] = __ldg(xv + i + u * stride);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) m = absmax8(m, r[u]);
   }
-  for (int64_t i = nvec * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride)
-    m = max(m, static_cast<uint32_t>(x[i] & 0x7FFFu) << 16);
+  for (; i < nvec; i += stride) m = absmax8(m, __ldg(xv + i));
+  for (int64_t j = nvec * 8 + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < n; j += stride)
+    m = max(m, static_cast<uint32_t>(x[j] & 0x7FFFu) << 16);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
   __shared__ uint32_t red[8];
@@ -327,8 +337,20 @@ cudaError_t launch_e4m3_calibrate(const void* x, int64_t n, uint32_t* amax_bits,
   cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(uint32_t), stream);
   if (e != cudaSuccess) return e;
   if (n > 0) {
+    // one wave of 256-thread blocks (8 per SM); each thread then keeps four loads in flight
+    static std::atomic<int> sm_count[64] = {};
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int sms = sm_count[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return e;
+      sm_count[dev].store(sms, std::memory_order_relaxed);
+    }
     int64_t want = (n / 8 + 255) / 256;
-    const int64_t cap = 152 * 8;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
     const unsigned blocks = static_cast<unsigned>(want < 1 ? 1 : (want > cap ? cap : want));
     absmax_bf16_kernel<<<blocks, 256, 0, stream>>>(static_cast<const uint16_t*>(x), n, amax_bits);
     e = cudaGetLastError();
