@@ -63,7 +63,7 @@ __device__ __forceinline__ float warp_max(float a) {
 // Large writes pair a token head's K and V rows in one warp (two row loads in flight per
 // lane, one slot load for both); small ones give each row its own warp, twice the warps to
 // spread a latency-bound launch over. Measured on one GB300 (int8 side / E4M3): 262144 tokens
-// 143 -> 120 / 113 -> 91 us paired; 2048 tokens 8-9 / 7 us either way.
+// 143 -> 117 / 113 -> 91 us paired; 2048 tokens 7-9 / 7 us either way.
 constexpr int64_t kPairedMinUnits = 16384;  // (token, head) units from which rows are paired
 
 // The (token t, head h) of a unit. 32-bit division whenever the index fits, which it does at
@@ -142,12 +142,16 @@ __device__ __forceinline__ void store_int8_row(const HeadVec& hv, int lane, bool
   const float scale = __fdiv_rn(a, 127.0f);
   uint32_t word[2] = {0u, 0u};
   if (scale > 0.f) {
+    uint32_t c[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      int c = __float2int_rn(__fdiv_rn(hv.x[i], scale));
-      c = max(-127, min(127, c));
-      word[i >> 2] |= (static_cast<uint32_t>(c) & 0xFFu) << (8 * (i & 3));
-    }
+    for (int i = 0; i < 8; ++i)
+      c[i] = static_cast<uint32_t>(max(-127, min(127, __float2int_rn(__fdiv_rn(hv.x[i], scale)))));
+    // low bytes of c[4w .. 4w + 3] into word w, c[4w] lowest: two byte permutes per pair, one
+    // to join the pairs
+#pragma unroll
+    for (int w = 0; w < 2; ++w)
+      word[w] = __byte_perm(__byte_perm(c[4 * w], c[4 * w + 1], 0x0040), __byte_perm(c[4 * w + 2], c[4 * w + 3], 0x0040),
+                            0x5410);
   }
   if (kInline) {
     uint8_t* base = cache + rec * (head_dim + 4);  // head_dim codes, then the fp32 scale
@@ -166,15 +170,16 @@ __device__ __forceinline__ void store_int8_row(const HeadVec& hv, int lane, bool
 // E4M3 codes of one head row (lanes that own dims only) into record `rec` of `cache`.
 __device__ __forceinline__ void store_e4m3_row(const HeadVec& hv, int lane, int head_dim, int64_t rec, float s,
                                                uint8_t* __restrict__ cache) {
-  uint32_t word[2] = {0u, 0u};
+  uint32_t p[4];
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    const float2 y = make_float2(__fdiv_rn(hv.x[i], s), __fdiv_rn(hv.x[i + 1], s));
+  for (int j = 0; j < 4; ++j) {
+    const float2 y = make_float2(__fdiv_rn(hv.x[2 * j], s), __fdiv_rn(hv.x[2 * j + 1], s));
     // .x lands in the low byte; round to nearest even, saturate to +-448, sign kept.
-    const uint32_t p = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-    word[i >> 2] |= (p & 0xFFFFu) << (8 * (i & 3));
+    p[j] = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
   }
-  *reinterpret_cast<uint2*>(cache + rec * head_dim + lane * 8) = make_uint2(word[0], word[1]);
+  // code pairs 2w, 2w + 1 into word w (low halves), one byte permute each
+  *reinterpret_cast<uint2*>(cache + rec * head_dim + lane * 8) =
+      make_uint2(__byte_perm(p[0], p[1], 0x5410), __byte_perm(p[2], p[3], 0x5410));
 }
 
 template <bool kInline, bool F16, bool kPaired, bool kPaged>
