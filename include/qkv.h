@@ -19,8 +19,9 @@
  *     trapped: the offending entry is skipped and a bit is OR-ed into the optional
  *     caller-provided device word `dev_status` (may be NULL).
  *   - head_dim must be 256 (256 B of int8 data per head, [INT8-PR §The finding worth
- *     upstreaming]) or 128 (the other common head size; all layouts and entry points); num_q_heads / num_kv_heads (the GQA group) must be 1..128 (groups above 16
- *     run as one CTA per 16 query heads, each gathering the row's slots).
+ *     upstreaming]) or 128 (the other common head size; all layouts and entry points).
+ *     num_q_heads / num_kv_heads (the GQA group) must be 1..128 (groups above 16 run as one
+ *     CTA per 16 query heads, each gathering the row's slots).
  *   - Pool layouts, S = num_slots, H = num_kv_heads, D = head_dim:
  *       QKV_BF16        K, V: bf16 [S, H, D]
  *       QKV_INT8_SIDE   K, V: int8 [S, H, D]; k_scale, v_scale: fp32 [S, H] (side tensors)
@@ -60,7 +61,8 @@ typedef enum {
 } qkv_format;
 
 /* Bits OR-ed into *dev_status by the kernels. */
-#define QKV_DEV_BAD_SLOT 1u  /* slot_mapping entry >= num_slots or < -1: that token is skipped */
+#define QKV_DEV_BAD_SLOT 1u  /* a write's slot is invalid (a slot_mapping entry >= num_slots or
+                                 < -1, or a bad paged entry, see qkv_write_ex): token skipped */
 #define QKV_DEV_BAD_INDEX 2u /* top-k entry >= num_slots or < -1: treated as padding (-1) */
 
 /*
