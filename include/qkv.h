@@ -253,8 +253,9 @@ qkv_status qkv_calib_stats_f16(const uint64_t* hist, float scale, qkv_calib_summ
  *   qsa_splitk_merge (pass v_scale_layer as its v_scale_post).
  *
  *   q             bf16 [rows, num_q_heads, head_dim], contiguous, 16 B-aligned.
- *   fmt           pool layout (see above); QKV_F16 is QKV_ERR_ARG here (qsa_gather_attn_f16). k_cache / v_cache base pointers 16 B-aligned.
- *                 S * num_kv_heads must stay <= 2^31 - 1 (else QKV_ERR_UNSUPPORTED).
+ *   fmt           pool layout (see above); QKV_F16 is QKV_ERR_ARG here (qsa_gather_attn_f16).
+ *                 k_cache / v_cache base pointers 16 B-aligned. S * num_kv_heads must stay
+ *                 <= 2^31 - 1 (else QKV_ERR_UNSUPPORTED).
  *   k_scale_tok, v_scale_tok  fp32 [S, H] for QKV_INT8_SIDE, else must be NULL.
  *   k_scale_layer, v_scale_layer  per-layer scales for QKV_E4M3 (finite, > 0, else
  *                 QKV_ERR_SCALE); ignored for the other formats.
