@@ -156,6 +156,12 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        return self.summarize(out)
+
+    @staticmethod
+    def summarize(out: str) -> dict:
+        """Median SM clock under load, the max clock and the throttle reasons seen, from the
+        sampler's CSV lines (FIELDS order, no header, no units)."""
         rows = []
         for line in out.strip().splitlines():
             p = [x.strip() for x in line.split(",")]
