@@ -60,9 +60,25 @@ def _stale(outputs_mtime: float) -> bool:
 
 
 def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = True) -> str:
-    """Compile csrc/*.cu and link libqkv.so next to this file. Returns the library path."""
+    """Compile csrc/*.cu and link libqkv.so next to this file. Returns the library path.
+
+    Processes that build at the same time (one per GPU under torchrun) take turns on a lock
+    file; a later one finds the library fresh and returns."""
     if not force and os.path.exists(LIB_PATH) and not _stale(os.path.getmtime(LIB_PATH)):
         return LIB_PATH
+    import fcntl
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and os.path.exists(LIB_PATH) and not _stale(os.path.getmtime(LIB_PATH)):
+                return LIB_PATH
+            return _build(ptxas_verbose, quiet)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build(ptxas_verbose: bool, quiet: bool) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
