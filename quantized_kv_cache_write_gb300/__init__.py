@@ -142,6 +142,10 @@ def qkv_write_int8(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=N
                    layout: int = QKV_INT8_SIDE, dev_status=None, stream=None):
     """int8 per-(token, head) quantize-on-write (side scales or inline 260 B records); bf16 or fp16 tokens."""
     T, H, D, stride = _tokens(k, v)
+    _need("slot_mapping", slot_mapping, _I64, T)
+    _need("k_scale", k_scale, _F32)
+    _need("v_scale", v_scale, _F32)
+    _need("dev_status", dev_status, _WORD)
     name = "qkv_write_int8_f16" if k.dtype == torch.float16 else "qkv_write_int8"
     st = getattr(lib, name)(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), layout, _ptr(k_cache),
                             _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), k_cache.shape[0], _ptr(dev_status),
@@ -153,6 +157,8 @@ def qkv_write_e4m3(k, v, slot_mapping, k_cache, v_cache, k_scale: float, v_scale
                    dev_status=None, stream=None):
     """FP8 E4M3 quantize-on-write with calibrated per-layer scales; bf16 or fp16 tokens."""
     T, H, D, stride = _tokens(k, v)
+    _need("slot_mapping", slot_mapping, _I64, T)
+    _need("dev_status", dev_status, _WORD)
     name = "qkv_write_e4m3_f16" if k.dtype == torch.float16 else "qkv_write_e4m3"
     st = getattr(lib, name)(_ptr(k), _ptr(v), T, H, D, stride, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
                             float(k_scale), float(v_scale), k_cache.shape[0], _ptr(dev_status), _stream(stream))
@@ -176,9 +182,13 @@ def qkv_write_ex(k, v, fmt: int, k_cache, v_cache, *, slot_mapping=None, token_s
         if block_table.dim() != 2:
             raise ValueError("block_table must be [num_seqs, max_blocks]")
         d.num_seqs, d.max_blocks, d.block_size = block_table.shape[0], block_table.shape[1], int(block_size)
-    for name, t in (("token_seq", token_seq), ("token_pos", token_pos)):
-        if t is not None and t.numel() != T:
-            raise ValueError(f"{name} must hold one entry per token ({T})")
+    _need("slot_mapping", slot_mapping, _I64, T)
+    _need("token_seq", token_seq, _I32, T)
+    _need("token_pos", token_pos, _I32, T)
+    _need("block_table", block_table, _I32)
+    _need("k_scale", k_scale, _F32)
+    _need("v_scale", v_scale, _F32)
+    _need("dev_status", dev_status, _WORD)
     d.k_cache, d.v_cache, d.k_scale, d.v_scale = _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale)
     d.k_scale_layer, d.v_scale_layer = float(k_scale_layer), float(v_scale_layer)
     d.num_slots, d.dev_status = k_cache.shape[0], _ptr(dev_status)
@@ -236,15 +246,47 @@ def _expect_shape(name: str, t, shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
+_I32 = (torch.int32,)
+_I64 = (torch.int64,)
+_F32 = (torch.float32,)
+_WORD = (torch.int32, torch.uint32)
+
+
+def _need(name: str, t, dtypes, numel: Optional[int] = None):
+    """A tensor the kernels read or write by raw pointer: its dtype, contiguity and size."""
+    if t is None:
+        return
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must be {' or '.join(str(d).replace('torch.', '') for d in dtypes)}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name} must hold {numel} elements, got {t.numel()}")
+
+
 def _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part=None, lse_part=None):
     """The kernels index every buffer by q's row count: the others must agree with it."""
     R, Hq, D = q.shape
     if topk_idx is not None and (topk_idx.dim() != 2 or topk_idx.shape[0] != R):
         raise ValueError(f"topk_idx must be [{R}, k], got {tuple(topk_idx.shape)}")
+    _need("topk_idx", topk_idx, _I32)
     _expect_shape("out", out, (R, Hq, D))
     _expect_shape("lse", lse, (R, Hq))
     _expect_shape("o_part", o_part, (R, num_splits, Hq, D))
     _expect_shape("lse_part", lse_part, (R, num_splits, Hq))
+    for name, t in (("out", out), ("lse", lse), ("o_part", o_part), ("lse_part", lse_part)):
+        _need(name, t, _F32)
+
+
+def _check_gather_aux(k_scale_tok, v_scale_tok, dev_status, counters=None, row_seq=None, block_table=None,
+                      topk_len=None, rows=None):
+    _need("k_scale_tok", k_scale_tok, _F32)
+    _need("v_scale_tok", v_scale_tok, _F32)
+    _need("dev_status", dev_status, _WORD)
+    _need("counters", counters, _WORD)
+    _need("row_seq", row_seq, _I32, rows)
+    _need("block_table", block_table, _I32)
+    _need("topk_len", topk_len, _I32, rows)
 
 
 def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: float, *, num_kv_heads: int = 1,
@@ -253,6 +295,7 @@ def qsa_gather_attn(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: floa
                     lse=None, o_part=None, lse_part=None, dev_status=None, stream=None):
     """Top-k gather decode attention. q bf16 (or fp16: qsa_gather_attn_f16) [R, Hq, D]; topk_idx int32 [R, k]."""
     _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
+    _check_gather_aux(k_scale_tok, v_scale_tok, dev_status)
     R, Hq, D = q.shape
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_idx.shape[1] if topk_idx is not None else 0
@@ -274,6 +317,7 @@ def qsa_gather_attn_varlen(q, fmt: int, k_cache, v_cache, topk_idx, topk_len, so
     R, Hq, D = q.shape
     if topk_len is None or topk_len.numel() != R or topk_len.dtype != torch.int32:
         raise ValueError(f"topk_len must be int32 [{R}]")
+    _check_gather_aux(k_scale_tok, v_scale_tok, dev_status, topk_len=topk_len, rows=R)
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_idx.shape[1]
     st = lib.qsa_gather_attn_varlen(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
@@ -303,6 +347,7 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
         raise ValueError(f"block_table must be [num_seqs, max_blocks] with row_seq [{R}]")
     if counters is not None and counters.numel() != R * num_kv_heads * ((Hq // num_kv_heads + 15) // 16):
         raise ValueError("counters must hold rows x num_kv_heads x ceil(G / 16) entries")
+    _check_gather_aux(k_scale_tok, v_scale_tok, dev_status, counters, row_seq, block_table, topk_len, R)
     d = GatherDesc()
     d.size = ctypes.sizeof(GatherDesc)
     d.q, d.q_fp16, d.rows, d.num_q_heads, d.num_kv_heads, d.head_dim = _ptr(q), int(q.dtype == torch.float16), R, Hq, \
@@ -338,6 +383,7 @@ def qsa_gather_attn_paged(q, fmt: int, k_cache, v_cache, block_table, row_seq, t
     R, Hq, D = q.shape
     if block_table.dim() != 2 or row_seq.dim() != 1 or row_seq.shape[0] != R:
         raise ValueError(f"block_table must be [num_seqs, max_blocks] and row_seq [{R}]")
+    _check_gather_aux(k_scale_tok, v_scale_tok, dev_status, row_seq=row_seq, block_table=block_table, rows=R)
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_pos.shape[1] if topk_pos is not None else 0
     st = lib.qsa_gather_attn_paged(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
@@ -364,6 +410,7 @@ def qsa_gather_attn_splitk_fused(q, fmt: int, k_cache, v_cache, topk_idx, softma
     chunks = (Hq // num_kv_heads + 15) // 16
     if counters is not None and counters.numel() != R * num_kv_heads * chunks:
         raise ValueError(f"counters must hold {R} x {num_kv_heads} x {chunks} entries, got {counters.numel()}")
+    _check_gather_aux(k_scale_tok, v_scale_tok, dev_status, counters)
     S = k_cache.shape[0] if num_slots is None else num_slots
     topk = topk_idx.shape[1] if topk_idx is not None else 0
     st = lib.qsa_gather_attn_splitk_fused(_ptr(q), R, Hq, num_kv_heads, D, fmt, _ptr(k_cache), _ptr(v_cache),
@@ -388,6 +435,8 @@ def qsa_splitk_merge(o_part, lse_part, out, lse=None, *, v_scale_post: float = 1
     _expect_shape("lse_part", lse_part, (R, P, Hq))
     _expect_shape("out", out, (R, Hq, D))
     _expect_shape("lse", lse, (R, Hq))
+    for name, t in (("o_part", o_part), ("lse_part", lse_part), ("out", out), ("lse", lse)):
+        _need(name, t, _F32)
     st = lib.qsa_splitk_merge(_ptr(o_part), _ptr(lse_part), R, Hq, D, P, float(v_scale_post), _ptr(out), _ptr(lse),
                               _stream(stream))
     _check("qsa_splitk_merge", st)
@@ -413,6 +462,7 @@ def qsa_gather_attn_splitk_noalloc(q, fmt: int, k_cache, v_cache, topk_idx, soft
     Calls share one scratch array per GPU, so calls that overlap on the GPU race.
     """
     _check_gather_shapes(q, topk_idx, num_splits, out, lse)
+    _check_gather_aux(k_scale_tok, v_scale_tok, dev_status)
     R, Hq, D = q.shape
     if num_splits > 1 and noalloc_scratch_bytes(R, num_splits, Hq, D) > NOALLOC_SCRATCH_BYTES:
         raise ValueError(f"{R} rows x {num_splits} splits x {Hq} heads needs "

@@ -161,6 +161,43 @@ def test_token_views_ignore_the_strides_of_unit_dimensions(lib):
         lib._tokens(torch.zeros((5, 1, 512), dtype=torch.bfloat16)[:, :, :256], k)  # token strides differ
 
 
+def test_binding_checks_raw_pointer_tensors(lib):
+    """Index, scale and output tensors reach the kernels as raw pointers: the binding refuses a
+    wrong dtype, a non-contiguous view or a wrong length before any call."""
+    import torch
+    k = torch.zeros((4, 1, 256), dtype=torch.bfloat16)
+    kc = torch.zeros((8, 1, 256), dtype=torch.int8)
+    sc = torch.zeros((8, 1), dtype=torch.float32)
+    sm = torch.arange(4, dtype=torch.int64)
+    with pytest.raises(ValueError, match="slot_mapping must be int64"):
+        lib.qkv_write_int8(k, k, sm.to(torch.int32), kc, kc, sc, sc)
+    with pytest.raises(ValueError, match="slot_mapping must hold 4"):
+        lib.qkv_write_int8(k, k, torch.arange(5, dtype=torch.int64), kc, kc, sc, sc)
+    with pytest.raises(ValueError, match="k_scale must be float32"):
+        lib.qkv_write_int8(k, k, sm, kc, kc, sc.double(), sc)
+    with pytest.raises(ValueError, match="dev_status"):
+        lib.qkv_write_e4m3(k, k, sm, kc, kc, 1.0, 1.0, dev_status=torch.zeros(1))
+    with pytest.raises(ValueError, match="token_pos must be int32"):
+        lib.qkv_write_ex(k, k, lib.QKV_E4M3, kc, kc, token_seq=torch.zeros(4, dtype=torch.int32),
+                         token_pos=torch.zeros(4, dtype=torch.int64), block_table=torch.zeros((2, 2), dtype=torch.int32),
+                         block_size=16)
+    q = torch.zeros((4, 16, 256), dtype=torch.bfloat16)
+    out = torch.zeros((4, 16, 256), dtype=torch.float32)
+    idx = torch.zeros((4, 6), dtype=torch.int32)
+    with pytest.raises(ValueError, match="topk_idx must be int32"):
+        lib.qsa_gather_attn(q, lib.QKV_INT8_SIDE, kc, kc, idx.long(), 0.0625, out=out)
+    with pytest.raises(ValueError, match="topk_idx must be contiguous"):
+        lib.qsa_gather_attn(q, lib.QKV_INT8_SIDE, kc, kc, torch.zeros((6, 4), dtype=torch.int32).t(), 0.0625, out=out)
+    with pytest.raises(ValueError, match="out must be float32"):
+        lib.qsa_gather_attn(q, lib.QKV_INT8_SIDE, kc, kc, idx, 0.0625, out=out.double())
+    with pytest.raises(ValueError, match="counters"):
+        lib.qsa_gather_attn_splitk_fused(q, lib.QKV_INT8_SIDE, kc, kc, idx, 0.0625, num_splits=2, out=out,
+                                         o_part=torch.zeros((4, 2, 16, 256)), lse_part=torch.zeros((4, 2, 16)),
+                                         counters=torch.zeros(4, dtype=torch.int64))
+    with pytest.raises(ValueError, match="o_part must be float32"):
+        lib.qsa_splitk_merge(torch.zeros((4, 2, 16, 256), dtype=torch.float64), torch.zeros((4, 2, 16)), out)
+
+
 def _gather_paged(lib, **over):
     a = dict(q=FAKE, rows=4, hq=16, hkv=1, d=256, fmt=lib.QKV_INT8_SIDE, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE,
              ksl=1.0, vsl=1.0, S=100, bt=FAKE, nseq=2, mb=8, bs=16, rs=FAKE, pos=FAKE, topk=8, sm=0.0625, P=1,
