@@ -846,6 +846,37 @@ def measure_workloads(q, flush, stream, reps, peak):
         "e4m3_calibrate_frac_of_hbm_peak": round(x.numel() * 2 / (a_ms * 1e-3) / 1e9 / peak, 4)}
     del x
 
+    # the generalisations at the page-1 shape (2048 rows x top-k 1024 over 262144 int8-side slots):
+    # head_dim 128, fp16 activations, and a GQA group of 32 query heads (two 16-head CTAs per row)
+    from gen import small_random
+    variants = {}
+    for name, kw in (("head_dim_128", dict(head_dim=128)), ("fp16_activations", dict(act_dtype="f16")),
+                     ("gqa_32", dict(num_q_heads=32))):
+        wl = small_random(11, num_slots=262144, rows=2048, topk=1024, outlier_frac=0.01, **kw)
+        Dv, Sv, Hv = wl.head_dim, wl.num_slots, wl.num_kv_heads
+        dt = torch.float16 if wl.act_dtype == "f16" else torch.bfloat16
+        tok = lambda b, dt=dt: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(dt).cuda()
+        kcv = torch.zeros((Sv, Hv, Dv), dtype=torch.int8, device="cuda")
+        vcv = torch.zeros_like(kcv)
+        ksv = torch.zeros((Sv, Hv), dtype=torch.float32, device="cuda")
+        vsv = torch.zeros_like(ksv)
+        q.qkv_write_int8(tok(wl.k_tokens), tok(wl.v_tokens), torch.from_numpy(wl.slot_mapping).cuda(), kcv, vcv,
+                         ksv, vsv)
+        qv = tok(wl.q)
+        iv = torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
+        ov = torch.empty((wl.rows, wl.num_q_heads, Dv), dtype=torch.float32, device="cuda")
+        t = _time_events(lambda: q.qsa_gather_attn(qv, q.QKV_INT8_SIDE, kcv, vcv, iv, wl.softmax_scale, out=ov,
+                                                   k_scale_tok=ksv, v_scale_tok=vsv), flush, stream, reps)
+        nb = wl.rows * wl.topk.shape[1] * (2 * Dv + 8)
+        variants[name] = {"gather_ms": round(t, 5), "gathered_GBps": round(nb / (t * 1e-3) / 1e9, 2),
+                          "frac_of_hbm_peak": round(nb / (t * 1e-3) / 1e9 / peak, 4),
+                          "num_q_heads": wl.num_q_heads, "head_dim": Dv, "activations": wl.act_dtype}
+        del kcv, vcv, ksv, vsv, qv, iv, ov
+    variants["note"] = ("int8 side pools, 2048 rows x top-k 1024 over 262144 slots; GB/s over each row's gathered "
+                        "bytes once (the GQA-32 rows gather every slot twice, once per 16-head CTA)")
+    res["variants"] = variants
+    torch.cuda.empty_cache()
+
     # pool fill: the page-1 pool's 262144 new tokens written in one call (HBM-bound at this size;
     # per token 1024 B of bf16 K and V read, 2 x 260 B (int8 + scale) or 2 x 256 B (E4M3) written)
     from gen import page1_shape
