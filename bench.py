@@ -889,6 +889,16 @@ def measure_workloads(q, flush, stream, reps, peak):
     ks = torch.zeros((S, 1), dtype=torch.float32, device="cuda")
     vs = torch.zeros_like(ks)
     w8 = _time_events(lambda: q.qkv_write_int8(k_tok, v_tok, slots, kc, vc, ks, vs), flush, stream, reps)
+    # the same tokens through a paged pool: one sequence, position t, blocks of 16 in a random
+    # physical order (qkv_write_ex), so each token's slot comes from the block table
+    B = 16
+    perm = np.random.default_rng(5).permutation(S // B).astype(np.int32)
+    table = torch.from_numpy(perm.reshape(1, -1)).cuda()
+    tseq = torch.zeros(T, dtype=torch.int32, device="cuda")
+    tpos = torch.arange(T, dtype=torch.int32, device="cuda")
+    w8p = _time_events(lambda: q.qkv_write_ex(k_tok, v_tok, q.QKV_INT8_SIDE, kc, vc, token_seq=tseq, token_pos=tpos,
+                                              block_table=table, block_size=B, k_scale=ks, v_scale=vs),
+                       flush, stream, reps)
     del kc, vc, ks, vs
     ec = torch.zeros((S, 1, HEAD_DIM), dtype=torch.uint8, device="cuda")
     evc = torch.zeros_like(ec)
@@ -897,6 +907,8 @@ def measure_workloads(q, flush, stream, reps, peak):
     res["pool_fill"] = {
         "shape": f"{T} bf16 tokens (1 KV head x 256, K and V) written into a {S}-slot pool in one call",
         "write_int8_side_ms": round(w8, 5), "write_e4m3_ms": round(we, 5),
+        "write_int8_side_paged_ms": round(w8p, 5),
+        "write_int8_side_paged_GBps": round(b8 / (w8p * 1e-3) / 1e9, 2),
         "write_int8_side_GBps": round(b8 / (w8 * 1e-3) / 1e9, 2),
         "write_e4m3_GBps": round(be / (we * 1e-3) / 1e9, 2),
         "write_int8_side_frac_of_hbm_peak": round(b8 / (w8 * 1e-3) / 1e9 / peak, 4),
