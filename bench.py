@@ -66,6 +66,33 @@ def dist_env():
     return rank, world, local
 
 
+def _free_port() -> int:
+    import socket
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_ranks(n: int, argv) -> int:
+    """Run this script as n ranks on this node (one process per GPU, torch.distributed.run on
+    127.0.0.1) and return their exit status. Used when --gpus N > 1 is given without an outer
+    launcher; under one, WORLD_SIZE is set and the ranks run directly."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={_free_port()}", os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
+
+
+def check_world(args) -> bool:
+    """True when this process is one rank of the launch --gpus asks for; False when it must
+    launch the ranks itself. A launcher whose WORLD_SIZE disagrees with --gpus is refused."""
+    if "WORLD_SIZE" in os.environ:
+        world = int(os.environ["WORLD_SIZE"])
+        if world != args.gpus:
+            raise SystemExit(f"bench.py: --gpus {args.gpus} but the launcher started {world} ranks")
+        return True
+    return args.gpus <= 1
+
+
 def load_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -190,25 +217,6 @@ def oracle_setup(wl):
     return oatt.int8_side_pool_fp64(kc, ks), oatt.int8_side_pool_fp64(vc, vs)
 
 
-def oracle_step(wl, K, V, rows):
-    """One bounded oracle step: quantize the sampled rows' new tokens, attend the sampled rows."""
-    from oracle import attention as oatt
-    from oracle import quant as oq
-    n = len(rows)
-    oq.int8_quantize(oq.bf16_bits_to_f32(wl.step_k[:n]))
-    oq.int8_quantize(oq.bf16_bits_to_f32(wl.step_v[:n]))
-    oatt.gather_attention(wl.q, K, V, wl.topk, wl.softmax_scale, rows=rows)
-
-
-def time_oracle(wl, K, V, rows, repeats):
-    times = []
-    for _ in range(repeats):
-        t0 = time.perf_counter()
-        oracle_step(wl, K, V, rows)
-        times.append(time.perf_counter() - t0)
-    return times
-
-
 _ORACLE = None  # (wl, K, V) shared with forked oracle workers (copy-on-write)
 
 
@@ -221,6 +229,40 @@ def _oracle_chunk(rows):
     oq.int8_quantize(oq.bf16_bits_to_f32(wl.step_v[lo:hi]))
     oatt.gather_attention(wl.q, K, V, wl.topk, wl.softmax_scale, rows=rows)
     return len(rows)
+
+
+def start_oracle_pool(wl):
+    """A pool of one forked oracle worker per host core, holding the page-1 workload and its
+    fp64 pool (shared copy-on-write). Must be called before the process first uses CUDA."""
+    global _ORACLE
+    import multiprocessing as mp
+    K, V = oracle_setup(wl)
+    _ORACLE = (wl, K, V)
+    cores = max(1, min(len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count(), 64))
+    return mp.get_context("fork").Pool(cores)
+
+
+def time_oracle_pool(pool, sample_rows: int = 0, repeats: int = 3) -> dict:
+    """cpu_baseline: the oracle on every host core over a bounded sample of the page-1 rows
+    (32 rows per core: about a second of CPU work per step), mean of `repeats` steps."""
+    cores = pool._processes
+    n = min(ROWS, sample_rows or 32 * cores)
+    per = -(-n // cores)
+    chunks = [list(range(i, min(n, i + per))) for i in range(0, n, per)]
+    pool.map(_oracle_chunk, chunks)  # warm the workers
+    times = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        pool.map(_oracle_chunk, chunks)
+        times.append(time.perf_counter() - t0)
+    pool.close()
+    pool.join()
+    sec = sum(times) / len(times)
+    return {"value": round(n * TOPK * SLOT_BYTES["int8_side"] / sec / 1e9, 4), "unit": "GB/s", "cores": len(chunks),
+            "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"first {n} of 2048 rows (and their {n} new tokens) per step, mean of {repeats} steps, fp64 "
+                      f"numpy oracle, rows split over {len(chunks)} forked workers with 1 BLAS thread each; "
+                      f"{round(n / sec, 1)} rows/s"}
 
 
 def cpu_model() -> str:
@@ -269,7 +311,7 @@ def run_reference(args):
     sec = sum(times) / len(times)
     gbs = n * TOPK * SLOT_BYTES["int8_side"] / sec / 1e9
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"page-1 shape, oracle sample of {n} of 2048 rows", "rows": ROWS, "topk": TOPK,
@@ -289,12 +331,21 @@ def run_reference(args):
 
 def main():
     args = parse_args()
+    if args.gpus < 1:
+        raise SystemExit("bench.py: --gpus must be >= 1")
+    if not check_world(args):
+        if args.impl == "ours":
+            import torch
+            if torch.cuda.device_count() < args.gpus:
+                raise SystemExit(f"bench.py: --gpus {args.gpus} but {torch.cuda.device_count()} GPU(s) are visible")
+        raise SystemExit(launch_ranks(args.gpus, sys.argv[1:]))
     if args.impl == "reference":
         run_reference(args)
         return
     rank, world, local = dist_env()
     if world > 1 or rank == 0:
         os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+        os.environ.setdefault("OMP_NUM_THREADS", "1")
     import numpy as np
     import torch
     import torch.distributed as dist
@@ -304,6 +355,13 @@ def main():
     import quantized_kv_cache_write_gb300 as q
     from gen import page1_shape
 
+    # the CPU baseline's worker pool is forked now, before this process touches the GPU (a
+    # process forked after CUDA starts cannot use it, and forking then is unsafe)
+    wl = page1_shape(1)
+    oracle_pool = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        oracle_pool = start_oracle_pool(wl)
+
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -311,7 +369,6 @@ def main():
     stream = torch.cuda.current_stream()
 
     # ---- setup (untimed): every rank runs its own page-1 shape problem (weak scaling)
-    wl = page1_shape(1)
     S, H, D = wl.num_slots, 1, HEAD_DIM
     bf = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
     k_tok, v_tok = bf(wl.k_tokens), bf(wl.v_tokens)
@@ -409,8 +466,7 @@ def main():
                      "kernel": "gather_attn_kernel<QKV_INT8_SIDE>",
                      "algorithmic_bytes_per_launch": gathered, "peak_source": peak_src,
                      "ncu": ({k: float(v) for k, v in prof.items() if k not in ("kernel_source_sha256_16",)}
-                             if (prof := load_profile()) else None),
-                     "ncu_source": "profiles/gather_int8_side_page1_full.md (same kernel source hash)"},
+                             if (prof := load_profile()) else None)},
         "wall_s_timed_region": round(t_wall, 3),
         "pages_context": {"gb10_side_ms": 9.6, "gb10_inline_ms": 60.2,
                           "note": "one GB10 (sm_121), Triton path; context only"},
@@ -475,18 +531,8 @@ def main():
     if not args.no_workloads and rank == 0:
         result["workloads"] = measure_workloads(q, flush, stream, max(5, min(args.steps, 20)), peak)
 
-    if rank == 0 and not args.no_cpu_baseline:
-        K, V = oracle_setup(wl)
-        n = args.cpu_sample_rows or 64
-        rows = list(range(n))
-        time_oracle(wl, K, V, rows, 1)
-        times = time_oracle(wl, K, V, rows, 3)
-        sec = sum(times) / len(times)
-        result["cpu_baseline"] = {
-            "value": round(n * TOPK * SLOT_BYTES["int8_side"] / sec / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
-            "sample": f"first {n} of 2048 rows (and their {n} new tokens) per step, mean of 3 steps, fp64 numpy "
-                      f"oracle, 1 BLAS thread; {round(n / sec, 1)} rows/s"}
+    if oracle_pool is not None:
+        result["cpu_baseline"] = time_oracle_pool(oracle_pool, args.cpu_sample_rows)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -674,6 +720,33 @@ def _time_graph(fn, flush, stream, reps):
     return ms
 
 
+def measure_l2_roof(stream, reps=20):
+    """An L2 bandwidth roof: the best of torch's sum (a read) and copy (a read plus a write) over
+    buffers of 16 to 64 MiB, well inside the 129 MB L2, each warmed once and then timed with
+    CUDA events (no flush: the point is to stay in L2). GB/s of bytes moved."""
+    import torch
+    best = {"sum": 0.0, "copy": 0.0}
+    for mib in (16, 32, 64):
+        n = (mib << 20) // 4
+        a = torch.ones(n, dtype=torch.float32, device="cuda")
+        b = torch.empty_like(a)
+        for name, fn, nbytes in (("sum", lambda: a.sum(), 4 * n), ("copy", lambda: b.copy_(a), 8 * n)):
+            fn()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            e1.synchronize()
+            best[name] = max(best[name], nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+        del a, b
+    torch.cuda.empty_cache()
+    return {"GBps": round(max(best.values()), 1), "read_GBps": round(best["sum"], 1),
+            "copy_GBps": round(best["copy"], 1),
+            "how": "best of torch sum (read) and copy (read + write) over 16-64 MiB L2-resident buffers"}
+
+
 def measure_workloads(q, flush, stream, reps, peak):
     """The pages' other workload shapes, gather path only (context; the metric is the page-1 shape).
 
@@ -814,14 +887,18 @@ def measure_workloads(q, flush, stream, reps, peak):
     gv = _time_events(lambda: q.qsa_gather_attn_varlen(qd, q.QKV_INT8_SIDE, kc, vc, idx, lens, wl.softmax_scale,
                                                        out=out, k_scale_tok=ks, v_scale_tok=vs), flush, stream, reps)
     visits = int((wl.topk >= 0).sum())
+    l2 = measure_l2_roof(stream)
     res["chunked_prefill"] = {
         "shape": "8192 new tokens into a 524288-slot pool; 8192 rows, row i attends min(1024, i) earlier tokens",
         "write_int8_ms": round(w8, 5), "write_e4m3_ms": round(we, 5),
         "write_int8_GBps": round(8192 * (1024 + 520) / (w8 * 1e-3) / 1e9, 2),
         "gather_int8_side_ms": round(g, 5), "gather_varlen_ms": round(gv, 5), "slot_visits": visits,
         "gather_GBps": round(visits * SLOT_BYTES["int8_side"] / (g * 1e-3) / 1e9, 2),
+        "gather_varlen_GBps": round(visits * SLOT_BYTES["int8_side"] / (gv * 1e-3) / 1e9, 2),
+        "l2_roof": l2,
+        "gather_varlen_frac_of_l2_roof": round(visits * SLOT_BYTES["int8_side"] / (gv * 1e-3) / 1e9 / l2["GBps"], 4),
         "note": "the 8192 written slots (4.3 MB) stay in L2: gathered GB/s is bounded by L2, not HBM "
-                f"(measured HBM peak {peak} GB/s)"}
+                f"(measured HBM peak {peak} GB/s; L2 roof measured here)"}
     del kc, vc, ec, evc
     torch.cuda.empty_cache()
 

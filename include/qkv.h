@@ -398,8 +398,10 @@ qkv_status qsa_suggest_num_splits(qkv_format fmt, int64_t rows, int num_q_heads,
  *   or 40 rows x 16 splits x 16 heads); larger calls return QKV_ERR_ARG and launch nothing.
  *   Set-up: the first call on each device looks up the array's device address with
  *   cudaGetSymbolAddress while that device is current; make that first call before any
- *   stream capture. The array is held by every GPU that loads the library until the process
- *   exits. All calls share it and it keeps the last call's partials (every partial is
+ *   stream capture. The cached address belongs to the device's current context: do not keep
+ *   using the library across cudaDeviceReset (or any other teardown of the primary context),
+ *   since the next call would reuse the old address. The array is held by every GPU that loads
+ *   the library until the process exits. All calls share it and it keeps the last call's partials (every partial is
  *   rewritten before it is read, so nothing needs clearing): calls that overlap on the GPU --
  *   on different streams or from different host threads -- race and corrupt each other.
  */

@@ -58,16 +58,19 @@ extern "C" qkv_status qsa_gather_attn_splitk_noalloc(
                            out, lse, nullptr, nullptr, dev_status, stream);
   if (rows < 0 || num_q_heads < 1 || num_splits < 1 || !qkv::head_dim_ok(head_dim)) return QKV_ERR_ARG;
   if (rows == 0) return QKV_OK;
-  if (static_cast<uint64_t>(rows) > kScratchBytes || static_cast<uint64_t>(num_splits) > kScratchBytes)
-    return QKV_ERR_ARG;
   if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 15) != 0) return QKV_ERR_ARG;
   if (lse != nullptr && (reinterpret_cast<uintptr_t>(lse) & 3) != 0) return QKV_ERR_ALIGN;
 
   // Partials layout inside the scratch: o_part [rows, P, Hq, head_dim] fp32, then lse_part
-  // [rows, P, Hq] fp32 starting on a 256 B boundary. Sizes beyond the array are refused.
-  const uint64_t parts = static_cast<uint64_t>(rows) * static_cast<uint64_t>(num_splits) *
-                         static_cast<uint64_t>(num_q_heads);
-  if (parts > kScratchBytes) return QKV_ERR_ARG;
+  // [rows, P, Hq] fp32 starting on a 256 B boundary. Sizes beyond the array are refused. Each
+  // factor is bounded by division before it multiplies, so the product cannot wrap.
+  const uint64_t cap = kScratchBytes;
+  if (static_cast<uint64_t>(rows) > cap) return QKV_ERR_ARG;
+  const uint64_t rp_cap = cap / static_cast<uint64_t>(rows);
+  if (static_cast<uint64_t>(num_splits) > rp_cap) return QKV_ERR_ARG;
+  const uint64_t rp = static_cast<uint64_t>(rows) * static_cast<uint64_t>(num_splits);  // <= cap
+  if (static_cast<uint64_t>(num_q_heads) > cap / rp) return QKV_ERR_ARG;
+  const uint64_t parts = rp * static_cast<uint64_t>(num_q_heads);  // <= cap
   const uint64_t o_bytes = parts * static_cast<uint64_t>(head_dim) * sizeof(float);
   const uint64_t lse_off = (o_bytes + 255) & ~uint64_t(255);
   if (lse_off + parts * sizeof(float) > kScratchBytes) return QKV_ERR_ARG;

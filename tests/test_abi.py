@@ -400,3 +400,21 @@ def test_write_ex_host_validation(lib):
     assert call(fmt=E.QKV_INT8_INLINE) == E.QKV_ERR_ARG  # inline records hold their scales
     assert call(num_tokens=0) == E.QKV_OK
     assert call(**{**paged, "num_tokens": 0}) == E.QKV_OK
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch_before_any_cuda_call(lib):
+    """The no-allocation split gather bounds each factor of its partials' size before it
+    multiplies them, so no product can wrap past the check (num_q_heads alone may be large)."""
+    L = lib.lib
+
+    def call(rows, hq, P, hkv=1):
+        return L.qsa_gather_attn_splitk_noalloc(FAKE, rows, hq, hkv, 256, lib.QKV_INT8_SIDE, FAKE, FAKE, FAKE, FAKE,
+                                                1.0, 1.0, 100, FAKE, 8, 0.0625, P, FAKE, None, None, None)
+
+    big = 2 ** 31 - 1
+    assert call(2 ** 20, big, 2 ** 20) == lib.QKV_ERR_ARG  # the 64-bit product would wrap
+    assert call(2 ** 24, 16, 2 ** 24) == lib.QKV_ERR_ARG
+    assert call(1, big, 2) == lib.QKV_ERR_ARG
+    assert call(2 ** 25, 16, 2) == lib.QKV_ERR_ARG
+    assert call(64, 16, 16) == lib.QKV_ERR_ARG  # 64 x 16 x 16 x 257 x 4 B: just past 16 MiB
+    assert call(0, 16, 8) == lib.QKV_OK  # nothing to do, nothing launched
