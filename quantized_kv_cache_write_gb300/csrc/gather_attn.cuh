@@ -59,11 +59,10 @@
 namespace qkv {
 namespace gather {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
 constexpr int kKeys = 16;  // keys per warp tile
 constexpr int kHeadsPerCta = 16;  // query heads per CTA: the M = 16 of the MMAs
 constexpr int kQkChains = 4;      // q.K^T accumulator chains per N-tile (one per 64 head dims)
+constexpr int kQGrain = 7;        // int8 layouts: q_hi is a multiple of 2^7 (see Fmt::kQSplit)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kMaxFinite = 3.4028234663852886e38f;  // largest finite fp32
@@ -78,40 +77,48 @@ constexpr int kPShift = 7;      // x < 2^15; a key 2^-21 below the running max s
 constexpr int kEuHeadroom = 2;  // int8: the V-scale bound 2^eu is raised 2^2 past the largest scale seen
 
 // Per-layout traits. kKShift: extra offset of the odd K rows. Row sizes depend on the head
-// dim too: see Geom.
+// dim too: see Geom. kWarps: warps per CTA. kQSplit (the int8 layouts): the query is staged
+// twice, q_hi = the pre-scaled query rounded to a multiple of 2^7 and q_lo = the rest, and
+// q.K^T runs on both. With integer codes every partial sum of q_hi . c is a multiple of 2^7
+// below 2^31, exactly representable in fp32, so that half of the dot product is exact in
+// whatever order the MMAs add; q_lo . c is 2^8 times smaller, so its rounding is too. The logit
+// is then formed relative to a reference with fused multiply-adds (see the softmax below), which
+// keeps the dot product's precision where it matters: a row whose output is a near cancellation
+// of two outlier keys with opposite values needs more than a rounded fp32 logit. The second
+// staged query does not fit three CTAs of four warps on an SM; two CTAs of five warps do.
 template <int FMT>
 struct Fmt;
 template <>
 struct Fmt<QKV_INT8_SIDE> {
-  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64;
+  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 64, kWarps = 5;
   static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false, kNatural = true;
-  static constexpr bool kWide = false, kF16 = false;
+  static constexpr bool kWide = false, kF16 = false, kQSplit = true;
 };
 template <>
 struct Fmt<QKV_INT8_INLINE> {
-  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 16;
+  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 16, kWarps = 5;
   static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false, kNatural = false;
-  static constexpr bool kWide = false, kF16 = false;
+  static constexpr bool kWide = false, kF16 = false, kQSplit = true;
 };
 template <>
 struct Fmt<QKV_E4M3> {
-  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64;
+  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false, kNatural = true;
-  static constexpr bool kWide = false, kF16 = false;
+  static constexpr bool kWide = false, kF16 = false, kQSplit = false;
 };
 template <>
 struct Fmt<QKV_BF16> {
-  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16;
+  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true, kNatural = false;
-  static constexpr bool kWide = true, kF16 = false;
+  static constexpr bool kWide = true, kF16 = false, kQSplit = false;
 };
 // fp16 pool: the unquantised cache of the FP16-activation contract; moved like bf16 rows,
 // multiplied as fp16 (q must be fp16 too)
 template <>
 struct Fmt<QKV_F16> {
-  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16;
+  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = false, kNatural = false;
-  static constexpr bool kWide = true, kF16 = true;
+  static constexpr bool kWide = true, kF16 = true, kQSplit = false;
 };
 
 // Head-dim dependent sizes (HD = 128 or 256).
@@ -126,6 +133,9 @@ struct Geom {
   static constexpr int kRowBytes = Fmt<FMT>::kInline ? HD + 16 : (Fmt<FMT>::kWide ? 2 * HD : HD);
   static constexpr int kGlobalRow = Fmt<FMT>::kInline ? HD + 4 : (Fmt<FMT>::kWide ? 2 * HD : HD);
   static constexpr int kBlocks = HD / 64, kSweeps = HD / 128, kTmemCols = HD / 2;
+  // columns allocated per CTA: warp w uses lanes 32 (w % 4) of columns kTmemCols (w / 4) ..
+  static constexpr int kTmemAlloc = kTmemCols * ((Fmt<FMT>::kWarps + 3) / 4);
+  static_assert((kTmemAlloc & (kTmemAlloc - 1)) == 0 && kTmemAlloc >= 32, "tensor-memory allocations are powers of two");
 };
 
 // V region i (rows i and i + 8) starts 16 B further along the bank cycle than a plain packing
@@ -144,8 +154,11 @@ template <int FMT, int HD = 256, int STAGES = Fmt<FMT>::kStages>
 struct Smem {
   using F = Fmt<FMT>;
   using G = Geom<FMT, HD>;
+  static constexpr int kWarps = F::kWarps;
   static constexpr size_t kQ = 0;  // [HD / 16 k-steps][16 heads][16] 16-bit, fragment order
-  static constexpr size_t kQBytes = (HD / 16) * 16 * 16 * 2;
+  static constexpr size_t kQOne = (HD / 16) * 16 * 16 * 2;
+  static constexpr size_t kQ2 = kQ + kQOne;  // the same for q_lo (split layouts)
+  static constexpr size_t kQBytes = kQOne * (F::kQSplit ? 2 : 1);
   static constexpr size_t kFac = kQ + kQBytes;  // [16] floats: logit factor per head
   // one stage: K rows, V rows, side scales (K then V), inline record offsets
   static constexpr size_t kKArea = 2 * 8 * size_t(G::kRowBytes) + F::kKShift;
@@ -172,7 +185,7 @@ struct Smem {
   static_assert(kRing % 16 == 0 && kKArea % 16 == 0 && kVArea % 16 == 0, "alignment");
   // the CTAs that fit an SM (228 KB of shared memory, 1 KB reserved each) never ask for more
   // than its 512 TMEM columns, so an allocation never has to wait for another CTA
-  static_assert((233472 / (kTotal + 1024)) * G::kTmemCols <= 512, "TMEM budget");
+  static_assert((233472 / (kTotal + 1024)) * G::kTmemAlloc <= 512, "TMEM budget");
 };
 
 // Key row (0..15 within a tile) feeding column n of N-tile nt of q.K^T -- and so the key whose
@@ -212,6 +225,14 @@ __device__ __forceinline__ uint32_t v_row_off(int r) {
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
 
+// ks (acc + accl) - R with the product and the subtraction fused: near the reference the
+// difference keeps the dot product's full precision (SPLIT: accl is the q_lo part)
+template <bool SPLIT>
+__device__ __forceinline__ float logit_rel(float ks, float acc, float accl, float R) {
+  const float u = fmaf(ks, acc, -R);
+  return SPLIT ? fmaf(ks, accl, u) : u;
+}
+
 // Byte offset of query element (k-step k, head hd, k-index kappa) in the staged query.
 __device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
   return k * 512 + hd * 32 + ((((kappa >> 3) ^ ((hd >> 2) & 1))) << 4) + (kappa & 7) * 2;
@@ -226,10 +247,11 @@ __device__ __forceinline__ uint32_t q_off(int k, int hd, int kappa) {
 // the query is staged.
 template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks,
           bool QF16 = false, int HD = 256>
-__global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const GatherArgs a) {
+__global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kernel(const GatherArgs a) {
   using F = Fmt<FMT>;
   using GM = Geom<FMT, HD>;
   using L = Smem<FMT, HD, STAGES>;
+  constexpr int kWarps = F::kWarps, kThreads = 32 * kWarps;
   static_assert(STAGES >= 2, "the ring needs a stage in flight while one is computed");
   static_assert(!(F::kBf16 && QF16) && !(F::kF16 && !QF16), "a 16-bit pool takes a query of its own type");
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -266,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   const uint32_t sQ = smem_u32(smem + L::kQ);
   uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kTmem);
   if (warp == 0) {
-    tmem_alloc(smem_u32(sTmem), GM::kTmemCols);
+    tmem_alloc(smem_u32(sTmem), GM::kTmemAlloc);
     tmem_relinquish_alloc_permit();
   }
 
@@ -413,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   // The query's global loads go out first, then the first tiles' index loads and copies: the
   // copies wait for their indices, and the query's latency overlaps both.
   constexpr int kW = HD / 16;  // query: 32-bit words (two head dims each) per thread
-  const int qh = tid >> 3, part = tid & 7;
+  const int qh = tid >> 3, part = tid & 7;  // threads 0 .. 127 stage the query (8 per head)
   const bool live = qh < Gc;
   uint32_t w[kW];
   if (live) {
@@ -517,12 +539,20 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
             x1 = __uint_as_float(b1 << 16);
           }
           f2unpack(f2mul(f2pack(x0, x1), uu), s0, s1);
+          if (F::kQSplit) {  // q_hi on the 2^7 grid here, the remainder in the second copy
+            const float h0v = rintf(s0 * (1.0f / (1 << kQGrain))) * static_cast<float>(1 << kQGrain);
+            const float h1v = rintf(s1 * (1.0f / (1 << kQGrain))) * static_cast<float>(1 << kQGrain);
+            if (qh < kHeadsPerCta)
+              sts32(smem_u32(smem + L::kQ2 + q_off(blk * 4 + ks, qh, up * 8 + 2 * cc)), pack_half2(s0 - h0v, s1 - h1v));
+            s0 = h0v;
+            s1 = h1v;
+          }
           v32 = pack_half2(s0, s1);
         }
-        sts32(smem_u32(smem + L::kQ + q_off(blk * 4 + ks, qh, up * 8 + 2 * cc)), v32);
+        if (qh < kHeadsPerCta) sts32(smem_u32(smem + L::kQ + q_off(blk * 4 + ks, qh, up * 8 + 2 * cc)), v32);
       }
     }
-    if (part == 0) {
+    if (part == 0 && qh < kHeadsPerCta) {
       float base = a.softmax_scale * kLog2e;
       if (F::kE4m3) base *= a.k_scale_layer;
       sFac[qh] = live ? base * pow2f(-sg) : 0.f;
@@ -533,9 +563,10 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   tmem_fence_after_sync();
   const float fac0 = sFac[h0], fac1 = sFac[h1];
   const uint64_t fac00 = f2pack(fac0, fac0), fac11 = f2pack(fac1, fac1);
-  // this warp's accumulator: its 32 TMEM lanes, columns [0, 128); column 4 t + j holds the
-  // C-fragment value j of N-tile t
-  const uint32_t tacc = *sTmem + (static_cast<uint32_t>(32 * warp) << 16);
+  // this warp's accumulator: its 32 TMEM lanes (quarter warp % 4) of the columns
+  // kTmemCols (warp / 4) onwards; column 4 t + j holds the C-fragment value j of N-tile t
+  const uint32_t tacc = *sTmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) +
+                        static_cast<uint32_t>(GM::kTmemCols * (warp >> 2));
   {
     float z[32];
 #pragma unroll
@@ -545,7 +576,9 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   }
 
   // ---------------- online-softmax state (per warp)
-  float mu0 = -INFINITY, mu1 = -INFINITY;  // running max in use (log2 domain), heads h0, h1
+  // the reference in dot-product units (ks . q . k) the logits are taken against, heads h0, h1;
+  // -inf until the head's first valid key; a padded head (no query) keeps 0 with a zero factor
+  float R0 = (h0 < Gc) ? -INFINITY : 0.f, R1 = (h1 < Gc) ? -INFINITY : 0.f;
   // this thread's share of sum p for heads h0 (l0) and h1 (l1), each kept as a pair of
   // partial sums (keys e = 0 and e = 1) so that it accumulates with packed adds
   uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
@@ -608,16 +641,21 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       }
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
-        uint32_t qa[4];
+        uint32_t qa[4], ql[4];
         {
           const int mtx = lane >> 3, j = lane & 7;
           const int hd = (mtx & 1) * 8 + j;
-          ldmatrix_x4(sQ + (blk * 4 + ks) * 512 + hd * 32 + ((((mtx >> 1) ^ ((hd >> 2) & 1))) << 4), qa[0], qa[1],
-                      qa[2], qa[3]);
+          const uint32_t qoff = (blk * 4 + ks) * 512 + hd * 32 + ((((mtx >> 1) ^ ((hd >> 2) & 1))) << 4);
+          ldmatrix_x4(sQ + qoff, qa[0], qa[1], qa[2], qa[3]);
+          if (F::kQSplit) ldmatrix_x4(sQ + L::kQOne + qoff, ql[0], ql[1], ql[2], ql[3]);
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-          if (F::kBf16) {
+          if (F::kQSplit) {  // q_hi chains 0, 1 (even / odd 64-dim blocks), q_lo chains 2, 3
+            const uint32_t b0 = i8pair_to_f16x2(kw[nt][ks]), b1 = i8pair_to_f16x2(kw[nt][ks] >> 8);
+            mma_f16(accc[blk & 1][nt], qa, b0, b1);
+            mma_f16(accc[2 + (blk & 1)][nt], ql, b0, b1);
+          } else if (F::kBf16) {
             mma_bf16(accc[blk % kQkChains][nt], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
           } else if (F::kF16) {
             mma_f16(accc[blk % kQkChains][nt], qa, kw[nt][2 * ks], kw[nt][2 * ks + 1]);
@@ -630,17 +668,30 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       }
     }
 
-    float acc[2][4];
+    // acc: the dot products (split layouts: the exact q_hi part); accl: the q_lo part
+    float acc[2][4], accl[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      uint64_t a01 = f2pack(accc[0][nt][0], accc[0][nt][1]), a23 = f2pack(accc[0][nt][2], accc[0][nt][3]);
+      if (F::kQSplit) {  // q_hi chains hold multiples of 2^7 below 2^31: their sum is exact
+        uint64_t a01 = f2add(f2pack(accc[0][nt][0], accc[0][nt][1]), f2pack(accc[1][nt][0], accc[1][nt][1]));
+        uint64_t a23 = f2add(f2pack(accc[0][nt][2], accc[0][nt][3]), f2pack(accc[1][nt][2], accc[1][nt][3]));
+        f2unpack(a01, acc[nt][0], acc[nt][1]);
+        f2unpack(a23, acc[nt][2], acc[nt][3]);
+        a01 = f2add(f2pack(accc[2][nt][0], accc[2][nt][1]), f2pack(accc[3][nt][0], accc[3][nt][1]));
+        a23 = f2add(f2pack(accc[2][nt][2], accc[2][nt][3]), f2pack(accc[3][nt][2], accc[3][nt][3]));
+        f2unpack(a01, accl[nt][0], accl[nt][1]);
+        f2unpack(a23, accl[nt][2], accl[nt][3]);
+      } else {
+        accl[nt][0] = accl[nt][1] = accl[nt][2] = accl[nt][3] = 0.f;  // (no q_lo part)
+        uint64_t a01 = f2pack(accc[0][nt][0], accc[0][nt][1]), a23 = f2pack(accc[0][nt][2], accc[0][nt][3]);
 #pragma unroll
-      for (int ch = 1; ch < kQkChains; ++ch) {
-        a01 = f2add(a01, f2pack(accc[ch][nt][0], accc[ch][nt][1]));
-        a23 = f2add(a23, f2pack(accc[ch][nt][2], accc[ch][nt][3]));
+        for (int ch = 1; ch < kQkChains; ++ch) {
+          a01 = f2add(a01, f2pack(accc[ch][nt][0], accc[ch][nt][1]));
+          a23 = f2add(a23, f2pack(accc[ch][nt][2], accc[ch][nt][3]));
+        }
+        f2unpack(a01, acc[nt][0], acc[nt][1]);
+        f2unpack(a23, acc[nt][2], acc[nt][3]);
       }
-      f2unpack(a01, acc[nt][0], acc[nt][1]);
-      f2unpack(a23, acc[nt][2], acc[nt][3]);
     }
 
     // ---- logits with the hoisted K scale; masked keys -> -inf
@@ -662,6 +713,8 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
       }
       vmx_bits = __reduce_max_sync(0xffffffffu, vb & 0x7FFFFFFFu);
     }
+    float kscs[2][2];
+    bool valids[2][2];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       float ksc2[2];
@@ -684,11 +737,16 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
         vsc[nt][e] = vs;
         ksc2[e] = ksc;
       }
+      kscs[nt][0] = ksc2[0];
+      kscs[nt][1] = ksc2[1];
+      valids[nt][0] = valid2[0];
+      valids[nt][1] = valid2[1];
       // logits of keys e = 0, 1 for heads h0 (acc 0, 1) and h1 (acc 2, 3), as fp32 pairs
-      const uint64_t kk = f2pack(ksc2[0], ksc2[1]);
-      float t0, t1, t2, t3;
-      f2unpack(f2mul(f2pack(acc[nt][0], acc[nt][1]), f2mul(fac00, kk)), t0, t1);
-      f2unpack(f2mul(f2pack(acc[nt][2], acc[nt][3]), f2mul(fac11, kk)), t2, t3);
+      // relative to the references (ks . acc - R, one rounding near the maximum), in log2 units
+      const float t0 = logit_rel<F::kQSplit>(ksc2[0], acc[nt][0], accl[nt][0], R0) * fac0;
+      const float t1 = logit_rel<F::kQSplit>(ksc2[1], acc[nt][1], accl[nt][1], R0) * fac0;
+      const float t2 = logit_rel<F::kQSplit>(ksc2[0], acc[nt][2], accl[nt][2], R1) * fac1;
+      const float t3 = logit_rel<F::kQSplit>(ksc2[1], acc[nt][3], accl[nt][3], R1) * fac1;
       s[nt][0] = valid2[0] ? t0 : -INFINITY;
       s[nt][1] = valid2[1] ? t1 : -INFINITY;
       s[nt][2] = valid2[0] ? t2 : -INFINITY;
@@ -706,47 +764,71 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
     bool rescale;
     float rf0 = 1.f, rf1 = 1.f;  // accumulator factors for heads h0, h1 when rescaling
     {
-      const float nm0 = (mx0 > mu0 + kTau) ? mx0 : mu0;
-      const float nm1 = (mx1 > mu1 + kTau) ? mx1 : mu1;
-      // int8: when a V scale reaches 2^eu, raise eu to kEuHeadroom past it (and rescale), so
-      // that every V scale stays below 2^eu and x below 2^15.
+      // a logit more than 2^kTau above its reference (any valid key when there is none yet), or
+      // an int8 V scale at the bound, moves the reference to the tile's largest ks . (q . k)
       int ne = eu;
-      if (F::kInt8 && vmx_bits != 0u) {
-        const int ev = static_cast<int>(vmx_bits >> 23) - 126;  // 2^ev > the largest |V scale|
+      if (vmx_bits != 0u) {
+        const int ev = static_cast<int>(vmx_bits >> 23) - 126;
         if (ev > eu) ne = ev + kEuHeadroom;
       }
-      // an accumulator row whose head has seen no valid key yet is still zero: it needs no rescale
-      const bool live0 = mu0 != -INFINITY, live1 = mu1 != -INFINITY;
-      rescale = __any_sync(0xffffffffu, (live0 && (nm0 != mu0 || ne != eu)) || (live1 && (nm1 != mu1 || ne != eu)));
-      if (rescale) {  // rare: the factors are only formed here
+      const bool up0 = mx0 > kTau, up1 = mx1 > kTau;
+      rescale = false;
+      if (__any_sync(0xffffffffu, up0 || up1 || ne != eu)) {
+        float v0 = -INFINITY, v1 = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if (valids[nt][e]) {
+              v0 = fmaxf(v0, kscs[nt][e] * (F::kQSplit ? acc[nt][e] + accl[nt][e] : acc[nt][e]));
+              v1 = fmaxf(v1, kscs[nt][e] * (F::kQSplit ? acc[nt][2 + e] + accl[nt][2 + e] : acc[nt][2 + e]));
+            }
+          }
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+          v0 = fmaxf(v0, __shfl_xor_sync(0xffffffffu, v0, off));
+          v1 = fmaxf(v1, __shfl_xor_sync(0xffffffffu, v1, off));
+        }
+        const float nR0 = up0 ? v0 : R0, nR1 = up1 ? v1 : R1;
+        const bool live0 = R0 != -INFINITY, live1 = R1 != -INFINITY;
+        rescale = __any_sync(0xffffffffu, (live0 && (nR0 != R0 || ne != eu)) || (live1 && (nR1 != R1 || ne != eu)));
         const float ov = F::kInt8 ? pow2f(max(eu - ne, -126)) : 1.f;
-        const float al0 = (nm0 == mu0) ? 1.f : fast_exp2(mu0 - nm0);  // mu0 = -inf gives 0
-        const float al1 = (nm1 == mu1) ? 1.f : fast_exp2(mu1 - nm1);
+        const float al0 = (nR0 == R0) ? 1.f : (live0 ? fast_exp2((R0 - nR0) * fac0) : 0.f);
+        const float al1 = (nR1 == R1) ? 1.f : (live1 ? fast_exp2((R1 - nR1) * fac1) : 0.f);
         rf0 = al0 * ov;
         rf1 = al1 * ov;
         l0 = f2mul(l0, f2pack(al0, al0));
         l1 = f2mul(l1, f2pack(al1, al1));
+        R0 = nR0;
+        R1 = nR1;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float k = kscs[nt][e];
+            s[nt][e] = valids[nt][e] ? logit_rel<F::kQSplit>(k, acc[nt][e], accl[nt][e], R0) * fac0 : -INFINITY;
+            s[nt][2 + e] =
+                valids[nt][e] ? logit_rel<F::kQSplit>(k, acc[nt][2 + e], accl[nt][2 + e], R1) * fac1 : -INFINITY;
+          }
       }
-      mu0 = nm0;
-      mu1 = nm1;
       eu = ne;
     }
 
-    // ---- p = exp2(s - m): fp32 sums, hi + lo A fragments
-    uint32_t pa[4], pl[4];
+    // ---- p = exp2(logit relative to the reference): fp32 sums, hi + lo A fragments (bf16: hi,
+    //      mid, lo -- three bf16 parts hold the 24 bits two fp16 parts give)
+    uint32_t pa[4], pl[4], p3[4];
     {
       const float pm = F::kInt8 ? pow2f(kPShift - eu) : (F::kBf16 ? 1.f : pow2f(kPShift));
-      // a head whose max is still -inf has only masked (-inf) logits: subtracting the most
-      // negative finite float instead gives exp2(-inf) = 0 rather than exp2(NaN)
-      const float m0 = fmaxf(mu0, -kMaxFinite), m1 = fmaxf(mu1, -kMaxFinite);
-      const uint64_t mm0 = f2pack(m0, m0), mm1 = f2pack(m1, m1), pm2 = f2pack(pm, pm);
+      const uint64_t pm2 = f2pack(pm, pm);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         float p[4];
         {
           float d0, d1, d2, d3;
-          f2unpack(f2sub(f2pack(s[nt][0], s[nt][1]), mm0), d0, d1);
-          f2unpack(f2sub(f2pack(s[nt][2], s[nt][3]), mm1), d2, d3);
+          d0 = s[nt][0];  // the logits are already relative to the references
+          d1 = s[nt][1];
+          d2 = s[nt][2];
+          d3 = s[nt][3];
           p[0] = fast_exp2(d0);  // masked: exp2(-inf) = 0
           p[1] = fast_exp2(d1);
           p[2] = fast_exp2(d2);
@@ -766,10 +848,17 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
           const __nv_bfloat162 a0 = __floats2bfloat162_rn(x0, x1), a1 = __floats2bfloat162_rn(x2, x3);
           pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&a0);
           pa[2 * nt + 1] = *reinterpret_cast<const uint32_t*>(&a1);
-          f2unpack(f2sub(x01, f2pack(__low2float(a0), __high2float(a0))), r0, r1);
-          f2unpack(f2sub(x23, f2pack(__low2float(a1), __high2float(a1))), r2, r3);
-          pl[2 * nt] = pack_bf162(r0, r1);
-          pl[2 * nt + 1] = pack_bf162(r2, r3);
+          const uint64_t y01 = f2sub(x01, f2pack(__low2float(a0), __high2float(a0)));
+          const uint64_t y23 = f2sub(x23, f2pack(__low2float(a1), __high2float(a1)));
+          f2unpack(y01, r0, r1);
+          f2unpack(y23, r2, r3);
+          const __nv_bfloat162 b0 = __floats2bfloat162_rn(r0, r1), b1 = __floats2bfloat162_rn(r2, r3);
+          pl[2 * nt] = *reinterpret_cast<const uint32_t*>(&b0);
+          pl[2 * nt + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+          f2unpack(f2sub(y01, f2pack(__low2float(b0), __high2float(b0))), r0, r1);
+          f2unpack(f2sub(y23, f2pack(__low2float(b1), __high2float(b1))), r2, r3);
+          p3[2 * nt] = pack_bf162(r0, r1);
+          p3[2 * nt + 1] = pack_bf162(r2, r3);
         } else {
           const __half2 a0 = __floats2half2_rn(x0, x1), a1 = __floats2half2_rn(x2, x3);
           pa[2 * nt] = *reinterpret_cast<const uint32_t*>(&a0);
@@ -901,6 +990,10 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
           else
             mma_f16(acc4, pl, bb[tt][0], bb[tt][1]);
         }
+        if (F::kBf16) {
+#pragma unroll
+          for (int tt = 0; tt < 16; ++tt) mma_bf16(&ob[tt >> 3][4 * (tt & 7)], p3, bb[tt][0], bb[tt][1]);
+        }
         tmem_st32(tacc + 64 * sw, ob[0]);
         tmem_st32(tacc + 64 * sw + 32, ob[1]);
       }
@@ -923,6 +1016,8 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   float* sM = reinterpret_cast<float*>(smem + L::kM);
   float* sL = reinterpret_cast<float*>(smem + L::kL);
   float* sPost = reinterpret_cast<float*>(smem + L::kPost);
+  // the references in log2 units (-inf for a head that saw no valid key)
+  const float mu0 = R0 * fac0, mu1 = R1 * fac1;
   if (c == 0) {
     sM[warp * 16 + h0] = mu0;
     sM[warp * 16 + h1] = mu1;
@@ -1066,7 +1161,7 @@ __global__ void __launch_bounds__(kThreads, MINB) gather_attn_kernel(const Gathe
   tmem_fence_before_sync();
   __syncthreads();
   tmem_fence_after_sync();
-  if (warp == 0) tmem_dealloc(*sTmem, GM::kTmemCols);
+  if (warp == 0) tmem_dealloc(*sTmem, GM::kTmemAlloc);
 }
 
 // CTAs of one launch: (row, KV head, 16-head chunk, split).
@@ -1105,7 +1200,7 @@ cudaError_t launch_variant(const GatherArgs& a, cudaStream_t stream) {
   cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB, QF16, HD>();
   if (e != cudaSuccess) return e;
   gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>
-      <<<static_cast<unsigned>(gather_grid(a)), kThreads, Smem<FMT, HD, STAGES>::kTotal, stream>>>(a);
+      <<<static_cast<unsigned>(gather_grid(a)), 32 * Fmt<FMT>::kWarps, Smem<FMT, HD, STAGES>::kTotal, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -1139,7 +1234,7 @@ cudaError_t resident_ctas_per_sm(int* n) {
   const size_t per_cta = Smem<FMT, 256, S>::kTotal + fa.sharedSizeBytes + static_cast<size_t>(reserved);
   const int by_smem = static_cast<int>(static_cast<size_t>(smem_sm) / per_cta);
   const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
-  const int by_regs = regs_warp > 0 ? regs_sm / (regs_warp * kWarps) : by_smem;
+  const int by_regs = regs_warp > 0 ? regs_sm / (regs_warp * Fmt<FMT>::kWarps) : by_smem;
   *n = by_smem < by_regs ? by_smem : by_regs;
   return cudaSuccess;
 }
