@@ -652,6 +652,19 @@ def measure_formats(q, wl, q_dev, idx, flush, stream, steps, peak):
         gbs = ROWS * TOPK * SLOT_BYTES[fmt] / (m * 1e-3) / 1e9
         res[fmt] = {"gather_ms": round(m, 5), "gathered_GBps": round(gbs, 2), "frac_of_hbm_peak": round(gbs / peak, 4),
                     "rows_per_s": round(ROWS / (m * 1e-3), 1), "bytes_per_slot": SLOT_BYTES[fmt]}
+        # the other engines of the same gather: the resident-grid scheduler (every format) and
+        # q.K^T on tcgen05 with tensor-memory operands (int8 side only)
+        sched = torch.zeros(2, dtype=torch.int32, device="cuda")
+        engines = {"persistent": q.QSA_ENGINE_PERSISTENT}
+        if fmt == "int8_side":
+            engines["tcgen05"] = q.QSA_ENGINE_TCGEN05
+        for name, eng in engines.items():
+            t = _time_events(lambda eng=eng: q.qsa_gather_attn_ex(
+                q_dev, code, kc, vc, idx, wl.softmax_scale, out=out, engine=eng,
+                sched=sched if eng == q.QSA_ENGINE_PERSISTENT else None, **kw), flush, stream, steps)
+            g2 = ROWS * TOPK * SLOT_BYTES[fmt] / (t * 1e-3) / 1e9
+            res[fmt][name + "_engine"] = {"gather_ms": round(t, 5), "gathered_GBps": round(g2, 2),
+                                          "frac_of_hbm_peak": round(g2 / peak, 4)}
         del kc, vc
         torch.cuda.empty_cache()
     return res
@@ -825,6 +838,43 @@ def measure_workloads(q, flush, stream, reps, peak):
             E4M3_SPLITK_LAYERS * bytes_layer / (graph["fused_suggested_ms"] * 1e-3) / 1e9, 2),
         "graph_note": "one CUDA graph of the 12 layers' fused launches, L2 flushed once before each replay"}
     del fns
+
+    # mixed decode batches: rows of very different lengths in one varlen launch with the fused
+    # split-K merge, on the default grid (one CTA per work item) and on the persistent grid
+    from gen import bulk_tail_decode, mixed_catchup_decode
+    mixed = {}
+    for wname, make in (("catchup_46_plus_decode_3", mixed_catchup_decode), ("bulk_48_plus_tail_13", bulk_tail_decode)):
+        wl = make()
+        lens = torch.from_numpy(wl.row_len).cuda()
+        visits = int(wl.row_len.sum())
+        entry = {"shape": wl.name, "key_visits": visits}
+        for fmt in ("e4m3", "int8_side"):
+            kc, vc, kw, _ = _device_pool(q, wl, fmt)
+            qd = torch.from_numpy(np.ascontiguousarray(wl.q).view(np.int16)).view(torch.bfloat16).cuda()
+            idx = torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
+            R, Hq, D = wl.rows, wl.num_q_heads, HEAD_DIM
+            code = q.FORMATS[fmt]
+            Pa = q.qsa_suggest_num_splits(code, R, Hq, wl.num_kv_heads, wl.topk.shape[1])
+            sched = torch.zeros(2, dtype=torch.int32, device="cuda")
+            t = {"suggested_splits": Pa}
+            for P in sorted({8, Pa}):
+                out = torch.empty((R, Hq, D), dtype=torch.float32, device="cuda")
+                o_part = torch.empty((R, P, Hq, D), dtype=torch.float32, device="cuda")
+                lse_part = torch.empty((R, P, Hq), dtype=torch.float32, device="cuda")
+                cnt = torch.zeros((R, 1, 1), dtype=torch.int32, device="cuda")
+                for ename, eng in (("default", q.QSA_ENGINE_DEFAULT), ("persistent", q.QSA_ENGINE_PERSISTENT)):
+                    t[f"fused_P{P}_{ename}_ms"] = round(_time_events(lambda eng=eng, P=P, out=out, o_part=o_part,
+                                                                      lse_part=lse_part, cnt=cnt: q.qsa_gather_attn_ex(
+                        qd, code, kc, vc, idx, wl.softmax_scale, num_splits=P, out=out, o_part=o_part,
+                        lse_part=lse_part, counters=cnt, topk_len=lens, engine=eng,
+                        sched=sched if eng == q.QSA_ENGINE_PERSISTENT else None, **kw), flush, stream, reps), 5)
+            entry[fmt] = t
+            del kc, vc
+        mixed[wname] = entry
+    mixed["note"] = ("varlen + fused split-K merge in one launch; default = one CTA per (row, split) item, "
+                     "persistent = resident CTAs taking items from an atomic counter; L2 flushed before each launch")
+    res["mixed_decode"] = mixed
+    torch.cuda.empty_cache()
 
     # long-context decode: 8 x 131072 tokens, 40 rows x top-k 2048, 16 splits; also the paged kernel
     wl = long_context_decode(3)

@@ -9,7 +9,9 @@ from .workloads import (  # noqa: F401
     e4m3_splitk_layer,
     f32_to_bf16_bits,
     f32_to_f16_bits,
+    bulk_tail_decode,
     long_context_decode,
+    mixed_catchup_decode,
     page1_shape,
     small_paged,
     small_random,

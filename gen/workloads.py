@@ -20,6 +20,9 @@ Workload shapes follow the page workloads:
   split-K shape.
 * SuperPUPS/Qwen3.8-Flash-Next-INT8KV, §What it buys you: MTP k=4 decode (5 query
   positions per sequence).
+* [Model][SM70][FP8] Add calibrated E4M3 QSA KV cache, §Implementation scope and §Targeted
+  mixed-batch scheduler regression: a 49-row batch of a 46-row catch-up chunk plus three
+  decode rows; batches split into a bulk and tails of at most 16 rows.
 """
 
 from __future__ import annotations
@@ -84,6 +87,9 @@ class Workload:
     # 16-bit type of q and of the new K/V tokens: "bf16", or "f16" for the FP16-activation
     # contract of "[Model][SM70][FP8] Add calibrated E4M3 QSA KV cache" (§Purpose)
     act_dtype: str = "bf16"
+    # Rows of different lengths (the varlen launch): valid entries per row int32 [R]; entries
+    # of row r past row_len[r] are -1.
+    row_len: Optional[np.ndarray] = None
 
     @property
     def rows(self) -> int:
@@ -338,6 +344,68 @@ def small_paged(seed: int, num_seqs: int = 3, max_blocks: int = 6, block_size: i
                     seed, S, H, Hq, D, k, v, slot_mapping, q, None, softmax_scale=1.0 / 16.0,
                     block_table=table, row_seq=row_seq, topk_pos=pos, block_size=block_size,
                     notes="paged rows only: slot ids come from the block table")
+
+def mixed_catchup_decode(seed: int = 6, catchup_rows: int = 46, catchup_start: int = 64,
+                         decode_rows: int = 3, decode_context: int = 8192, topk: int = 2051,
+                         num_slots: int = 131072) -> Workload:
+    """A 49-row mixed batch: a 46-row catch-up chunk of one request plus three decode rows.
+
+    The catch-up chunk covers positions catchup_start .. catchup_start + 45 of its request, and
+    its row i attends every earlier position (catchup_start + i keys: short rows). Each decode
+    row belongs to a request of decode_context tokens and attends top-k 2051 distinct positions
+    of it. Every token of the four requests is written to its own slot of a shared pool; the
+    rows list slot ids, with -1 past each row's length (row_len).
+    """
+    H, D, G = 1, HEAD_DIM, 16
+    n_cu = catchup_start + catchup_rows
+    T = n_cu + decode_rows * decode_context
+    rng = np.random.default_rng(seed)
+    k = f32_to_bf16_bits(_normals(rng, (T, H, D)))
+    v = f32_to_bf16_bits(_normals(rng, (T, H, D)))
+    slot_mapping = rng.choice(num_slots, size=T, replace=False).astype(np.int64)
+    R = catchup_rows + decode_rows
+    q = f32_to_bf16_bits(_normals(rng, (R, H * G, D)))
+    idx = np.full((R, topk), -1, dtype=np.int32)
+    lens = np.zeros(R, dtype=np.int32)
+    for i in range(catchup_rows):
+        n = min(topk, catchup_start + i)
+        idx[i, :n] = slot_mapping[rng.permutation(catchup_start + i)[:n]]
+        lens[i] = n
+    for j in range(decode_rows):
+        base = n_cu + j * decode_context
+        idx[catchup_rows + j] = slot_mapping[base + rng.choice(decode_context, size=topk, replace=False)]
+        lens[catchup_rows + j] = topk
+    return Workload(f"mixed catch-up/decode batch ({catchup_rows} catch-up rows of "
+                    f"{catchup_start}..{n_cu - 1} keys + {decode_rows} decode rows of top-k {topk})",
+                    seed, num_slots, H, H * G, D, k, v, slot_mapping, q, idx,
+                    softmax_scale=1.0 / 16.0, num_splits=8, row_len=lens)
+
+
+def bulk_tail_decode(seed: int = 7, bulk_rows: int = 48, tail_rows: int = 13, topk: int = 2051,
+                     num_slots: int = 131072) -> Workload:
+    """A 16-divisible bulk of 48 full rows (top-k 2051) followed by a 13-row tail of mixed lengths.
+
+    Tail row j attends a length drawn uniformly from 1 .. 2051 (one tail row is forced to 1,
+    one to the full 2051). All rows gather distinct slots of one 131072-slot pool.
+    """
+    H, D, G = 1, HEAD_DIM, 16
+    rng = np.random.default_rng(seed)
+    k = f32_to_bf16_bits(_normals(rng, (num_slots, H, D)))
+    v = f32_to_bf16_bits(_normals(rng, (num_slots, H, D)))
+    slot_mapping = rng.permutation(num_slots).astype(np.int64)
+    R = bulk_rows + tail_rows
+    q = f32_to_bf16_bits(_normals(rng, (R, H * G, D)))
+    idx = _distinct_rows(rng, R, num_slots, topk).astype(np.int32)
+    lens = np.full(R, topk, dtype=np.int32)
+    lens[bulk_rows:] = rng.integers(1, topk + 1, tail_rows)
+    lens[bulk_rows] = 1
+    lens[bulk_rows + 1] = topk
+    for r in range(bulk_rows, R):
+        idx[r, lens[r]:] = -1
+    return Workload(f"bulk + tail decode batch ({bulk_rows} rows of top-k {topk} + {tail_rows} tail rows "
+                    f"of mixed length)", seed, num_slots, H, H * G, D, k, v, slot_mapping, q, idx,
+                    softmax_scale=1.0 / 16.0, num_splits=8, row_len=lens)
+
 
 CONFIGS = {
     1: tiny,

@@ -64,6 +64,10 @@ typedef enum {
 #define QKV_DEV_BAD_SLOT 1u  /* a write's slot is invalid (a slot_mapping entry >= num_slots or
                                  < -1, or a bad paged entry, see qkv_write_ex): token skipped */
 #define QKV_DEV_BAD_INDEX 2u /* top-k entry >= num_slots or < -1: treated as padding (-1) */
+#define QKV_DEV_TIMEOUT 4u   /* a gather CTA's bounded wait for its own copies or tensor-core
+                                work ran out (not expected on a healthy GPU): the CTA stopped
+                                early, its outputs are incomplete; the kernel returns instead of
+                                hanging */
 
 /*
  * qkv_write_int8 -- quantize new K/V tokens to int8 with one absmax scale per (token, head)
@@ -461,7 +465,25 @@ qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, i
  *   counters    NULL, or the fused merge's arrival counters (qsa_gather_attn_splitk_fused);
  *               with num_splits > 1, out (and optionally lse) then receive the merged result
  *               and o_part / lse_part are the workspace.
+ *   engine      QSA_ENGINE_DEFAULT, or QSA_ENGINE_TCGEN05: the same gather with q.K^T on the
+ *               fifth-generation tensor cores (tcgen05.mma, K dequantised into tensor memory)
+ *               in a warp-specialised CTA. It computes the same result to the same tolerance
+ *               and is slower on GB300 (the tensor-memory MMA issue rate bounds it); only
+ *               QKV_INT8_SIDE, head_dim 256, G <= 16, a bf16 query, no block table and no
+ *               counters, else QKV_ERR_UNSUPPORTED. QSA_ENGINE_PERSISTENT: the default
+ *               kernels on a persistent grid -- as many CTAs as stay resident, each taking
+ *               the next free work item (row, KV head, 16-head chunk, split) from the counter
+ *               sched[0] until none is left; no CTA waits for another. Any combination of the
+ *               options above. Any other value is QKV_ERR_ARG.
+ *   sched       QSA_ENGINE_PERSISTENT only (ignored otherwise): uint32 [2] on the device,
+ *               zero before the first call (cudaMemset); every launch leaves it zero again.
+ *               One launch at a time per sched buffer. NULL with that engine: QKV_ERR_ARG;
+ *               not 4-byte aligned: QKV_ERR_ALIGN.
  */
+#define QSA_ENGINE_DEFAULT 0
+#define QSA_ENGINE_TCGEN05 1
+#define QSA_ENGINE_PERSISTENT 2
+
 typedef struct {
   size_t size;
   const void* q;
@@ -494,6 +516,8 @@ typedef struct {
   int block_size;
   const int32_t* row_seq;
   uint32_t* counters;
+  int engine;
+  uint32_t* sched;
 } qsa_gather_desc;
 
 qkv_status qsa_gather_attn_ex(const qsa_gather_desc* desc, void* stream);

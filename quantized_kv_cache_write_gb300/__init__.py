@@ -22,6 +22,8 @@ QKV_OK, QKV_ERR_ARG, QKV_ERR_SCALE, QKV_ERR_UNSUPPORTED, QKV_ERR_ALIGN, QKV_ERR_
 QKV_BF16, QKV_INT8_SIDE, QKV_INT8_INLINE, QKV_E4M3, QKV_F16 = range(5)
 QKV_DEV_BAD_SLOT = 1
 QKV_DEV_BAD_INDEX = 2
+QKV_DEV_TIMEOUT = 4
+QSA_ENGINE_DEFAULT, QSA_ENGINE_TCGEN05, QSA_ENGINE_PERSISTENT = 0, 1, 2
 HEAD_DIM = 256
 FORMATS = {"bf16": QKV_BF16, "int8_side": QKV_INT8_SIDE, "int8_inline": QKV_INT8_INLINE, "e4m3": QKV_E4M3,
            "f16": QKV_F16}
@@ -72,7 +74,8 @@ class GatherDesc(ctypes.Structure):
                 ("num_slots", _i64), ("topk_idx", _p), ("topk", _i32), ("softmax_scale", _f32),
                 ("num_splits", _i32), ("out", _p), ("lse", _p), ("o_part", _p), ("lse_part", _p),
                 ("dev_status", _p), ("topk_len", _p), ("block_table", _p), ("num_seqs", _i64),
-                ("max_blocks", _i32), ("block_size", _i32), ("row_seq", _p), ("counters", _p)]
+                ("max_blocks", _i32), ("block_size", _i32), ("row_seq", _p), ("counters", _p),
+                ("engine", _i32), ("sched", _p)]
 
 
 lib.qsa_gather_attn_ex.argtypes = [ctypes.POINTER(GatherDesc), _p]
@@ -332,12 +335,16 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
                        num_slots: Optional[int] = None, k_scale_tok=None, v_scale_tok=None,
                        k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, num_splits: int = 1, out=None,
                        lse=None, o_part=None, lse_part=None, dev_status=None, topk_len=None, block_table=None,
-                       row_seq=None, block_size: int = 0, counters=None, stream=None):
+                       row_seq=None, block_size: int = 0, counters=None, engine: int = 0, sched=None,
+                       stream=None):
     """Any combination of the gather's options in one call (see qsa_gather_attn_ex in qkv.h).
 
     q bf16 or fp16 [R, Hq, D]; topk_len int32 [R] (varlen); block_table int32 [num_seqs,
     max_blocks] with row_seq int32 [R] and block_size (paged: topk_idx holds positions);
-    counters [R, Hkv, ceil(G / 16)] (fused split-K merge into out / lse).
+    counters [R, Hkv, ceil(G / 16)] (fused split-K merge into out / lse); engine
+    QSA_ENGINE_TCGEN05 selects the tensor-memory q.K^T variant of the int8 side gather;
+    QSA_ENGINE_PERSISTENT runs on a resident grid that takes work items from sched (int32 or
+    uint32 [2], zero on the first call and left zero).
     """
     _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
     R, Hq, D = q.shape
@@ -348,6 +355,9 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
     if counters is not None and counters.numel() != R * num_kv_heads * ((Hq // num_kv_heads + 15) // 16):
         raise ValueError("counters must hold rows x num_kv_heads x ceil(G / 16) entries")
     _check_gather_aux(k_scale_tok, v_scale_tok, dev_status, counters, row_seq, block_table, topk_len, R)
+    _need("sched", sched, _WORD, None if sched is None else 2)
+    if sched is not None and sched.device != q.device:
+        raise ValueError("sched must be on the query's device")
     d = GatherDesc()
     d.size = ctypes.sizeof(GatherDesc)
     d.q, d.q_fp16, d.rows, d.num_q_heads, d.num_kv_heads, d.head_dim = _ptr(q), int(q.dtype == torch.float16), R, Hq, \
@@ -360,7 +370,7 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
         num_splits
     d.out, d.lse, d.o_part, d.lse_part, d.dev_status = _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), \
         _ptr(dev_status)
-    d.topk_len, d.counters = _ptr(topk_len), _ptr(counters)
+    d.topk_len, d.counters, d.engine, d.sched = _ptr(topk_len), _ptr(counters), int(engine), _ptr(sched)
     if block_table is not None:
         d.block_table, d.num_seqs, d.max_blocks, d.block_size = _ptr(block_table), block_table.shape[0], \
             block_table.shape[1], int(block_size)

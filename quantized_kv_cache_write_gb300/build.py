@@ -32,6 +32,7 @@ SOURCES = [
     "gather_e4m3.cu",
     "gather_bf16.cu",
     "gather_noalloc.cu",
+    "gather_umma_int8_side.cu",
     "gather_paged_int8_side.cu",
     "gather_paged_int8_inline.cu",
     "gather_paged_e4m3.cu",
@@ -41,7 +42,7 @@ SOURCES = [
     "gather_f16q_e4m3.cu",
     "gather_f16q_f16.cu",
 ]
-HEADERS = ["qkv_internal.cuh", "gather_attn.cuh"]
+HEADERS = ["qkv_internal.cuh", "gather_attn.cuh", "gather_umma.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -259,18 +259,32 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   const int c = lane & 3, hn = lane >> 2;
   const int h0 = hn, h1 = hn + 8;
   const int P = a.num_splits, H = a.num_kv_heads, Hq = a.num_q_heads, G = Hq / H;
-  // a GQA group above 16 query heads runs as chunks of 16, one CTA each (adjacent in launch
+  // a GQA group above 16 query heads runs as chunks of 16, one item each (adjacent in launch
   // order, so a chunk's second gather of the same slots mostly hits L2)
   const int QC = (G + kHeadsPerCta - 1) / kHeadsPerCta;
-  const int64_t bid = blockIdx.x;
+  float* sFac = reinterpret_cast<float*>(smem + L::kFac);
+  uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
+  const uint32_t sQ = smem_u32(smem + L::kQ);
+  uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kTmem);
+  volatile uint32_t* sItem = reinterpret_cast<volatile uint32_t*>(smem + L::kTmem + 4);
+  if (warp == 0) {
+    tmem_alloc(smem_u32(sTmem), GM::kTmemAlloc);
+    tmem_relinquish_alloc_permit();
+  }
+  // Work items (row, KV head, head chunk, split), split fastest. One CTA per item, or (a.sched
+  // set) a resident grid whose CTAs take item blockIdx.x first and then pull the next free one
+  // from the counter a.sched[0] until none is left -- no CTA ever waits for another.
+  const int64_t num_items = a.rows * H * QC * P;
+  int64_t bid = blockIdx.x;
+  for (;;) {
   const int split = static_cast<int>(bid % P);
   const int64_t unit = bid / P;  // (row, KV head, head chunk): the fused merge's counter index
   const int qc = static_cast<int>(unit % QC);
   const int64_t rh = unit / QC;
   const int h = static_cast<int>(rh % H);
   const int64_t r = rh / H;
-  const int hq0 = h * G + kHeadsPerCta * qc;            // first query head of this CTA
-  const int Gc = min(kHeadsPerCta, G - kHeadsPerCta * qc);  // query heads of this CTA (1..16)
+  const int hq0 = h * G + kHeadsPerCta * qc;            // first query head of this item
+  const int Gc = min(kHeadsPerCta, G - kHeadsPerCta * qc);  // query heads of this item (1..16)
   // the split partition is over the full width topk; a row with a valid length (varlen) ends
   // there, and its columns past it are never read
   int len = a.topk;
@@ -283,14 +297,6 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   const int per_split = (a.topk + P - 1) / P;
   const int col0 = min(len, split * per_split);
   const int col1 = min(len, split * per_split + per_split);
-  float* sFac = reinterpret_cast<float*>(smem + L::kFac);
-  uint8_t* ring = smem + L::kRing + warp * L::kWarpRing;
-  const uint32_t sQ = smem_u32(smem + L::kQ);
-  uint32_t* sTmem = reinterpret_cast<uint32_t*>(smem + L::kTmem);
-  if (warp == 0) {
-    tmem_alloc(smem_u32(sTmem), GM::kTmemAlloc);
-    tmem_relinquish_alloc_permit();
-  }
 
   // ---------------- this warp's tiles: split tiles warp, warp + 4, ... (an empty pool has
   // no valid index: every row is empty)
@@ -1002,7 +1008,7 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     __syncwarp();
   }
 
-  // ---------------- merge the four warps' partial results, one 128-dim half at a time
+  // ---------------- merge the warps' partial results, one 128-dim half at a time
   cp_async_wait<0>();
 #pragma unroll
   for (int off = 1; off <= 2; off <<= 1) {
@@ -1157,6 +1163,26 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
       if (tid == 0) a.counters[unit] = 0u;  // every split has arrived: ready for the next call
     }
   }
+  if (a.sched == nullptr) break;
+  // next item: the query, the rings, the merge buffer and the accumulators are rewritten, so
+  // every thread is past this one first
+  tmem_fence_before_sync();
+  __syncthreads();
+  if (tid == 0) *sItem = gridDim.x + atomicAdd(a.sched, 1u);
+  __syncthreads();
+  tmem_fence_after_sync();
+  bid = *sItem;
+  if (bid >= num_items) break;
+  }  // items
+  if (a.sched != nullptr && tid == 0) {
+    // the CTA that finishes last (every CTA has taken its last item by then) leaves the
+    // counters zero for the next launch
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.sched, 0u);
+      atomicExch(a.sched + 1, 0u);
+    }
+  }
   // every warp's TMEM accesses are complete (the loads above were waited for): free the columns
   tmem_fence_before_sync();
   __syncthreads();
@@ -1194,13 +1220,61 @@ cudaError_t prepare_variant() {
   return cudaSuccess;
 }
 
+// CTAs of a variant that one SM holds at once: the smaller of its shared-memory and register
+// limits (registers allocated per warp in units of 256).
+template <int FMT, bool PAGED, int STAGES, int MINB, bool QF16, int HD>
+cudaError_t variant_ctas_per_sm(int* n) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>);
+  if (e != cudaSuccess) return e;
+  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess) return e;
+  const size_t per_cta = Smem<FMT, HD, STAGES>::kTotal + fa.sharedSizeBytes + static_cast<size_t>(reserved);
+  const int by_smem = static_cast<int>(static_cast<size_t>(smem_sm) / per_cta);
+  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
+  const int by_regs = regs_warp > 0 ? regs_sm / (regs_warp * Fmt<FMT>::kWarps) : by_smem;
+  *n = by_smem < by_regs ? by_smem : by_regs;
+  return cudaSuccess;
+}
+
+// CTAs of the variant that stay resident on the whole device (the persistent grid), once per
+// device.
+template <int FMT, bool PAGED, int STAGES, int MINB, bool QF16, int HD>
+cudaError_t resident_ctas(int64_t* out) {
+  static std::atomic<int64_t> cached[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int64_t n = cached[dev].load(std::memory_order_acquire);
+  if (n == 0) {
+    int per_sm = 0, sms = 0;
+    if ((e = variant_ctas_per_sm<FMT, PAGED, STAGES, MINB, QF16, HD>(&per_sm)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    n = static_cast<int64_t>(per_sm > 0 ? per_sm : 1) * sms;
+    cached[dev].store(n, std::memory_order_release);
+  }
+  *out = n;
+  return cudaSuccess;
+}
+
 template <int FMT, bool PAGED, int STAGES = Fmt<FMT>::kStages, int MINB = Fmt<FMT>::kMinBlocks,
           bool QF16 = false, int HD = 256>
 cudaError_t launch_variant(const GatherArgs& a, cudaStream_t stream) {
   cudaError_t e = prepare_variant<FMT, PAGED, STAGES, MINB, QF16, HD>();
   if (e != cudaSuccess) return e;
+  int64_t grid = gather_grid(a);
+  if (a.sched != nullptr) {
+    int64_t resident = 0;
+    e = resident_ctas<FMT, PAGED, STAGES, MINB, QF16, HD>(&resident);
+    if (e != cudaSuccess) return e;
+    grid = grid < resident ? grid : resident;
+  }
   gather_attn_kernel<FMT, PAGED, STAGES, MINB, QF16, HD>
-      <<<static_cast<unsigned>(gather_grid(a)), 32 * Fmt<FMT>::kWarps, Smem<FMT, HD, STAGES>::kTotal, stream>>>(a);
+      <<<static_cast<unsigned>(grid), 32 * Fmt<FMT>::kWarps, Smem<FMT, HD, STAGES>::kTotal, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -1218,25 +1292,11 @@ cudaError_t launch_f16q(const GatherArgs& a, cudaStream_t stream) {
   return launch_hd<FMT, false, true>(a, stream);
 }
 
-// CTAs of the default kernel of this layout that one SM holds at once: the smaller of its
-// shared-memory and register limits (allocated per warp in units of 256 registers).
+// CTAs of the default kernel of this layout that one SM holds at once.
 template <int FMT>
 cudaError_t resident_ctas_per_sm(int* n) {
   constexpr int S = Fmt<FMT>::kStages, B = Fmt<FMT>::kMinBlocks;
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, gather_attn_kernel<FMT, false, S, B>);
-  if (e != cudaSuccess) return e;
-  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess) return e;
-  const size_t per_cta = Smem<FMT, 256, S>::kTotal + fa.sharedSizeBytes + static_cast<size_t>(reserved);
-  const int by_smem = static_cast<int>(static_cast<size_t>(smem_sm) / per_cta);
-  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;
-  const int by_regs = regs_warp > 0 ? regs_sm / (regs_warp * Fmt<FMT>::kWarps) : by_smem;
-  *n = by_smem < by_regs ? by_smem : by_regs;
-  return cudaSuccess;
+  return variant_ctas_per_sm<FMT, false, S, B, false, 256>(n);
 }
 
 template <int FMT, bool PAGED = false>

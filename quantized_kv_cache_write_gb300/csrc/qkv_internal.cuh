@@ -81,6 +81,9 @@ struct GatherArgs {
   int64_t num_seqs = 0;
   int max_blocks = 0;
   int block_size = 0;
+  // persistent grid: [2] counters (next item, CTAs finished), zero on entry and left zero; the
+  // launch then sizes its grid to the CTAs that stay resident. Null = one CTA per item.
+  uint32_t* sched = nullptr;
 };
 
 cudaError_t launch_gather_bf16(const GatherArgs& a, cudaStream_t stream);
@@ -95,6 +98,9 @@ cudaError_t launch_gather_f16q_int8_side(const GatherArgs& a, cudaStream_t strea
 cudaError_t launch_gather_f16q_int8_inline(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_f16q_e4m3(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_gather_f16q_f16(const GatherArgs& a, cudaStream_t stream);
+// tensor-core (tcgen05) gather: persistent, one CTA per SM; int8 side scales, head dim 256,
+// GQA group <= 16, slot ids, bf16 query
+cudaError_t launch_umma_int8_side(const GatherArgs& a, cudaStream_t stream);
 cudaError_t gather_ctas_per_sm_bf16(int* n);
 cudaError_t gather_ctas_per_sm_int8_side(int* n);
 cudaError_t gather_ctas_per_sm_int8_inline(int* n);

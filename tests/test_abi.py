@@ -343,6 +343,41 @@ def test_gather_ex_host_validation(lib):
     assert L.qsa_gather_attn_ex(None, None) == E.QKV_ERR_ARG
 
 
+def test_gather_ex_engine_selection_host_validation(lib):
+    """The tensor-memory engine serves only the int8 side pool, head_dim 256, G <= 16, a bf16
+    query, unpaged and unfused; everything else is refused before any launch."""
+    import ctypes
+    E, L = lib, lib.lib
+
+    def desc(**kw):
+        d = lib.GatherDesc()
+        d.size = ctypes.sizeof(d)
+        d.q, d.rows, d.num_q_heads, d.num_kv_heads, d.head_dim, d.fmt = FAKE, 4, 16, 1, 256, E.QKV_INT8_SIDE
+        d.k_cache = d.v_cache = d.k_scale_tok = d.v_scale_tok = d.topk_idx = d.out = FAKE
+        d.num_slots, d.topk, d.softmax_scale, d.num_splits = 100, 8, 0.0625, 1
+        d.k_scale_layer = d.v_scale_layer = 1.0
+        d.engine = E.QSA_ENGINE_TCGEN05
+        for k, v in kw.items():
+            setattr(d, k, v)
+        return L.qsa_gather_attn_ex(ctypes.byref(d), None)
+
+    assert desc(engine=2) == E.QKV_ERR_ARG
+    assert desc(engine=-1) == E.QKV_ERR_ARG
+    assert desc(fmt=E.QKV_E4M3, k_scale_tok=None, v_scale_tok=None) == E.QKV_ERR_UNSUPPORTED
+    assert desc(fmt=E.QKV_BF16, k_scale_tok=None, v_scale_tok=None) == E.QKV_ERR_UNSUPPORTED
+    assert desc(head_dim=128) == E.QKV_ERR_UNSUPPORTED
+    assert desc(num_q_heads=32) == E.QKV_ERR_UNSUPPORTED  # G = 32
+    assert desc(q_fp16=1) == E.QKV_ERR_UNSUPPORTED
+    assert desc(block_table=FAKE, row_seq=FAKE, num_seqs=2, max_blocks=8, block_size=16) == E.QKV_ERR_UNSUPPORTED
+    assert desc(num_splits=2, o_part=FAKE, lse_part=FAKE, counters=FAKE) == E.QKV_ERR_UNSUPPORTED
+    assert desc(rows=0) == E.QKV_OK  # nothing to do: no launch
+    # the persistent grid needs its scheduling counter: present and 4-byte aligned
+    P = E.QSA_ENGINE_PERSISTENT
+    assert desc(engine=P, sched=None) == E.QKV_ERR_ARG
+    assert desc(engine=P, sched=FAKE + 2) == E.QKV_ERR_ALIGN
+    assert desc(engine=P, sched=None, rows=0) == E.QKV_OK
+
+
 def test_write_desc_layout_matches_the_header(lib, tmp_path):
     """The binding's ctypes mirror of qkv_write_desc has the C compiler's field offsets."""
     import ctypes

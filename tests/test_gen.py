@@ -61,3 +61,34 @@ def test_small_random_padding_and_zero_tokens():
     assert set(valid.tolist()) <= set(wl.slot_mapping.tolist())
     # zero factor keeps the sign of negative draws: -0.0 is a zero too
     assert np.sum(np.all((wl.k_tokens & 0x7FFF) == 0, axis=(1, 2))) == 3
+
+
+def test_mixed_catchup_decode_rows():
+    from gen import mixed_catchup_decode
+    wl = mixed_catchup_decode(6)
+    assert wl.rows == 49 and wl.topk.shape == (49, 2051)
+    lens = wl.row_len
+    assert lens[:46].tolist() == list(range(64, 110)) and lens[46:].tolist() == [2051] * 3
+    for r in range(49):
+        row = wl.topk[r]
+        assert np.all(row[lens[r]:] == -1) and np.all(row[:lens[r]] >= 0)
+        assert np.unique(row[:lens[r]]).size == lens[r]
+    # a catch-up row attends exactly the request's earlier positions: row i's slots are those
+    # of positions 0 .. 63 + i, so each row's set contains the previous row's
+    cu = [set(wl.topk[i, :lens[i]].tolist()) for i in range(46)]
+    assert cu[0] == set(wl.slot_mapping[:64].tolist())
+    assert all(cu[i] < cu[i + 1] for i in range(45))
+    # the decode rows draw from their own requests only (disjoint slot ranges of the pool)
+    dec = [set(wl.topk[46 + j].tolist()) for j in range(3)]
+    assert not (dec[0] & dec[1]) and not (dec[1] & dec[2]) and not (dec[0] & cu[-1])
+
+
+def test_bulk_tail_decode_rows():
+    from gen import bulk_tail_decode
+    wl = bulk_tail_decode(7)
+    assert wl.rows == 61 and np.all(wl.row_len[:48] == 2051)
+    assert wl.row_len[48] == 1 and wl.row_len[49] == 2051 and np.all((wl.row_len >= 1) & (wl.row_len <= 2051))
+    for r in range(61):
+        row = wl.topk[r]
+        assert np.all(row[wl.row_len[r]:] == -1) and np.unique(row[:wl.row_len[r]]).size == wl.row_len[r]
+        assert row[:wl.row_len[r]].max() < wl.num_slots
