@@ -85,32 +85,36 @@ constexpr int kEuHeadroom = 2;  // int8: the V-scale bound 2^eu is raised 2^2 pa
 // is then formed relative to a reference with fused multiply-adds (see the softmax below), which
 // keeps the dot product's precision where it matters: a row whose output is a near cancellation
 // of two outlier keys with opposite values needs more than a rounded fp32 logit. The second
-// staged query does not fit three CTAs of four warps on an SM; two CTAs of five warps do.
+// staged query leaves no room for two full K + V stages per warp at three CTAs of four warps
+// per SM; kSplitRing rotates three half-stage slots instead (see Smem).
+// kSide: the scales sit in a per-stage scale area of shared memory; kInline: the pool holds
+// (HD + 4)-byte records, codes then the fp32 scale, which the copies realign into exactly the
+// side layout's shared memory -- from there on both int8 layouts run the same arithmetic.
 template <int FMT>
 struct Fmt;
 template <>
 struct Fmt<QKV_INT8_SIDE> {
-  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 64, kWarps = 5;
+  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64, kWarps = 4;
   static constexpr bool kInt8 = true, kSide = true, kInline = false, kE4m3 = false, kBf16 = false, kNatural = true;
-  static constexpr bool kWide = false, kF16 = false, kQSplit = true;
+  static constexpr bool kWide = false, kF16 = false, kQSplit = true, kSplitRing = true;
 };
 template <>
 struct Fmt<QKV_INT8_INLINE> {
-  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 16, kWarps = 5;
-  static constexpr bool kInt8 = true, kSide = false, kInline = true, kE4m3 = false, kBf16 = false, kNatural = false;
-  static constexpr bool kWide = false, kF16 = false, kQSplit = true;
+  static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64, kWarps = 4;
+  static constexpr bool kInt8 = true, kSide = true, kInline = true, kE4m3 = false, kBf16 = false, kNatural = true;
+  static constexpr bool kWide = false, kF16 = false, kQSplit = true, kSplitRing = true;
 };
 template <>
 struct Fmt<QKV_E4M3> {
   static constexpr int kStages = 2, kMinBlocks = 3, kKShift = 64, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = true, kBf16 = false, kNatural = true;
-  static constexpr bool kWide = false, kF16 = false, kQSplit = false;
+  static constexpr bool kWide = false, kF16 = false, kQSplit = false, kSplitRing = false;
 };
 template <>
 struct Fmt<QKV_BF16> {
   static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true, kNatural = false;
-  static constexpr bool kWide = true, kF16 = false, kQSplit = false;
+  static constexpr bool kWide = true, kF16 = false, kQSplit = false, kSplitRing = false;
 };
 // fp16 pool: the unquantised cache of the FP16-activation contract; moved like bf16 rows,
 // multiplied as fp16 (q must be fp16 too)
@@ -118,19 +122,18 @@ template <>
 struct Fmt<QKV_F16> {
   static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = false, kNatural = false;
-  static constexpr bool kWide = true, kF16 = true, kQSplit = false;
+  static constexpr bool kWide = true, kF16 = true, kQSplit = false, kSplitRing = false;
 };
 
 // Head-dim dependent sizes (HD = 128 or 256).
-//   kRowBytes   one K (or V) row in shared memory; the inline layout keeps the HD + 16 bytes of
-//               aligned 16 B chunks that cover any (HD + 4)-byte record on a 4 B boundary
+//   kRowBytes   one K (or V) row in shared memory (an inline record's codes, realigned)
 //   kGlobalRow  bytes of one record in the pool
 //   kBlocks     64-dim blocks of q.K^T; kSweeps: 128-dim sweeps of p.V and of the final merge
 //   kTmemCols   fp32 accumulator columns per TMEM lane (16 heads x HD dims over 32 lanes)
 template <int FMT, int HD>
 struct Geom {
   static_assert(HD == 128 || HD == 256, "head_dim 128 or 256");
-  static constexpr int kRowBytes = Fmt<FMT>::kInline ? HD + 16 : (Fmt<FMT>::kWide ? 2 * HD : HD);
+  static constexpr int kRowBytes = Fmt<FMT>::kWide ? 2 * HD : HD;
   static constexpr int kGlobalRow = Fmt<FMT>::kInline ? HD + 4 : (Fmt<FMT>::kWide ? 2 * HD : HD);
   static constexpr int kBlocks = HD / 64, kSweeps = HD / 128, kTmemCols = HD / 2;
   // columns allocated per CTA: warp w uses lanes 32 (w % 4) of columns kTmemCols (w / 4) ..
@@ -166,13 +169,18 @@ struct Smem {
   static constexpr size_t kVArea = 8 * kVRegion + v_region_shift<FMT>(7);
   static constexpr size_t kStageK = 0;
   static constexpr size_t kStageV = kKArea;
-  static constexpr size_t kStageKs = kStageV + kVArea;
-  static constexpr size_t kStageMeta = kStageKs + (F::kSide ? 2 * kKeys * 4 : 0);
+  // split ring (kSplitRing): each warp rotates three slots, each holding one tile's K rows or
+  // its V rows, so a tile's K and V need not share a stage; the int8 scales of both tensors
+  // travel with K
+  static constexpr size_t kSlotRows = kKArea > kVArea ? kKArea : kVArea;
+  static constexpr size_t kStageKs = F::kSplitRing ? kSlotRows : kStageV + kVArea;
   // deeper rings keep each stage's valid-key mask here (a two-stage ring keeps it in registers)
-  static constexpr size_t kStageMask = (kStageMeta + (F::kInline ? kKeys : 0) + 3) / 4 * 4;
-  static constexpr size_t kStageBytes = ((kStageMask + (STAGES > 2 ? 4 : 0)) + 15) / 16 * 16;
-  static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][STAGES] stages
-  static constexpr size_t kWarpRing = size_t(STAGES) * kStageBytes;
+  static constexpr size_t kStageMask = (kStageKs + (F::kSide ? 2 * kKeys * 4 : 0) + 3) / 4 * 4;
+  static constexpr size_t kStageBytes =
+      ((kStageMask + (STAGES > 2 && !F::kSplitRing ? 4 : 0)) + 15) / 16 * 16;  // a stage, or a slot
+  static constexpr int kSlots = F::kSplitRing ? 3 : STAGES;
+  static constexpr size_t kRing = kFac + 16 * 4;  // [kWarps][kSlots] stages or slots
+  static constexpr size_t kWarpRing = size_t(kSlots) * kStageBytes;
   // final merge buffer [kWarps][16][merge_row] floats, reusing the rings (which it may outgrow
   // for small rows)
   static constexpr size_t kMergeBytes = size_t(kWarps) * 16 * merge_row<FMT>() * 4;
@@ -369,16 +377,10 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   const uint32_t dk_l = F::kInline ? 0u : k_row_off<FMT, HD>(key_sub) + 16 * chunk_sub;
   const uint32_t dv_l = F::kInline ? 0u : v_row_off<FMT, HD>(key_sub) - L::kStageV + 16 * chunk_sub;
 
-  // Copy one 16-key tile into ring stage i % STAGES; returns the tile's valid-key mask (a
-  // two-stage ring carries it one tile ahead in a register, a deeper one in the stage).
-  auto issue = [&](int i, int idxv) -> uint32_t {  // idxv: this lane's checked slot (or -1)
-    const int st = i % STAGES;
-    const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
-    uint8_t* sb = ring + size_t(st) * L::kStageBytes;
-    const uint32_t sbase = smem_u32(sb);
-    if (STAGES > 2 && lane == 0) sts32(sbase + L::kStageMask, mask);
-    // record number (slot * H + h; the host keeps it below 2^31) of key `lane`, -1 = padding
-    const int rec_l = idxv >= 0 ? idxv * H + h : -1;
+  // Copies of one 16-key tile. rec_l: record number (slot * H + h; the host keeps it below
+  // 2^31) of key `lane`, -1 = padding. K rows go to kdst + k_row_off(r), with the int8 scales
+  // of both tensors at kdst + kStageKs; V rows go to vdst + v_row_off(r).
+  auto copy_tile = [&](bool do_k, bool do_v, uint32_t kdst, uint32_t vdst, int rec_l) {
     if (!F::kInline) {
 #pragma unroll
       for (int t = 0; t < kKeys / kKpi; ++t) {
@@ -394,49 +396,53 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
         const uint32_t tk = k_row_off<FMT, HD>(kKpi * t), tv = v_row_off<FMT, HD>(kKpi * t);
 #pragma unroll
         for (int u = 0; u < kHs; ++u) {
-          cp_async16(sbase + dk_l + tk + 128 * u, kb_l + off + 128 * u, nb);
-          cp_async16(sbase + dv_l + tv + 128 * u, vb_l + off + 128 * u, nb);
+          if (do_k) cp_async16(kdst + dk_l + tk + 128 * u, kb_l + off + 128 * u, nb);
+          if (do_v) cp_async16(vdst + dv_l + tv + 128 * u, vb_l + off + 128 * u, nb);
         }
       }
     } else {
-      // 16 B copies: consecutive lanes take consecutive chunks of a row (whole lines)
-      constexpr int kChunks = GM::kRowBytes / 16;  // inline: HD / 16 + 1
-      constexpr int kTotalCopies = kKeys * kChunks;
-      constexpr int kIters = (kTotalCopies + 31) / 32;
+      // inline records sit on 4 B boundaries only (HD + 4 bytes apart): 4 B copies, lane l taking
+      // words l, l + 32, .. of each record's codes, land them 16 B-aligned in the side layout
 #pragma unroll
-      for (int t = 0; t < kIters; ++t) {
-        const int e = lane + 32 * t;
-        const bool act = e < kTotalCopies;
-        const int key = act ? e / kChunks : 0;
-        const int jj = e - key * kChunks;
-        int slot = __shfl_sync(0xffffffffu, idxv, key);
-        const bool valid = slot >= 0;
-        slot = valid ? slot : 0;
-        const int64_t rec = static_cast<int64_t>(slot) * H + h;
-        if (act) {
-          const uint32_t dK = sbase + k_row_off<FMT, HD>(key) + jj * 16;
-          const uint32_t dV = sbase + v_row_off<FMT, HD>(key) + jj * 16;
-          if (F::kInline) {
-            const int64_t off = rec * GM::kGlobalRow;
-            const int64_t al = off & ~int64_t(15);
-            const int delta = static_cast<int>(off - al);
-            // the 17th chunk copies only the record's own bytes (never past the pool's end)
-            const int nb = valid ? (jj == kChunks - 1 ? delta + 4 : 16) : 0;
-            cp_async16(dK, a.k_cache + al + jj * 16, nb);
-            cp_async16(dV, a.v_cache + al + jj * 16, nb);
-            if (jj == 0) sb[L::kStageMeta + key] = static_cast<uint8_t>(delta);  // where the record starts
-          }
+      for (int r = 0; r < kKeys; ++r) {
+        const int rec = __shfl_sync(0xffffffffu, rec_l, r);
+        const int nb = rec >= 0 ? 4 : 0;
+        const uint64_t off = static_cast<uint64_t>(static_cast<uint32_t>(max(rec, 0))) * GM::kGlobalRow + 4 * lane;
+#pragma unroll
+        for (int u = 0; u < HD / 128; ++u) {
+          if (do_k) cp_async4(kdst + k_row_off<FMT, HD>(r) + 4 * lane + 128 * u, a.k_cache + off + 128 * u, nb);
+          if (do_v) cp_async4(vdst + v_row_off<FMT, HD>(r) + 4 * lane + 128 * u, a.v_cache + off + 128 * u, nb);
         }
       }
     }
-    if (F::kSide) {
-      // lanes 0-15: K scales of the 16 keys; lanes 16-31: V scales (zero for padding)
+    if (F::kSide && do_k) {
+      // lanes 0-15: K scales of the 16 keys; lanes 16-31: V scales (zero for padding), from the
+      // side tensors or from the records' last 4 bytes
       const int rec = __shfl_sync(0xffffffffu, rec_l, lane & 15);
-      const float* gs = (lane >> 4) ? a.v_scale_tok : a.k_scale_tok;
-      cp_async4(sbase + L::kStageKs + lane * 4, gs + max(rec, 0), rec >= 0 ? 4 : 0);
+      const void* src;
+      if (F::kInline) {
+        src = ((lane >> 4) ? a.v_cache : a.k_cache) +
+              static_cast<uint64_t>(static_cast<uint32_t>(max(rec, 0))) * GM::kGlobalRow + HD;
+      } else {
+        src = ((lane >> 4) ? a.v_scale_tok : a.k_scale_tok) + max(rec, 0);
+      }
+      cp_async4(kdst + L::kStageKs + lane * 4, src, rec >= 0 ? 4 : 0);
     }
+  };
+  auto rec_of = [&](int idxv) -> int { return idxv >= 0 ? idxv * H + h : -1; };
+  // Copy one 16-key tile, K and V, into ring stage i % STAGES; returns the tile's valid-key
+  // mask (a two-stage ring carries it one tile ahead in a register, a deeper one in the stage).
+  auto issue = [&](int i, int idxv) -> uint32_t {  // idxv: this lane's checked slot (or -1)
+    const int st = i % STAGES;
+    const uint32_t mask = __ballot_sync(0xffffffffu, idxv >= 0) & 0xFFFFu;
+    const uint32_t sbase = smem_u32(ring + size_t(st) * L::kStageBytes);
+    if (STAGES > 2 && lane == 0) sts32(sbase + L::kStageMask, mask);
+    copy_tile(true, true, sbase, sbase, rec_of(idxv));
     return mask;
   };
+  // split ring: slot j of this warp (tile i's K in slot 2i mod 3, its V in slot 2i + 1 mod 3)
+  const uint32_t ring_u32 = smem_u32(ring);
+  auto slot_addr = [&](int j) -> uint32_t { return ring_u32 + static_cast<uint32_t>(j % 3) * L::kStageBytes; };
 
   // The query's global loads go out first, then the first tiles' index loads and copies: the
   // copies wait for their indices, and the query's latency overlaps both.
@@ -461,7 +467,35 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   // STAGES - 1's entry for the first loop iteration.
   int nidx, nblk = -1, ppos = -1;
   uint32_t mask_cur = 0;  // two-stage ring: valid keys of the tile being computed (bit k = key k)
-  {
+  // split ring: tile i + 1's mask and records (its V rows are issued during tile i)
+  uint32_t mask_n1 = 0;
+  int rec_n1 = -1;
+  if (F::kSplitRing) {
+    // K of tile 0, V of tile 0, K of tile 1: one commit group each
+    const int e0 = load_idx(0), e1 = load_idx(1);
+    nidx = load_idx(2);
+    int c0, c1;
+    if (PAGED) {
+      ppos = load_idx(3);
+      const int b0 = lookup(e0), b1 = lookup(e1);
+      nblk = lookup(nidx);
+      c0 = checked_paged(e0, b0);
+      c1 = checked_paged(e1, b1);
+    } else {
+      c0 = checked(e0);
+      c1 = checked(e1);
+    }
+    const int r0 = rec_of(c0);
+    rec_n1 = rec_of(c1);
+    mask_cur = __ballot_sync(0xffffffffu, c0 >= 0) & 0xFFFFu;
+    mask_n1 = __ballot_sync(0xffffffffu, c1 >= 0) & 0xFFFFu;
+    if (my > 0) copy_tile(true, false, slot_addr(0), 0u, r0);
+    cp_async_commit();
+    if (my > 0) copy_tile(false, true, 0u, slot_addr(1) - static_cast<uint32_t>(L::kStageV), r0);
+    cp_async_commit();
+    if (my > 1) copy_tile(true, false, slot_addr(2), 0u, rec_n1);
+    cp_async_commit();
+  } else {
     int ent[STAGES - 1];
 #pragma unroll
     for (int t = 0; t < STAGES - 1; ++t) ent[t] = load_idx(t);
@@ -590,24 +624,32 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
   int eu = -100;                           // int8: 2^eu > every V scale seen
   for (int i = 0; i < my; ++i) {
-    const int inext = i + STAGES - 1;  // the tile issued now, into the stage freed last iteration
-    const uint32_t mask_next =
-        (inext < my) ? issue(inext, PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : 0u;
-    cp_async_commit();
-    if (PAGED) {
-      nidx = ppos;
-      nblk = lookup(ppos);
-      ppos = load_idx(i + STAGES + 1);
+    uint32_t mask_next = 0u;
+    if (!F::kSplitRing) {
+      const int inext = i + STAGES - 1;  // the tile issued now, into the stage freed last iteration
+      mask_next = (inext < my) ? issue(inext, PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : 0u;
+      cp_async_commit();
+      if (PAGED) {
+        nidx = ppos;
+        nblk = lookup(ppos);
+        ppos = load_idx(i + STAGES + 1);
+      } else {
+        nidx = load_idx(i + STAGES);
+      }
+      cp_async_wait<STAGES - 1>();
     } else {
-      nidx = load_idx(i + STAGES);
+      cp_async_wait<2>();  // K of tile i (V of tile i and K of tile i + 1 may be in flight)
     }
-    cp_async_wait<STAGES - 1>();
     const int st = i % STAGES;
     __syncwarp();
 
-    const uint8_t* sb = ring + size_t(st) * L::kStageBytes;
-    const uint32_t sbase = smem_u32(sb);
-    const uint32_t mask = (STAGES == 2) ? mask_cur : lds32(sbase + L::kStageMask);
+    // where this tile's K rows and scales (kslot) and V rows (vbase + v_row_off) are: one stage,
+    // or two slots of the split ring
+    const uint32_t sbase = smem_u32(ring + size_t(st) * L::kStageBytes);
+    const uint32_t kslot = F::kSplitRing ? slot_addr(2 * i) : sbase;
+    const uint32_t vslot = F::kSplitRing ? slot_addr(2 * i + 1) : sbase;
+    const uint32_t vbase = F::kSplitRing ? vslot - static_cast<uint32_t>(L::kStageV) : sbase;
+    const uint32_t mask = (STAGES == 2 || F::kSplitRing) ? mask_cur : lds32(sbase + L::kStageMask);
 
     // ---- q . K^T for this warp's 16 keys
     // kQkChains independent accumulator chains per N-tile (64-dim blocks dealt round-robin),
@@ -620,13 +662,8 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) accc[ch][nt][0] = accc[ch][nt][1] = accc[ch][nt][2] = accc[ch][nt][3] = 0.f;
     uint32_t rowK[2];
-    int delta_k[2] = {0, 0};  // inline: offset of each record inside its 272 B row
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int key = key_of<FMT>(nt, hn);
-      rowK[nt] = sbase + k_row_off<FMT, HD>(key);
-      if (F::kInline) delta_k[nt] = lds_u8(sbase + L::kStageMeta + key);
-    }
+    for (int nt = 0; nt < 2; ++nt) rowK[nt] = kslot + k_row_off<FMT, HD>(key_of<FMT>(nt, hn));
 #pragma unroll
     for (int blk = 0; blk < GM::kBlocks; ++blk) {
       uint32_t kw[2][8];
@@ -637,9 +674,6 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
           const uint4 y = lds128(rowK[nt] + (8 * blk + 2 * c + 1) * 16);
           kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
           kw[nt][4] = y.x; kw[nt][5] = y.y; kw[nt][6] = y.z; kw[nt][7] = y.w;
-        } else if (F::kInline) {
-          const uint32_t p = rowK[nt] + delta_k[nt] + 64 * blk + 16 * c;
-          kw[nt][0] = lds32(p); kw[nt][1] = lds32(p + 4); kw[nt][2] = lds32(p + 8); kw[nt][3] = lds32(p + 12);
         } else {
           const uint4 x = lds128(rowK[nt] + (4 * blk + c) * 16);
           kw[nt][0] = x.x; kw[nt][1] = x.y; kw[nt][2] = x.z; kw[nt][3] = x.w;
@@ -710,12 +744,7 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     if (F::kInt8) {
       uint32_t vb = 0;
       if (lane < kKeys) {
-        if (F::kSide) {
-          vb = lds32(sbase + L::kStageKs + (kKeys + lane) * 4);
-        } else {
-          const int dl = lds_u8(sbase + L::kStageMeta + lane);
-          vb = lds32(sbase + v_row_off<FMT, HD>(lane) + dl + HD);
-        }
+        vb = lds32(kslot + L::kStageKs + (kKeys + lane) * 4);
       }
       vmx_bits = __reduce_max_sync(0xffffffffu, vb & 0x7FFFFFFFu);
     }
@@ -732,12 +761,8 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
         valid2[e] = valid;
         float ksc = 1.f, vs = 0.f;
         if (F::kSide) {
-          ksc = __uint_as_float(lds32(sbase + L::kStageKs + kt * 4));
-          vs = __uint_as_float(lds32(sbase + L::kStageKs + (kKeys + kt) * 4));
-        } else if (F::kInline) {
-          const int dl = lds_u8(sbase + L::kStageMeta + kt);
-          ksc = __uint_as_float(lds32(sbase + k_row_off<FMT, HD>(kt) + dl + HD));
-          vs = __uint_as_float(lds32(sbase + v_row_off<FMT, HD>(kt) + dl + HD));
+          ksc = __uint_as_float(lds32(kslot + L::kStageKs + kt * 4));
+          vs = __uint_as_float(lds32(kslot + L::kStageKs + (kKeys + kt) * 4));
         }
         // (padding keys already carry a zero V scale: their scale copies zero-fill)
         vsc[nt][e] = vs;
@@ -764,6 +789,12 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     for (int off = 1; off <= 2; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    if (F::kSplitRing) {
+      // every lane is done with this tile's K slot: the V rows of tile i + 1 go there
+      __syncwarp();
+      if (i + 1 < my) copy_tile(false, true, 0u, kslot - static_cast<uint32_t>(L::kStageV), rec_n1);
+      cp_async_commit();
     }
 
     // ---- lazy rescale: raise the max in use only past the threshold
@@ -886,14 +917,14 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
       const int rows[4] = {key_of<FMT>(0, 2 * c), key_of<FMT>(0, 2 * c + 1), key_of<FMT>(1, 2 * c),
                            key_of<FMT>(1, 2 * c + 1)};
       uint32_t rowV[4];
-      int dv[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int ri = 0; ri < 4; ++ri) {
-        rowV[ri] = sbase + v_row_off<FMT, HD>(rows[ri]);
-        if (F::kInline) dv[ri] = lds_u8(sbase + L::kStageMeta + rows[ri]);
+      if (F::kSplitRing) {  // V of tile i (K of tile i + 1 and V of tile i + 1 may be in flight)
+        cp_async_wait<2>();
+        __syncwarp();
       }
+#pragma unroll
+      for (int ri = 0; ri < 4; ++ri) rowV[ri] = vbase + v_row_off<FMT, HD>(rows[ri]);
       // natural layouts: lane l addresses key row l % 16 of the 16 B column block l / 16 (+ 2 m)
-      const uint32_t vmat = sbase + v_row_off<FMT, HD>(lane & 15) + 16 * (lane >> 4);
+      const uint32_t vmat = vbase + v_row_off<FMT, HD>(lane & 15) + 16 * (lane >> 4);
 #pragma unroll
       for (int sw = 0; sw < GM::kSweeps; ++sw) {
         // accumulator quarters 2 sw (N-tiles 16 sw + 0..7) and 2 sw + 1 (16 sw + 8..15)
@@ -936,37 +967,6 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
             bb[tt][0] = __byte_perm(vw[0][tt >> 1], vw[1][tt >> 1], sel);
             bb[tt][1] = __byte_perm(vw[2][tt >> 1], vw[3][tt >> 1], sel);
           }
-        } else {
-          uint32_t vw[4][4];
-#pragma unroll
-          for (int ri = 0; ri < 4; ++ri) {
-            const uint32_t p = rowV[ri] + dv[ri] + 128 * sw + 16 * hn;
-            if (F::kInline) {
-              vw[ri][0] = lds32(p); vw[ri][1] = lds32(p + 4); vw[ri][2] = lds32(p + 8); vw[ri][3] = lds32(p + 12);
-            } else {
-              const uint4 x = lds128(p);
-              vw[ri][0] = x.x; vw[ri][1] = x.y; vw[ri][2] = x.z; vw[ri][3] = x.w;
-            }
-          }
-          if (F::kInt8) {
-#pragma unroll
-            for (int tt = 0; tt < 16; ++tt) {
-              const uint32_t sel = (tt & 3) | (((tt & 3) + 4) << 8);
-              bb[tt][0] = i8pair_to_f16x2(__byte_perm(vw[0][tt >> 2], vw[1][tt >> 2], sel));
-              bb[tt][1] = i8pair_to_f16x2(__byte_perm(vw[2][tt >> 2], vw[3][tt >> 2], sel));
-            }
-          } else {
-#pragma unroll
-            for (int t4 = 0; t4 < 8; ++t4) {  // [a_t, b_t, a_t+1, b_t+1] pairs, t = 2*t4
-              const uint32_t sel = (t4 & 1) ? 0x7362u : 0x5140u;
-              const uint32_t u = __byte_perm(vw[0][t4 >> 1], vw[1][t4 >> 1], sel);
-              const uint32_t w = __byte_perm(vw[2][t4 >> 1], vw[3][t4 >> 1], sel);
-              bb[2 * t4][0] = e4m3pair_to_f16x2(u);
-              bb[2 * t4][1] = e4m3pair_to_f16x2(w);
-              bb[2 * t4 + 1][0] = e4m3pair_to_f16x2(u >> 16);
-              bb[2 * t4 + 1][1] = e4m3pair_to_f16x2(w >> 16);
-            }
-          }
         }
         tmem_wait_ld(ob[0]);
         tmem_wait_ld(ob[1]);
@@ -1004,7 +1004,27 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
         tmem_st32(tacc + 64 * sw + 32, ob[1]);
       }
     }
-    if (STAGES == 2) mask_cur = mask_next;
+    if (F::kSplitRing) {
+      // every lane is done with this tile's V slot: the K rows of tile i + 2 go there
+      __syncwarp();
+      const int c2 = (i + 2 < my) ? (PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : -1;
+      const int r2 = rec_of(c2);
+      const uint32_t m2 = __ballot_sync(0xffffffffu, c2 >= 0) & 0xFFFFu;
+      if (i + 2 < my) copy_tile(true, false, vslot, 0u, r2);
+      cp_async_commit();
+      if (PAGED) {
+        nidx = ppos;
+        nblk = lookup(ppos);
+        ppos = load_idx(i + 4);
+      } else {
+        nidx = load_idx(i + 3);
+      }
+      mask_cur = mask_n1;
+      mask_n1 = m2;
+      rec_n1 = r2;
+    } else if (STAGES == 2) {
+      mask_cur = mask_next;
+    }
     __syncwarp();
   }
 

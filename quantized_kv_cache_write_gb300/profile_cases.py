@@ -20,6 +20,8 @@ flush (a 256 MiB write), and synchronises. Profile the last launch with
   mixed_<engine>     the 49-row catch-up/decode batch, E4M3, varlen, fused, 8 splits, engine =
                      default or persistent ("[Model][SM70][FP8] Add calibrated E4M3 QSA KV
                      cache", §Targeted mixed-batch scheduler regression)
+  chunked_prefill    8192 causal rows (row i attends min(1024, i) of the 8192 tokens just
+                     written into a 524288-slot int8 side pool), varlen
 """
 
 from __future__ import annotations
@@ -34,10 +36,11 @@ import torch
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 
 import quantized_kv_cache_write_gb300 as q  # noqa: E402
-from gen import e4m3_splitk_layer, long_context_decode, mixed_catchup_decode, page1_shape, small_random  # noqa: E402
+from gen import (chunked_prefill, e4m3_splitk_layer, long_context_decode, mixed_catchup_decode,  # noqa: E402
+                 page1_shape, small_random)
 
 CASES = ["page1_int8_side", "page1_int8_inline", "page1_e4m3", "page1_bf16", "page1_tcgen05", "page1_gqa32",
-         "e4m3_layer", "long_context", "mixed_default", "mixed_persistent"]
+         "e4m3_layer", "long_context", "mixed_default", "mixed_persistent", "chunked_prefill"]
 
 
 def _dev(bits):
@@ -119,6 +122,14 @@ def build(case: str):
                                             o_part=o_part, lse_part=lse_part, counters=counters, topk_len=lens,
                                             engine=engine, sched=sched if engine == q.QSA_ENGINE_PERSISTENT else None,
                                             **kw)
+    if case == "chunked_prefill":
+        wl = chunked_prefill(4)
+        kc, vc, kw = _pool(wl, "int8_side")
+        qd, idx = _dev(wl.q), torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
+        lens = torch.from_numpy(np.minimum(np.arange(wl.rows), wl.topk.shape[1]).astype(np.int32)).cuda()
+        out = torch.empty((wl.rows, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
+        return lambda: q.qsa_gather_attn_varlen(qd, q.QKV_INT8_SIDE, kc, vc, idx, lens, wl.softmax_scale, out=out,
+                                                **kw)
     raise SystemExit(f"unknown case {case!r}; one of {', '.join(CASES)}")
 
 
