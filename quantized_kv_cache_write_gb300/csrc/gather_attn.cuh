@@ -285,12 +285,15 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   const int64_t num_items = a.rows * H * QC * P;
   int64_t bid = blockIdx.x;
   for (;;) {
-  const int split = static_cast<int>(bid % P);
-  const int64_t unit = bid / P;  // (row, KV head, head chunk): the fused merge's counter index
-  const int qc = static_cast<int>(unit % QC);
-  const int64_t rh = unit / QC;
-  const int h = static_cast<int>(rh % H);
-  const int64_t r = rh / H;
+  // (the host keeps the item count below 2^31: 32-bit division, not the 64-bit routine)
+  const uint32_t ub = static_cast<uint32_t>(bid);
+  const int split = static_cast<int>(ub % static_cast<uint32_t>(P));
+  const uint32_t unit32 = ub / static_cast<uint32_t>(P);
+  const int64_t unit = unit32;  // (row, KV head, head chunk): the fused merge's counter index
+  const int qc = static_cast<int>(unit32 % static_cast<uint32_t>(QC));
+  const uint32_t rh = unit32 / static_cast<uint32_t>(QC);
+  const int h = static_cast<int>(rh % static_cast<uint32_t>(H));
+  const int64_t r = rh / static_cast<uint32_t>(H);
   const int hq0 = h * G + kHeadsPerCta * qc;            // first query head of this item
   const int Gc = min(kHeadsPerCta, G - kHeadsPerCta * qc);  // query heads of this item (1..16)
   // the split partition is over the full width topk; a row with a valid length (varlen) ends
