@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
       return false;
     };
     // barrier of the compute warps that also agrees on stopping (the flag may be set by another
-    // warp at any time, so each thread's reading is OR-ed into one verdict)
+    // warp at any time, so each thread's reading is OR-ed into one result)
     auto sync_go = [&](bool failed) -> bool { return !bar_compute_or(failed || *sFlag != 0u); };
 
     // query staging (thread (head qh, part) holds 16 dims, prefetched an item ahead)
