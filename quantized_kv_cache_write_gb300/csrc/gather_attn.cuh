@@ -112,17 +112,17 @@ struct Fmt<QKV_E4M3> {
 };
 template <>
 struct Fmt<QKV_BF16> {
-  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16, kWarps = 4;
+  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 16, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = true, kNatural = false;
-  static constexpr bool kWide = true, kF16 = false, kQSplit = false, kSplitRing = false;
+  static constexpr bool kWide = true, kF16 = false, kQSplit = false, kSplitRing = true;
 };
 // fp16 pool: the unquantised cache of the FP16-activation contract; moved like bf16 rows,
 // multiplied as fp16 (q must be fp16 too)
 template <>
 struct Fmt<QKV_F16> {
-  static constexpr int kStages = 2, kMinBlocks = 1, kKShift = 16, kWarps = 4;
+  static constexpr int kStages = 2, kMinBlocks = 2, kKShift = 16, kWarps = 4;
   static constexpr bool kInt8 = false, kSide = false, kInline = false, kE4m3 = false, kBf16 = false, kNatural = false;
-  static constexpr bool kWide = true, kF16 = true, kQSplit = false, kSplitRing = false;
+  static constexpr bool kWide = true, kF16 = true, kQSplit = false, kSplitRing = true;
 };
 
 // Head-dim dependent sizes (HD = 128 or 256).

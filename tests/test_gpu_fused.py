@@ -136,8 +136,8 @@ def test_long_context_decode_fused():
 def test_suggested_split_counts():
     import quantized_kv_cache_write_gb300 as q
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # occupancy 3, 3, 2, 1 CTAs per SM, capped at 2
-    for fmt, per_sm in (("int8_side", 2), ("e4m3", 2), ("int8_inline", 2), ("bf16", 1)):
+    # occupancy 3, 3, 3, 2 CTAs per SM (int8 side, E4M3, int8 inline, bf16), capped at 2
+    for fmt, per_sm in (("int8_side", 2), ("e4m3", 2), ("int8_inline", 2), ("bf16", 2)):
         code = q.FORMATS[fmt]
         # 40 decode rows x top-k 2048: one wave of resident CTAs
         assert q.qsa_suggest_num_splits(code, 40, 16, 1, 2048) == max(1, min(16, sms * per_sm // 40))
