@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   };
   // split ring: slot j of this warp (tile i's K in slot 2i mod 3, its V in slot 2i + 1 mod 3)
   const uint32_t ring_u32 = smem_u32(ring);
-  auto slot_addr = [&](int j) -> uint32_t { return ring_u32 + static_cast<uint32_t>(j % 3) * L::kStageBytes; };
+  auto slot_addr = [&](int j) -> uint32_t { return ring_u32 + static_cast<uint32_t>(j) * L::kStageBytes; };
 
   // The query's global loads go out first, then the first tiles' index loads and copies: the
   // copies wait for their indices, and the query's latency overlaps both.
@@ -626,6 +626,7 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   // partial sums (keys e = 0 and e = 1) so that it accumulates with packed adds
   uint64_t l0 = f2pack(0.f, 0.f), l1 = f2pack(0.f, 0.f);
   int eu = -100;                           // int8: 2^eu > every V scale seen
+  int ks = 0;  // split ring: the slot of tile i's K rows, 2i mod 3 (its V rows: the next slot)
   for (int i = 0; i < my; ++i) {
     uint32_t mask_next = 0u;
     if (!F::kSplitRing) {
@@ -649,8 +650,9 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     // where this tile's K rows and scales (kslot) and V rows (vbase + v_row_off) are: one stage,
     // or two slots of the split ring
     const uint32_t sbase = smem_u32(ring + size_t(st) * L::kStageBytes);
-    const uint32_t kslot = F::kSplitRing ? slot_addr(2 * i) : sbase;
-    const uint32_t vslot = F::kSplitRing ? slot_addr(2 * i + 1) : sbase;
+    const uint32_t kslot = F::kSplitRing ? slot_addr(ks) : sbase;
+    const uint32_t vslot = F::kSplitRing ? slot_addr(ks == 2 ? 0 : ks + 1) : sbase;
+    ks = ks == 0 ? 2 : ks - 1;  // (2i + 2) mod 3 for the next tile
     const uint32_t vbase = F::kSplitRing ? vslot - static_cast<uint32_t>(L::kStageV) : sbase;
     const uint32_t mask = (STAGES == 2 || F::kSplitRing) ? mask_cur : lds32(sbase + L::kStageMask);
 
@@ -741,16 +743,6 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     float s[2][4];  // [nt][0..1: head h0 keys e=0,1; 2..3: head h1]
     float vsc[2][2];
     float mx0 = -INFINITY, mx1 = -INFINITY;
-    // int8: the tile's largest |V scale|, as fp32 bits (non-negative floats order as integers):
-    // lane k < 16 reads key k's scale, one warp-wide integer max reduces them
-    uint32_t vmx_bits = 0;
-    if (F::kInt8) {
-      uint32_t vb = 0;
-      if (lane < kKeys) {
-        vb = lds32(kslot + L::kStageKs + (kKeys + lane) * 4);
-      }
-      vmx_bits = __reduce_max_sync(0xffffffffu, vb & 0x7FFFFFFFu);
-    }
     float kscs[2][2];
     bool valids[2][2];
 #pragma unroll
@@ -788,11 +780,6 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
       mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
       mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
-#pragma unroll
-    for (int off = 1; off <= 2; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
     if (F::kSplitRing) {
       // every lane is done with this tile's K slot: the V rows of tile i + 1 go there
       __syncwarp();
@@ -805,15 +792,35 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     float rf0 = 1.f, rf1 = 1.f;  // accumulator factors for heads h0, h1 when rescaling
     {
       // a logit more than 2^kTau above its reference (any valid key when there is none yet), or
-      // an int8 V scale at the bound, moves the reference to the tile's largest ks . (q . k)
-      int ne = eu;
-      if (vmx_bits != 0u) {
-        const int ev = static_cast<int>(vmx_bits >> 23) - 126;
-        if (ev > eu) ne = ev + kEuHeadroom;
+      // an int8 V scale at the bound, moves the reference to the tile's largest ks . (q . k).
+      // int8: the largest |V scale| of this thread's four keys, as fp32 bits (non-negative
+      // floats order as integers); the threads' keys together are the tile's 16
+      uint32_t myv = 0u;
+      if (F::kInt8) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) myv = max(myv, __float_as_uint(vsc[nt][e]) & 0x7FFFFFFFu);
       }
-      const bool up0 = mx0 > kTau, up1 = mx1 > kTau;
+      const bool vup = F::kInt8 && myv != 0u && static_cast<int>(myv >> 23) - 126 > eu;
+      // (this thread's own logits decide whether any head needs a look; the four threads of a
+      // head agree on it inside, from their common maximum)
       rescale = false;
-      if (__any_sync(0xffffffffu, up0 || up1 || ne != eu)) {
+      int ne = eu;
+      if (__any_sync(0xffffffffu, mx0 > kTau || mx1 > kTau || vup)) {
+#pragma unroll
+        for (int off = 1; off <= 2; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const bool up0 = mx0 > kTau, up1 = mx1 > kTau;
+        if (F::kInt8) {  // the new bound from the tile's largest V scale (warp-uniform)
+          const uint32_t vmx_bits = __reduce_max_sync(0xffffffffu, myv);
+          if (vmx_bits != 0u) {
+            const int ev = static_cast<int>(vmx_bits >> 23) - 126;
+            if (ev > eu) ne = ev + kEuHeadroom;
+          }
+        }
         float v0 = -INFINITY, v1 = -INFINITY;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
