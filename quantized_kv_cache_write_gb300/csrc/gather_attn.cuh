@@ -171,7 +171,8 @@ struct Smem {
   static constexpr size_t kStageV = kKArea;
   // split ring (kSplitRing): each warp rotates three slots, each holding one tile's K rows or
   // its V rows, so a tile's K and V need not share a stage; the int8 scales of both tensors
-  // travel with K
+  // travel with K. Tile i's K sits in slot 2i mod 3, its V in slot 2i + 1 mod 3; once tile i is
+  // done, tile i + 1's V goes into its K slot and tile i + 2's K into its V slot
   static constexpr size_t kSlotRows = kKArea > kVArea ? kKArea : kVArea;
   static constexpr size_t kStageKs = F::kSplitRing ? kSlotRows : kStageV + kVArea;
   // deeper rings keep each stage's valid-key mask here (a two-stage ring keeps it in registers)
@@ -780,12 +781,6 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
       mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
       mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
     }
-    if (F::kSplitRing) {
-      // every lane is done with this tile's K slot: the V rows of tile i + 1 go there
-      __syncwarp();
-      if (i + 1 < my) copy_tile(false, true, 0u, kslot - static_cast<uint32_t>(L::kStageV), rec_n1);
-      cp_async_commit();
-    }
 
     // ---- lazy rescale: raise the max in use only past the threshold
     bool rescale;
@@ -927,8 +922,8 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
       const int rows[4] = {key_of<FMT>(0, 2 * c), key_of<FMT>(0, 2 * c + 1), key_of<FMT>(1, 2 * c),
                            key_of<FMT>(1, 2 * c + 1)};
       uint32_t rowV[4];
-      if (F::kSplitRing) {  // V of tile i (K of tile i + 1 and V of tile i + 1 may be in flight)
-        cp_async_wait<2>();
+      if (F::kSplitRing) {  // V of tile i (K of tile i + 1 may be in flight)
+        cp_async_wait<1>();
         __syncwarp();
       }
 #pragma unroll
@@ -1015,8 +1010,11 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
       }
     }
     if (F::kSplitRing) {
-      // every lane is done with this tile's V slot: the K rows of tile i + 2 go there
+      // every lane is done with this tile's slots: the V rows of tile i + 1 go to its K slot, the
+      // K rows of tile i + 2 to its V slot
       __syncwarp();
+      if (i + 1 < my) copy_tile(false, true, 0u, kslot - static_cast<uint32_t>(L::kStageV), rec_n1);
+      cp_async_commit();
       const int c2 = (i + 2 < my) ? (PAGED ? checked_paged(nidx, nblk) : checked(nidx)) : -1;
       const int r2 = rec_of(c2);
       const uint32_t m2 = __ballot_sync(0xffffffffu, c2 >= 0) & 0xFFFFu;
@@ -1035,7 +1033,7 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     } else if (STAGES == 2) {
       mask_cur = mask_next;
     }
-    __syncwarp();
+    if (!F::kSplitRing) __syncwarp();
   }
 
   // ---------------- merge the warps' partial results, one 128-dim half at a time
