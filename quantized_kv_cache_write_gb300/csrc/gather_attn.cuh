@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   // STAGES - 1's entry for the first loop iteration.
   int nidx, nblk = -1, ppos = -1;
   uint32_t mask_cur = 0;  // two-stage ring: valid keys of the tile being computed (bit k = key k)
-  // split ring: tile i + 1's mask and records (its V rows are issued during tile i)
+  // split ring: tile i + 1's mask and records (its V rows go out once tile i is done)
   uint32_t mask_n1 = 0;
   int rec_n1 = -1;
   if (F::kSplitRing) {
