@@ -479,6 +479,16 @@ qkv_status qsa_gather_attn_paged(const void* q, int64_t rows, int num_q_heads, i
  *               zero before the first call (cudaMemset); every launch leaves it zero again.
  *               One launch at a time per sched buffer. NULL with that engine: QKV_ERR_ARG;
  *               not 4-byte aligned: QKV_ERR_ALIGN.
+ *   shard       0, or 1: this pool is one shard of a pool split by slot range. It holds the
+ *               global slots [slot_lo, slot_lo + num_slots) at local ids 0 .. num_slots - 1;
+ *               topk_idx holds global slot ids, and an entry outside the shard's range is
+ *               another shard's: skipped, not flagged (entries below -1 are still flagged).
+ *               The output (out / lse, or the partials) is this shard's normalised partial and
+ *               its lse: qsa_splitk_merge over the shards' partials gives the attention over the
+ *               whole pool (the E4M3 V scale is applied inside each shard's unsplit output, so
+ *               the cross-shard merge takes v_scale_post = 1). Not with a block table or the
+ *               tcgen05 engine (QKV_ERR_ARG / QKV_ERR_UNSUPPORTED); any other value: QKV_ERR_ARG.
+ *   slot_lo     shard only: the first global slot id of this shard, 0 <= slot_lo <= 2^31 - 1.
  */
 #define QSA_ENGINE_DEFAULT 0
 #define QSA_ENGINE_TCGEN05 1
@@ -518,6 +528,8 @@ typedef struct {
   uint32_t* counters;
   int engine;
   uint32_t* sched;
+  int shard;
+  int64_t slot_lo;
 } qsa_gather_desc;
 
 qkv_status qsa_gather_attn_ex(const qsa_gather_desc* desc, void* stream);

@@ -75,7 +75,7 @@ class GatherDesc(ctypes.Structure):
                 ("num_splits", _i32), ("out", _p), ("lse", _p), ("o_part", _p), ("lse_part", _p),
                 ("dev_status", _p), ("topk_len", _p), ("block_table", _p), ("num_seqs", _i64),
                 ("max_blocks", _i32), ("block_size", _i32), ("row_seq", _p), ("counters", _p),
-                ("engine", _i32), ("sched", _p)]
+                ("engine", _i32), ("sched", _p), ("shard", _i32), ("slot_lo", _i64)]
 
 
 lib.qsa_gather_attn_ex.argtypes = [ctypes.POINTER(GatherDesc), _p]
@@ -336,7 +336,7 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
                        k_scale_layer: float = 1.0, v_scale_layer: float = 1.0, num_splits: int = 1, out=None,
                        lse=None, o_part=None, lse_part=None, dev_status=None, topk_len=None, block_table=None,
                        row_seq=None, block_size: int = 0, counters=None, engine: int = 0, sched=None,
-                       stream=None):
+                       slot_lo: Optional[int] = None, stream=None):
     """Any combination of the gather's options in one call (see qsa_gather_attn_ex in qkv.h).
 
     q bf16 or fp16 [R, Hq, D]; topk_len int32 [R] (varlen); block_table int32 [num_seqs,
@@ -344,7 +344,9 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
     counters [R, Hkv, ceil(G / 16)] (fused split-K merge into out / lse); engine
     QSA_ENGINE_TCGEN05 selects the tensor-memory q.K^T variant of the int8 side gather;
     QSA_ENGINE_PERSISTENT runs on a resident grid that takes work items from sched (int32 or
-    uint32 [2], zero on the first call and left zero).
+    uint32 [2], zero on the first call and left zero). slot_lo (not None): this pool is the
+    shard of global slots [slot_lo, slot_lo + num_slots); topk_idx holds global ids and entries
+    of other shards are skipped.
     """
     _check_gather_shapes(q, topk_idx, num_splits, out, lse, o_part, lse_part)
     R, Hq, D = q.shape
@@ -371,6 +373,7 @@ def qsa_gather_attn_ex(q, fmt: int, k_cache, v_cache, topk_idx, softmax_scale: f
     d.out, d.lse, d.o_part, d.lse_part, d.dev_status = _ptr(out), _ptr(lse), _ptr(o_part), _ptr(lse_part), \
         _ptr(dev_status)
     d.topk_len, d.counters, d.engine, d.sched = _ptr(topk_len), _ptr(counters), int(engine), _ptr(sched)
+    d.shard, d.slot_lo = (0, 0) if slot_lo is None else (1, int(slot_lo))
     if block_table is not None:
         d.block_table, d.num_seqs, d.max_blocks, d.block_size = _ptr(block_table), block_table.shape[0], \
             block_table.shape[1], int(block_size)

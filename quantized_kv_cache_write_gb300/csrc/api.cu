@@ -206,7 +206,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
                        float* lse, float* o_part, float* lse_part, uint32_t* dev_status, void* stream,
                        const Paging* pg, uint32_t* counters = nullptr, bool q_f16 = false,
                        const int32_t* topk_len = nullptr, int engine = QSA_ENGINE_DEFAULT,
-                       uint32_t* sched = nullptr) {
+                       uint32_t* sched = nullptr, bool shard = false, int64_t slot_lo = 0) {
   if (rows < 0 || topk < 0 || num_splits < 1 || num_slots < 0) return QKV_ERR_ARG;
   // a 16-bit pool is multiplied in its own type, so it needs a query of that type
   if ((fmt == QKV_F16 && !q_f16) || (fmt == QKV_BF16 && q_f16)) return QKV_ERR_ARG;
@@ -251,6 +251,7 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
     if (sched == nullptr) return QKV_ERR_ARG;
     if (!aligned(sched, 4)) return QKV_ERR_ALIGN;
   }
+  if (shard && (slot_lo < 0 || slot_lo > INT32_MAX || pg != nullptr)) return QKV_ERR_ARG;
   if (pg != nullptr) {
     if (!pg->block_table || !pg->row_seq) return QKV_ERR_ARG;
     if (!aligned(pg->block_table, 4) || !aligned(pg->row_seq, 4)) return QKV_ERR_ALIGN;
@@ -281,6 +282,8 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
   a.dev_status = dev_status;
   a.counters = num_splits > 1 ? counters : nullptr;
   a.sched = engine == QSA_ENGINE_PERSISTENT ? sched : nullptr;
+  a.shard = shard;
+  a.slot_lo = shard ? slot_lo : 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (pg != nullptr) {
     a.block_table = pg->block_table;
@@ -308,7 +311,8 @@ qkv_status gather_impl(const void* q, int64_t rows, int num_q_heads, int num_kv_
     }
   }
   if (engine == QSA_ENGINE_TCGEN05) {
-    if (fmt != QKV_INT8_SIDE || head_dim != 256 || num_q_heads / num_kv_heads > 16 || a.counters != nullptr)
+    if (fmt != QKV_INT8_SIDE || head_dim != 256 || num_q_heads / num_kv_heads > 16 || a.counters != nullptr ||
+        shard)
       return QKV_ERR_UNSUPPORTED;
     return cuda_status(qkv::launch_umma_int8_side(a, s));
   }
@@ -425,6 +429,7 @@ qkv_status qsa_gather_attn_ex(const qsa_gather_desc* d, void* stream) {
   if (d->q_fp16 != 0 && d->q_fp16 != 1) return QKV_ERR_ARG;
   if (d->engine != QSA_ENGINE_DEFAULT && d->engine != QSA_ENGINE_TCGEN05 && d->engine != QSA_ENGINE_PERSISTENT)
     return QKV_ERR_ARG;
+  if (d->shard != 0 && d->shard != 1) return QKV_ERR_ARG;
   const bool paged = d->block_table != nullptr;
   if (!paged && d->row_seq != nullptr) return QKV_ERR_ARG;
   const Paging pg{d->block_table, d->row_seq, d->num_seqs, d->max_blocks, d->block_size};
@@ -432,7 +437,8 @@ qkv_status qsa_gather_attn_ex(const qsa_gather_desc* d, void* stream) {
   return gather_impl(d->q, d->rows, d->num_q_heads, d->num_kv_heads, d->head_dim, d->fmt, d->k_cache, d->v_cache,
                      d->k_scale_tok, d->v_scale_tok, d->k_scale_layer, d->v_scale_layer, d->num_slots, d->topk_idx,
                      d->topk, d->softmax_scale, d->num_splits, d->out, d->lse, d->o_part, d->lse_part, d->dev_status,
-                     stream, paged ? &pg : nullptr, counters, d->q_fp16 != 0, d->topk_len, d->engine, d->sched);
+                     stream, paged ? &pg : nullptr, counters, d->q_fp16 != 0, d->topk_len, d->engine, d->sched,
+                     d->shard != 0, d->slot_lo);
 }
 
 qkv_status qsa_splitk_merge(const float* o_part, const float* lse_part, int64_t rows, int num_q_heads,

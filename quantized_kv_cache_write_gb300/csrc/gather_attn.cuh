@@ -323,9 +323,11 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
   }
   const int my = (ntiles > warp && a.num_slots > 0 && seq_ok) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   const int32_t* idx_row = a.topk_idx + r * a.topk;
-  if (a.num_slots == 0 && a.dev_status != nullptr) {  // no tiles run: still flag every non-padding entry
-    for (int col = col0 + tid; col < col1; col += kThreads)
-      if (__ldg(idx_row + col) != -1) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+  if (a.num_slots == 0 && a.dev_status != nullptr) {  // no tiles run: still flag the bad entries
+    for (int col = col0 + tid; col < col1; col += kThreads) {
+      const int v = __ldg(idx_row + col);
+      if (a.shard ? v < -1 : v != -1) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
+    }
   }
 
   // Start the load of tile i's index of key `lane` (-1 past the split's end). The value is
@@ -336,7 +338,12 @@ __global__ void __launch_bounds__(32 * Fmt<FMT>::kWarps, MINB) gather_attn_kerne
     return col < col1 ? __ldg(idx_row + col) : -1;
   };
   // Entries outside [-1, num_slots) are flagged and become padding.
+  // A shard maps a global slot id to its own local id, and skips other shards' slots.
   auto checked = [&](int v) -> int {
+    if (a.shard && v >= 0) {
+      const int64_t l = static_cast<int64_t>(v) - a.slot_lo;
+      return (l >= 0 && l < a.num_slots) ? static_cast<int>(l) : -1;
+    }
     if (v < -1 || static_cast<int64_t>(v) >= a.num_slots) {
       if (a.dev_status != nullptr) atomicOr(a.dev_status, QKV_DEV_BAD_INDEX);
       v = -1;

@@ -84,6 +84,11 @@ struct GatherArgs {
   // persistent grid: [2] counters (next item, CTAs finished), zero on entry and left zero; the
   // launch then sizes its grid to the CTAs that stay resident. Null = one CTA per item.
   uint32_t* sched = nullptr;
+  // slot-range shard: the pool holds global slots [slot_lo, slot_lo + num_slots) at local ids
+  // 0 .. num_slots - 1; an entry outside that range is another shard's and is skipped (not
+  // flagged). Off: entries are local slot ids, as always.
+  int64_t slot_lo = 0;
+  bool shard = false;
 };
 
 cudaError_t launch_gather_bf16(const GatherArgs& a, cudaStream_t stream);

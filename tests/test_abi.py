@@ -376,6 +376,14 @@ def test_gather_ex_engine_selection_host_validation(lib):
     assert desc(engine=P, sched=None) == E.QKV_ERR_ARG
     assert desc(engine=P, sched=FAKE + 2) == E.QKV_ERR_ALIGN
     assert desc(engine=P, sched=None, rows=0) == E.QKV_OK
+    # a slot-range shard: the flag, its first slot, and the combinations it does not take
+    D0 = E.QSA_ENGINE_DEFAULT
+    assert desc(engine=D0, shard=2) == E.QKV_ERR_ARG
+    assert desc(engine=D0, shard=1, slot_lo=-1) == E.QKV_ERR_ARG
+    assert desc(engine=D0, shard=1, slot_lo=2 ** 31) == E.QKV_ERR_ARG
+    assert desc(engine=D0, shard=1, slot_lo=0, block_table=FAKE, row_seq=FAKE, num_seqs=2, max_blocks=8,
+                block_size=16) == E.QKV_ERR_ARG
+    assert desc(engine=E.QSA_ENGINE_TCGEN05, shard=1, slot_lo=100) == E.QKV_ERR_UNSUPPORTED
 
 
 def test_write_desc_layout_matches_the_header(lib, tmp_path):

@@ -1,8 +1,9 @@
 """A slot-range-sharded pool across two gloo ranks, with the library's own partials (GPU).
 
 Each rank is a separate process with its own CUDA context on the one GPU of this machine. A rank
-writes the pool with the library, attends the entries of each row that fall in its own slot
-range (qsa_gather_attn: a normalised partial and its lse), and the ranks exchange those
+holds only its own slot range, written with the library at local ids, and attends the rows'
+global entries in shard mode (qsa_gather_attn_ex with slot_lo: other ranks' entries are
+skipped; a normalised partial and its lse come out), and the ranks exchange those
 partials with one all_gather over gloo (host tensors). Every rank then merges the gathered
 partials with qsa_splitk_merge and must match the oracle's unsharded attention. The ranks'
 kernels never wait on one another: the only exchange is the host collective between launches.
@@ -40,18 +41,24 @@ def _rank(rank, world, port, fmt, out):
         from gen import small_random
         from harness import GpuPool, OraclePool, act_dev
         torch.cuda.set_device(0)
+        import dataclasses
         wl = small_random(153, num_slots=5000, rows=7, topk=600, pad_frac=0.05, outlier_frac=0.02)
-        gp = GpuPool(wl, fmt)
         R, Hq, D, S = wl.rows, wl.num_q_heads, wl.head_dim, wl.num_slots
         lo, hi = rank * S // world, (rank + 1) * S // world
-        mine = np.where((wl.topk >= lo) & (wl.topk < hi), wl.topk, -1).astype(np.int32)
+        # this rank holds only its own slots, at local ids; the rows keep their global ids
+        sm = wl.slot_mapping
+        local = dataclasses.replace(wl, num_slots=hi - lo, slot_mapping=np.where((sm >= lo) & (sm < hi), sm - lo, -1))
+        gp = GpuPool(local, fmt)
         o = torch.empty((R, Hq, D), dtype=torch.float32, device="cuda")
         lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
-        q.qsa_gather_attn(act_dev(wl.q), gp.code, gp.k_cache, gp.v_cache, torch.from_numpy(mine).cuda(),
-                          wl.softmax_scale, k_scale_tok=gp.k_scale_tok, v_scale_tok=gp.v_scale_tok,
-                          k_scale_layer=float(gp.k_scale_layer), v_scale_layer=float(gp.v_scale_layer),
-                          out=o, lse=lse)
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        q.qsa_gather_attn_ex(act_dev(wl.q), gp.code, gp.k_cache, gp.v_cache,
+                             torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda(), wl.softmax_scale,
+                             num_slots=hi - lo, k_scale_tok=gp.k_scale_tok, v_scale_tok=gp.v_scale_tok,
+                             k_scale_layer=float(gp.k_scale_layer), v_scale_layer=float(gp.v_scale_layer),
+                             out=o, lse=lse, dev_status=status, slot_lo=lo)
         torch.cuda.synchronize()
+        assert status.item() == 0
         # the exchange: every rank's (o, lse) partial, gathered on the host
         o_all = [torch.empty((R, Hq, D), dtype=torch.float32) for _ in range(world)]
         l_all = [torch.empty((R, Hq), dtype=torch.float32) for _ in range(world)]
