@@ -11,8 +11,9 @@
 // One warp owns one (token, head) row of K or V, or both rows when the write is large: 32 lanes
 // x 8 values = a 256-wide head vector, read as one coalesced line (head_dim 128: lanes 16..31
 // idle); the absmax is a 5-step shuffle reduction; the codes leave as one coalesced line.
-// Division is IEEE (__fdiv_rn) and rounding is round-to-nearest-even, so the stored bytes
-// equal a plain fp32 reference bit for bit.
+// Every code is the one the IEEE quotient fl(x / scale) rounds to (round-to-nearest-even), so
+// the stored bytes equal a plain fp32 reference bit for bit; int8 takes the division itself
+// only where a bracket of two multiplications cannot decide (see bracket_lo / bracket_hi).
 #include <atomic>
 
 #include "qkv_internal.cuh"
@@ -53,6 +54,23 @@ __device__ __forceinline__ HeadVec widen8(const uint4& raw) {
   }
   return h;
 }
+
+// int8 codes without a division per value. With r = fl(1 / s), the exact products
+// x fl(r (1 -+ 2^-20)) lie below and above the IEEE quotient fl(x / s): the roundings of r and
+// of r (1 -+ 2^-20) each move a value by at most 2^-24 of itself, so both products differ from
+// x / s by more than 2^-22 of it, on opposite sides, and fl(x / s) by at most 2^-24. Rounding to
+// an integer is monotonic, so where both products round to the same integer, fl(x / s) rounds to
+// it as well; otherwise (x / s within about 2^-20 of a half-integer, a few values in 10^4) the
+// division decides. This holds while r is a finite normal float: scales in [2^-100, 2^100];
+// other scales always divide. (E4M3 keeps its division: a bracket there takes two conversions
+// per pair instead of one, which measured slower than the divisions.)
+constexpr float kBracket = 9.5367431640625e-07f;  // 2^-20
+__device__ __forceinline__ bool bracket_ok(float s) { return s >= 7.8886090522101181e-31f && s <= 1.2676506002282294e30f; }
+__device__ __forceinline__ float bracket_lo(float s) { return __fmul_rn(__frcp_rn(s), 1.0f - kBracket); }
+__device__ __forceinline__ float bracket_hi(float s) { return __fmul_rn(__frcp_rn(s), 1.0f + kBracket); }
+// RN(y + 1.5 2^23) holds rint(y), ties to even, in its low mantissa bits for |y| < 2^22; its low
+// byte is the code's two's complement byte
+constexpr float kRintMagic = 12582912.0f;
 
 __device__ __forceinline__ float warp_max(float a) {
 #pragma unroll
@@ -142,10 +160,17 @@ __device__ __forceinline__ void store_int8_row(const HeadVec& hv, int lane, bool
   const float scale = __fdiv_rn(a, 127.0f);
   uint32_t word[2] = {0u, 0u};
   if (scale > 0.f) {
+    // |x| <= amax and scale = fl(amax / 127) keep |x / scale| below 127.5, so the clamp never
+    // acts on a finite value (a NaN value fails the bracket test and takes the clamped division)
+    const bool br = bracket_ok(scale);
+    const float rlo = bracket_lo(scale), rhi = bracket_hi(scale);
     uint32_t c[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      c[i] = static_cast<uint32_t>(max(-127, min(127, __float2int_rn(__fdiv_rn(hv.x[i], scale)))));
+    for (int i = 0; i < 8; ++i) {
+      const float lo = __fmaf_rn(hv.x[i], rlo, kRintMagic), hi = __fmaf_rn(hv.x[i], rhi, kRintMagic);
+      c[i] = (br && lo == hi) ? __float_as_uint(lo)
+                              : static_cast<uint32_t>(max(-127, min(127, __float2int_rn(__fdiv_rn(hv.x[i], scale)))));
+    }
     // low bytes of c[4w .. 4w + 3] into word w, c[4w] lowest: two byte permutes per pair, one
     // to join the pairs
 #pragma unroll
