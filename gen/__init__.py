@@ -10,6 +10,7 @@ from .workloads import (  # noqa: F401
     f32_to_bf16_bits,
     f32_to_f16_bits,
     bulk_tail_decode,
+    cancelling_pairs,
     long_context_decode,
     mixed_catchup_decode,
     page1_shape,

@@ -345,6 +345,52 @@ def small_paged(seed: int, num_seqs: int = 3, max_blocks: int = 6, block_size: i
                     block_table=table, row_seq=row_seq, topk_pos=pos, block_size=block_size,
                     notes="paged rows only: slot ids come from the block table")
 
+def cancelling_pairs(seed: int = 8, rows: int = 32, background: int = 300, num_slots: int = 8192,
+                     pair_gain: float = 4.0, v_gain: float = 16.0) -> Workload:
+    """Rows whose output is a near cancellation of two outlier keys.
+
+    Row r gathers its own pair of tokens A_r, B_r plus `background` distinct ordinary tokens,
+    in random order. A_r's K is pair_gain x a normal vector and B_r's K equals it, except that
+    one coordinate is scaled by (1 + eps), eps cycling through 0, 2^-7, 2^-5 and 2^-3 (an
+    exact tie, then ever larger gaps). Their V vectors are v_gain x a normal vector and its
+    exact negation. Every head's q is A_r's K times 16 L / |K|^2 plus N(0, 0.2) noise, so the
+    pair's logits sit ~L above the rest (softmax scale 1/16), L = 8 (the other keys still
+    count) or 40 (only the pair does; outlier keys reach such logits on the pages' data,
+    gain 16 x a normal vector against a normal q). The output is the small difference of two
+    large, nearly equal terms: only logits accurate to ~1e-6 keep it within 5e-5, and at
+    L = 40 the rounding of an fp32 logit alone exceeds that.
+    """
+    S, H, G, D = num_slots, 1, 16, HEAD_DIM
+    T = S
+    rng = np.random.default_rng(seed)
+    k = _normals(rng, (T, H, D))
+    v = _normals(rng, (T, H, D))
+    eps = np.array([0.0, 2.0 ** -7, 2.0 ** -5, 2.0 ** -3], dtype=np.float32)
+    q = np.empty((rows, H * G, D), dtype=np.float32)
+    for r in range(rows):
+        a, b = 2 * r, 2 * r + 1
+        k[a] *= np.float32(pair_gain)
+        k[b] = k[a]
+        d = int(rng.integers(D))
+        k[b, 0, d] = k[a, 0, d] * (np.float32(1.0) + eps[r % eps.size])
+        v[a] *= np.float32(v_gain)
+        v[b] = -v[a]
+        ka = k[a, 0]
+        gap = 8.0 if (r // eps.size) % 2 == 0 else 40.0
+        q[r] = ka[None, :] * np.float32(16.0 * gap / float(ka @ ka)) + np.float32(0.2) * rng.standard_normal(
+            (H * G, D), dtype=np.float32)
+    slot_mapping = rng.permutation(S).astype(np.int64)
+    idx = np.empty((rows, background + 2), dtype=np.int32)
+    for r in range(rows):
+        others = 2 * rows + rng.choice(T - 2 * rows, size=background, replace=False)
+        toks = rng.permutation(np.concatenate([[2 * r, 2 * r + 1], others]))
+        idx[r] = slot_mapping[toks]
+    return Workload(f"cancelling outlier pairs (S={S}, R={rows}, k={background + 2})", seed, S, H, H * G, D,
+                    f32_to_bf16_bits(k), f32_to_bf16_bits(v), slot_mapping, f32_to_bf16_bits(q), idx,
+                    softmax_scale=1.0 / 16.0,
+                    notes="pair tokens 2r, 2r + 1 per row r; K_B = K_A up to one coordinate, V_B = -V_A")
+
+
 def mixed_catchup_decode(seed: int = 6, catchup_rows: int = 46, catchup_start: int = 64,
                          decode_rows: int = 3, decode_context: int = 8192, topk: int = 2051,
                          num_slots: int = 131072) -> Workload:
