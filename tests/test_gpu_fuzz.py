@@ -2,7 +2,8 @@
 
 Each case draws a pool layout, head dim, GQA group, KV-head count, row count, top-k width,
 padding and outlier fractions, per-row lengths (or none), a split count, the fused merge (or
-the separate merge) and an engine, then checks every output and lse element within
+the separate merge), an engine and the query type (bf16, or fp16 with fp16 tokens written
+into the pool), then checks every output and lse element within
 |gpu - ref| <= 5e-5 + 1e-3 |ref| and that nothing was flagged. The draws are seeded, so a
 failure names a reproducible configuration.
 """
@@ -39,15 +40,22 @@ def _draw(seed):
         engine = "persistent"
     elif fmt == "int8_side" and hd == 256 and g <= 16 and not fused and rng.integers(3) == 0:
         engine = "tcgen05"
+    seed = int(rng.integers(1 << 30))
+    # the query type, drawn last so that the draws above stay as they were: an unquantised pool
+    # takes a query of its own type; int8 and E4M3 pools take either (the FP16-activation
+    # contract), except on the tcgen05 engine (bf16 queries only)
+    act = "f16" if fmt == "f16" else "bf16"
+    if fmt in ("int8_side", "int8_inline", "e4m3") and engine != "tcgen05" and rng.integers(3) == 0:
+        act = "f16"
     return dict(fmt=fmt, hd=hd, hkv=hkv, g=g, rows=rows, topk=topk, P=P, fused=fused, varlen=varlen, pad=pad,
-                outl=outl, engine=engine, seed=int(rng.integers(1 << 30)))
+                outl=outl, engine=engine, seed=seed, act=act)
 
 
 @pytest.mark.parametrize("case", range(96))
 def test_random_configuration(case):
     import quantized_kv_cache_write_gb300 as q
     c = _draw(case)
-    act = "f16" if c["fmt"] == "f16" else "bf16"
+    act = c["act"]
     wl = small_random(c["seed"], num_slots=3000, rows=c["rows"], topk=c["topk"], num_q_heads=c["g"] * c["hkv"],
                       num_kv_heads=c["hkv"], pad_frac=c["pad"], outlier_frac=c["outl"], act_dtype=act,
                       head_dim=c["hd"])
