@@ -15,7 +15,9 @@
 // memory.
 //
 // Gathering: 16 B cp.async copies, consecutive lanes on consecutive chunks of a row (whole
-// lines per request), into a two-stage ring per warp. The rows' placement keeps every
+// lines per request), into a ring per warp: two full K + V stages (E4M3), or three half-stage
+// slots that K and V rows rotate through (int8 and 16-bit pools, see kSplitRing). Inline int8
+// records, 4 B-aligned only, go by 4 B copies into the same places. The rows' placement keeps every
 // fragment read below bank-conflict free: odd K rows sit 64 B (bf16: 16 B) further along the
 // bank cycle than even ones, and V row r lands in one of 8 regions whose start rotates with r.
 // (Bulk copies on the TMA engine, one 256 B row each, were measured slower on this access
@@ -35,7 +37,8 @@
 // Per 16-key tile and warp:
 //   q.K^T  mma.sync m16n8k16, M = the GQA group (16 query heads, padded), N = 8 keys, K = 16
 //          head dims. Query fragments come from shared memory (ldmatrix; staged once per CTA
-//          as fp16 with a per-head power of two, bf16 for the bf16 layout). Key codes are
+//          as fp16 with a per-head power of two, bf16 for the bf16 layout; int8 layouts stage
+//          it twice, q_hi and q_lo, for an exact q_hi . c -- see Fmt::kQSplit). Key codes are
 //          dequantised straight into B fragments (int8 -> fp16 by an exponent splice, E4M3 ->
 //          fp16 by the native cvt, bf16 as stored); the head-dim order inside a fragment
 //          follows how a code word unpacks and the staged query uses the same permutation.
@@ -44,7 +47,7 @@
 //          exceeds it by more than 2^8 (log2 domain), so the accumulators are rescaled a few
 //          times per row rather than every tile; p <= 2^8 is sized for that.
 //   p.V    p comes straight from the q.K^T accumulators (the m16n8 C layout of two N-tiles is
-//          the m16k16 A layout) as an fp16 hi + lo pair (bf16 pair for the bf16 layout): with
+//          the m16k16 A layout) as an fp16 hi + lo pair (three bf16 parts for the bf16 layout): with
 //          outlier tokens a row can be a near-even mix of two large V rows of opposite sign,
 //          and single-fp16 p would lose ~1e-3 of the result to cancellation. int8 p also
 //          carries the slot's V scale and a power of two keeping it a normal fp16. HD / 8
