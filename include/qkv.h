@@ -29,7 +29,8 @@
  *                       little-endian (the 260 B record of [INT8-PR]; 132 B for D = 128)
  *       QKV_E4M3        K, V: E4M3 bytes [S, H, D]; one fp32 K and one fp32 V scale per layer
  *       QKV_F16         K, V: IEEE half [S, H, D] (the unquantised cache of the FP16-activation
- *                       contract; gathered by qsa_gather_attn_f16 only)
+ *                       contract; gathered with an fp16 query only: qsa_gather_attn_f16, or
+ *                       qsa_gather_attn_ex with q_fp16 set)
  *   - Activations (q and new K/V tokens) are bf16; the *_f16 entry points take IEEE half
  *     instead, for the FP16-activation contract of [E4M3-PR §Purpose]. Widening is exact either way.
  */
