@@ -12,6 +12,7 @@ flush (a 256 MiB write), and synchronises. Profile the last launch with
                      QSA path", §The finding worth upstreaming)
   page1_tcgen05      the same, int8 side, QSA_ENGINE_TCGEN05
   page1_gqa32        the same, int8 side, 32 query heads on one KV head
+  page1_hd128        the same, int8 side, head_dim 128 (128 B of codes per head row)
   e4m3_layer         one calibrated E4M3 layer: 64 rows x top-k 2051 over 131072 slots, fused
                      split-K at qsa_suggest_num_splits' count ("[Perf][SM70][FP8] Hoist QSA
                      E4M3 KV scales", §Combined SM70 validation provenance)
@@ -40,7 +41,7 @@ from gen import (chunked_prefill, e4m3_splitk_layer, long_context_decode, mixed_
                  page1_shape, small_random)
 
 CASES = ["page1_int8_side", "page1_int8_inline", "page1_e4m3", "page1_bf16", "page1_tcgen05", "page1_gqa32",
-         "e4m3_layer", "long_context", "mixed_default", "mixed_persistent", "chunked_prefill"]
+         "page1_hd128", "e4m3_layer", "long_context", "mixed_default", "mixed_persistent", "chunked_prefill"]
 
 
 def _dev(bits):
@@ -84,6 +85,9 @@ def build(case: str):
         what = case[len("page1_"):]
         if what == "gqa32":
             wl, fmt = small_random(11, num_slots=262144, rows=2048, topk=1024, outlier_frac=0.01, num_q_heads=32), \
+                "int8_side"
+        elif what == "hd128":
+            wl, fmt = small_random(11, num_slots=262144, rows=2048, topk=1024, outlier_frac=0.01, head_dim=128), \
                 "int8_side"
         else:
             wl, fmt = page1_shape(1, with_step=False), ("int8_side" if what == "tcgen05" else what)
