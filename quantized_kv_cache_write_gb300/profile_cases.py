@@ -1,4 +1,4 @@
-"""One named gather case, launched a few times: the command a profiler wraps.
+"""One named case of the library's kernels, launched a few times: the command a profiler wraps.
 
     python -m quantized_kv_cache_write_gb300.profile_cases <case> [--launches N]
 
@@ -23,6 +23,10 @@ flush (a 256 MiB write), and synchronises. Profile the last launch with
                      cache", §Targeted mixed-batch scheduler regression)
   chunked_prefill    8192 causal rows (row i attends min(1024, i) of the 8192 tokens just
                      written into a 524288-slot int8 side pool), varlen
+  write_<fmt>_fill   the page-1 pool fill: 262144 bf16 tokens written into a 262144-slot pool,
+                     fmt = int8 (side tensors) or e4m3 (calibrated scales)
+  merge_e4m3_layer   qsa_splitk_merge of the E4M3 layer's split partials (64 rows, 16 heads, P
+                     from qsa_suggest_num_splits), the separate-merge path
 """
 
 from __future__ import annotations
@@ -41,7 +45,8 @@ from gen import (chunked_prefill, e4m3_splitk_layer, long_context_decode, mixed_
                  page1_shape, small_random)
 
 CASES = ["page1_int8_side", "page1_int8_inline", "page1_e4m3", "page1_bf16", "page1_tcgen05", "page1_gqa32",
-         "page1_hd128", "e4m3_layer", "long_context", "mixed_default", "mixed_persistent", "chunked_prefill"]
+         "page1_hd128", "e4m3_layer", "long_context", "mixed_default", "mixed_persistent", "chunked_prefill",
+         "write_int8_fill", "write_e4m3_fill", "merge_e4m3_layer"]
 
 
 def _dev(bits):
@@ -134,6 +139,35 @@ def build(case: str):
         out = torch.empty((wl.rows, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device="cuda")
         return lambda: q.qsa_gather_attn_varlen(qd, q.QKV_INT8_SIDE, kc, vc, idx, lens, wl.softmax_scale, out=out,
                                                 **kw)
+    if case in ("write_int8_fill", "write_e4m3_fill"):
+        wl = page1_shape(1, with_step=False)
+        S, H, D = wl.num_slots, wl.num_kv_heads, wl.head_dim
+        k, v, slots = _dev(wl.k_tokens), _dev(wl.v_tokens), torch.from_numpy(wl.slot_mapping).cuda()
+        kc = torch.zeros((S, H, D), dtype=torch.int8 if case == "write_int8_fill" else torch.uint8, device="cuda")
+        vc = torch.zeros_like(kc)
+        if case == "write_int8_fill":
+            ks = torch.zeros((S, H), dtype=torch.float32, device="cuda")
+            vs = torch.zeros_like(ks)
+            return lambda: q.qkv_write_int8(k, v, slots, kc, vc, ks, vs)
+        amax = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sc = torch.zeros(2, dtype=torch.float32, device="cuda")
+        q.qkv_e4m3_calibrate(k, amax, sc[0:1])
+        q.qkv_e4m3_calibrate(v, amax, sc[1:2])
+        ksl, vsl = sc.tolist()
+        return lambda: q.qkv_write_e4m3(k, v, slots, kc, vc, ksl, vsl)
+    if case == "merge_e4m3_layer":
+        wl = e4m3_splitk_layer(0)
+        kc, vc, kw = _pool(wl, "e4m3")
+        qd, idx = _dev(wl.q), torch.from_numpy(np.ascontiguousarray(wl.topk, dtype=np.int32)).cuda()
+        R, Hq, D = wl.rows, wl.num_q_heads, wl.head_dim
+        P = q.qsa_suggest_num_splits(q.QKV_E4M3, R, Hq, wl.num_kv_heads, wl.topk.shape[1])
+        o_part = torch.empty((R, P, Hq, D), dtype=torch.float32, device="cuda")
+        lse_part = torch.empty((R, P, Hq), dtype=torch.float32, device="cuda")
+        q.qsa_gather_attn(qd, q.QKV_E4M3, kc, vc, idx, wl.softmax_scale, num_splits=P, o_part=o_part,
+                          lse_part=lse_part, **kw)
+        out = torch.empty((R, Hq, D), dtype=torch.float32, device="cuda")
+        lse = torch.empty((R, Hq), dtype=torch.float32, device="cuda")
+        return lambda: q.qsa_splitk_merge(o_part, lse_part, out, lse, v_scale_post=float(kw["v_scale_layer"]))
     raise SystemExit(f"unknown case {case!r}; one of {', '.join(CASES)}")
 
 
