@@ -44,6 +44,7 @@
 #pragma once
 
 #include <atomic>
+#include <cstdlib>
 #include "qkv_internal.cuh"
 
 namespace qkv {
@@ -139,9 +140,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t mbar) {
 __device__ __forceinline__ void mbar_arrive_cp(uint32_t mbar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(mbar) : "memory");
 }
-// Wait for the phase with the given parity to complete; false if the poll limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-  for (uint32_t it = 0; it < kWaitLimit; ++it) {
+// Wait for the phase with the given parity to complete; false if `limit` polls ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint32_t limit) {
+  for (uint32_t it = 0; it < limit; ++it) {
     uint32_t ok;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -250,8 +251,13 @@ __device__ __forceinline__ Cursor cursor_next_item(const GatherArgs& a, Cursor c
   return c;
 }
 
+// wait_limit: mbarrier polls before a wait is declared lost (kWaitLimit). drop_tk: the block
+// whose K hand-off to the MMA warp the compute warps leave out, -1 for none -- a test of the
+// lost-wait path (see launch); with it, the MMA warp's wait for that block and the compute
+// warps' wait for its scores both run out, and the CTA winds down with QKV_DEV_TIMEOUT set.
 template <int FMT>
-__global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherArgs a, int64_t num_items) {
+__global__ void __launch_bounds__(kThreads, 1)
+    umma_gather_kernel(const GatherArgs a, int64_t num_items, uint32_t wait_limit, int64_t drop_tk) {
   static_assert(FMT == QKV_INT8_SIDE, "int8 pool with side-tensor scales");
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
         if (kb >= kStages) {
           int stop = 0;
           if (lane == 0) {
-            if (!mbar_wait(sb + kBarKEmpty + 8 * st, static_cast<uint32_t>((kb / kStages - 1) & 1))) *sFlag = 1u;
+            if (!mbar_wait(sb + kBarKEmpty + 8 * st, static_cast<uint32_t>((kb / kStages - 1) & 1), wait_limit)) *sFlag = 1u;
             stop = *sFlag != 0u;
           }
           if (__shfl_sync(0xffffffffu, stop, 0)) { ok = false; break; }
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
         if (vb >= kStages) {
           int stop = 0;
           if (lane == 0) {
-            if (!mbar_wait(sb + kBarVEmpty + 8 * st, static_cast<uint32_t>((vb / kStages - 1) & 1))) *sFlag = 1u;
+            if (!mbar_wait(sb + kBarVEmpty + 8 * st, static_cast<uint32_t>((vb / kStages - 1) & 1), wait_limit)) *sFlag = 1u;
             stop = *sFlag != 0u;
           }
           if (__shfl_sync(0xffffffffu, stop, 0)) { ok = false; break; }
@@ -392,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
       int64_t gk = 0;
       for (; c.it < num_items; ++gk) {
         const int b = static_cast<int>(gk & 1);
-        if (!mbar_wait(sb + kBarTK + 8 * b, static_cast<uint32_t>((gk >> 1) & 1))) {
+        if (!mbar_wait(sb + kBarTK + 8 * b, static_cast<uint32_t>((gk >> 1) & 1), wait_limit)) {
           *sFlag = 1u;
           break;
         }
@@ -408,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
       }
       // after an abort the compute warps may not wait for the last batch: it completes before the
       // tensor memory it writes is freed
-      if (gk > 0 && *sFlag != 0u) mbar_wait(sb + kBarS + 8 * ((gk - 1) & 1), static_cast<uint32_t>(((gk - 1) >> 1) & 1));
+      if (gk > 0 && *sFlag != 0u)
+        mbar_wait(sb + kBarS + 8 * ((gk - 1) & 1), static_cast<uint32_t>(((gk - 1) >> 1) & 1), wait_limit);
     }
     __syncwarp();
   } else {
@@ -438,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
 
     // thread 0 polls an mbarrier for the compute warps; true when its wait ran out
     auto wait0 = [&](uint32_t mbar, uint32_t parity) -> bool {
-      if (tid == 0 && !mbar_wait(mbar, parity)) {
+      if (tid == 0 && !mbar_wait(mbar, parity, wait_limit)) {
         *sFlag = 1u;
         return true;
       }
@@ -538,7 +545,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
       tmem_fence_before_sync();
       bar_compute();
       if (tid == 0) {
-        mbar_arrive(sb + kBarTK);
+        if (drop_tk != 0) mbar_arrive(sb + kBarTK);
         mbar_arrive(sb + kBarKEmpty);  // block 0's K rows are no longer needed
       }
       cursor_next(a, fcur, num_items, stride);
@@ -576,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_gather_kernel(const GatherAr
         tmem_fence_before_sync();
         bar_compute();
         if (tid == 0) {
-          mbar_arrive(sb + kBarTK + 8 * static_cast<uint32_t>((g + 1) & 1));
+          if (g + 1 != drop_tk) mbar_arrive(sb + kBarTK + 8 * static_cast<uint32_t>((g + 1) & 1));
           mbar_arrive(sb + kBarKEmpty + 8 * fst);  // its K rows are no longer needed
         }
       }
@@ -796,7 +803,21 @@ cudaError_t launch(const GatherArgs& a, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   const int64_t items = a.rows * a.num_kv_heads * a.num_splits;
   const int grid = static_cast<int>(items < sms ? items : sms);
-  umma_gather_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, kSmemTotal, stream>>>(a, items);
+  // Test of the lost-wait path: QKV_TEST_TCGEN05_DROP_HANDOFF=<block> makes the compute warps
+  // leave out that block's K hand-off (read at each launch; unset in any other use). The poll
+  // limit then drops to 2^14, so that the waits run out in milliseconds, not seconds.
+  int64_t drop_tk = -1;
+  uint32_t wait_limit = kWaitLimit;
+  if (const char* t = std::getenv("QKV_TEST_TCGEN05_DROP_HANDOFF")) {
+    char* end = nullptr;
+    const long long b = std::strtoll(t, &end, 10);
+    if (end != t && b >= 0) {
+      drop_tk = b;
+      wait_limit = 1u << 14;
+    }
+  }
+  umma_gather_kernel<FMT><<<static_cast<unsigned>(grid), kThreads, kSmemTotal, stream>>>(a, items, wait_limit,
+                                                                                           drop_tk);
   return cudaGetLastError();
 }
 
