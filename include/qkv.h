@@ -68,7 +68,9 @@ typedef enum {
 #define QKV_DEV_TIMEOUT 4u   /* a gather CTA's bounded wait for its own copies or tensor-core
                                 work ran out (not expected on a healthy GPU): the CTA stopped
                                 early, its outputs are incomplete; the kernel returns instead of
-                                hanging */
+                                hanging. Only the tcgen05 engine waits. A test can make it happen:
+                                QKV_TEST_TCGEN05_DROP_HANDOFF=<block> in the environment drops
+                                that block's hand-off inside each CTA (never set it otherwise) */
 
 /*
  * qkv_write_int8 -- quantize new K/V tokens to int8 with one absmax scale per (token, head)
